@@ -1,0 +1,201 @@
+"""FP64 CPU oracle for paged latent-MLA decode -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never links, loads or calls it,
+and this package imports nothing from the CUDA library: the two share no code.
+
+The arithmetic lives in ``mla_oracle.c`` (plain C, double precision, one (row, head)
+at a time, OpenMP across rows); this module only marshals numpy arrays through ctypes
+and builds the shared object with gcc on first use.
+
+What it computes ("[Kimi-K3 MLA TP8] MLA performance", §2 geometry, §4.1 argument
+table, §5.2 page_size = 1; "Scaling Kimi K3 on AMD Instinct MI355X", §1 DCP merge):
+
+  for request b, query token t < T_b (row r = qo_indptr[b] + t), head h:
+    J     = positions 0 .. L_b - T_b + t        (all L_b positions when T_b = 1)
+    s_j   = sm_scale * q_scale * kv_scale * sum_{d<576} q[r,h,d] * kv[row_j, d]
+    lse   = m + ln sum_j exp(s_j - m),   m = max_j s_j
+    o[c]  = kv_scale * sum_j exp(s_j - lse) * kv[row_j, c],   c < 512
+
+  merge of partials (o_i, lse_i):  M = max lse_i, w_i = exp(lse_i - M),
+    o = sum w_i o_i / sum w_i,  lse = M + ln sum w_i.
+
+Every function has a pin in ``tests/test_oracle_pins.py`` (brute force, closed forms,
+invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libmlaoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+D = 576
+DV = 512
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile mla_oracle.c into oracle/_build/libmlaoracle.so (portable C, no ISA flags)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.mlao_fp8_e4m3fn.restype = ctypes.c_double
+        lib.mlao_fp8_e4m3fn.argtypes = [ctypes.c_uint]
+        lib.mlao_fp8_table.restype = None
+        lib.mlao_fp8_table.argtypes = [_f64p]
+        lib.mlao_attend_one.restype = ctypes.c_int
+        lib.mlao_attend_one.argtypes = [_u8p, _u8p, ctypes.c_int64, _i32p, ctypes.c_int64,
+                                        ctypes.c_double, ctypes.c_double, _f64p, _f64p]
+        lib.mlao_decode.restype = ctypes.c_int
+        lib.mlao_decode.argtypes = [_u8p, ctypes.c_int, _u8p, ctypes.c_int64, _i32p, _i32p,
+                                    _i32p, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                    ctypes.c_double, _f64p, _f64p, ctypes.c_int]
+        lib.mlao_merge.restype = None
+        lib.mlao_merge.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_int64, _f64p, _f64p]
+        lib.mlao_max_threads.restype = ctypes.c_int
+        lib.mlao_max_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def _u8(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("fp8 operands are passed as their raw uint8 bytes")
+    return np.ascontiguousarray(a)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def fp8_e4m3fn_table() -> np.ndarray:
+    """The 256 float8 e4m3fn codes decoded from the format definition (fp64)."""
+    lib = _load()
+    out = np.empty(256, dtype=np.float64)
+    lib.mlao_fp8_table(_ptr(out, _f64p))
+    return out
+
+
+def max_threads() -> int:
+    return int(_load().mlao_max_threads())
+
+
+def attend_one(qvec, kv, rows, sm_scale, q_scale, kv_scale):
+    """One (query row, head): qvec (576,) u8, kv (N, 576) u8, rows (n_att,) int32.
+
+    Returns (o (512,) fp64, lse float).  Scales are taken as given (pass the float32
+    values the kernel sees, converted exactly to Python floats).
+    """
+    lib = _load()
+    qvec = _u8(qvec).reshape(-1)
+    kv = _u8(kv)
+    rows = _i32(rows).reshape(-1)
+    if qvec.size != D or kv.ndim != 2 or kv.shape[1] != D:
+        raise ValueError("qvec must be (576,), kv (N, 576)")
+    o = np.empty(DV, dtype=np.float64)
+    lse = np.empty(1, dtype=np.float64)
+    c = float(sm_scale) * float(q_scale) * float(kv_scale)
+    rc = lib.mlao_attend_one(_ptr(qvec, _u8p), _ptr(kv, _u8p), kv.shape[0],
+                             _ptr(rows, _i32p), rows.size, c, float(kv_scale),
+                             _ptr(o, _f64p), _ptr(lse, _f64p))
+    if rc != 0:
+        raise ValueError(f"oracle attend_one failed with status {rc}")
+    return o, float(lse[0])
+
+
+def decode(q, kv, qo_indptr, kv_indptr, kv_indices, sm_scale, q_scale, kv_scale,
+           n_threads: int = 0):
+    """Whole decode call on host arrays.
+
+    q (sum_T, H, 576) u8; kv (N, 576) u8 (or (N,1,1,576)); indptrs (B+1,) int32;
+    kv_indices (>= kv_indptr[B],) int32.  Returns (o (sum_T, H, 512) fp64,
+    lse (sum_T, H) fp64).
+    """
+    lib = _load()
+    q = _u8(q)
+    if q.ndim != 3 or q.shape[2] != D:
+        raise ValueError("q must be (sum_T, H, 576)")
+    kv = _u8(kv).reshape(-1, D)
+    qo = _i32(qo_indptr)
+    kvp = _i32(kv_indptr)
+    idx = _i32(kv_indices)
+    B = qo.size - 1
+    if kvp.size != B + 1:
+        raise ValueError("qo_indptr and kv_indptr must both have B+1 entries")
+    if idx.size < int(kvp[-1]):
+        raise ValueError("kv_indices shorter than kv_indptr[B]")
+    if int(qo[-1]) != q.shape[0]:
+        raise ValueError("qo_indptr[B] must equal q.shape[0]")
+    n_tok, H = q.shape[0], q.shape[1]
+    o = np.zeros((n_tok, H, DV), dtype=np.float64)
+    lse = np.zeros((n_tok, H), dtype=np.float64)
+    if idx.size == 0:
+        idx = np.zeros(1, dtype=np.int32)
+    rc = lib.mlao_decode(_ptr(q, _u8p), H, _ptr(kv, _u8p), kv.shape[0], _ptr(qo, _i32p),
+                         _ptr(kvp, _i32p), _ptr(idx, _i32p), B, float(sm_scale),
+                         float(q_scale), float(kv_scale), _ptr(o, _f64p), _ptr(lse, _f64p),
+                         int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle decode failed with status {rc}")
+    return o, lse
+
+
+def merge(o_parts, lse_parts):
+    """Merge partials of one output: o_parts (P, W) fp64, lse_parts (P,) fp64."""
+    lib = _load()
+    o_parts = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    lse_parts = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64)).reshape(-1)
+    P = lse_parts.size
+    W = o_parts.size // max(P, 1) if P else 0
+    o = np.empty(max(W, 1), dtype=np.float64)
+    lse = np.empty(1, dtype=np.float64)
+    if P == 0:
+        return np.zeros(0), float("-inf")
+    lib.mlao_merge(_ptr(o_parts, _f64p), _ptr(lse_parts, _f64p), P, W, _ptr(o, _f64p),
+                   _ptr(lse, _f64p))
+    return o[:W].copy(), float(lse[0])
+
+
+def merge_rows(o_parts, lse_parts):
+    """Merge along axis 0 for every trailing row: o_parts (P, R, W), lse_parts (P, R)."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    P, R, W = o_parts.shape
+    o = np.empty((R, W))
+    lse = np.empty(R)
+    for r in range(R):
+        o[r], lse[r] = merge(o_parts[:, r, :], lse_parts[:, r])
+    return o, lse
