@@ -1,0 +1,177 @@
+/*
+ * paged_mla.h -- C ABI of the GB300 (sm_103a) paged latent-MLA decode library.
+ *
+ * The operation is absorbed (latent) multi-head latent attention decode over a paged
+ * FP8 KV cache with page size 1, as captured in "[Kimi-K3 MLA TP8] MLA performance"
+ * (ROCm/aiter issue 4541):
+ *   §2 "K3 MLA geometry": every cached token is one 576-wide latent entry (512 latent +
+ *      64 rope) shared by all query heads; sm_scale = 1/sqrt(192).
+ *   §3 "Entry point": the argument list of the decode call this ABI mirrors, with
+ *      page_size = 1 and a single latent KV head.
+ *   §4.1 / §4.2 argument tables: q and kv_buffer are float8_e4m3fn, q_scale and kv_scale
+ *      are float32 scalars on the device, o is bfloat16 (tokens, heads, 512).
+ *   §5.2: kv_indptr holds per-request token counts (CSR), kv_indices one cache row id per
+ *      token, kv_last_page_lens is all ones.
+ * and the partial-result merge of "Scaling Kimi K3 on AMD Instinct MI355X" §1 "Cache"
+ * (decode context parallelism: partial answers carry normalisation information so that
+ * a softmax-weighted merge is exact) and §4 "MLA" (history split into partitions).
+ *
+ * For request b, query token t < T_b = qo_indptr[b+1]-qo_indptr[b], head h:
+ *   L_b   = kv_indptr[b+1] - kv_indptr[b]
+ *   J     = { j : 0 <= j <= L_b - T_b + t }      (causal within the draft tokens;
+ *                                                  every position when T_b = 1)
+ *   s_j   = sm_scale * q_scale * kv_scale * sum_{d<576} q[r,h,d] * kv[kv_indices[kv_indptr[b]+j], d]
+ *   lse   = ln sum_{j in J} exp(s_j)
+ *   o[c]  = kv_scale * sum_{j in J} exp(s_j - lse) * kv[row_j, c],   c < 512
+ * with r = qo_indptr[b] + t.  An empty J gives o = 0 and lse = -inf.
+ *
+ * Conventions for every entry point
+ *  - Ownership: the caller owns every buffer.  All tensor pointers are DEVICE pointers
+ *    on the current CUDA device.  The library never allocates device memory; scratch
+ *    comes from the caller's workspace.  It keeps only per-device caches of device
+ *    attributes and kernel attributes.
+ *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream) and the
+ *    call returns without waiting, except mla_validate and mla_check_error, which
+ *    synchronise `stream`.
+ *  - Errors: every function returns an mla_status.  Argument errors are detected on the
+ *    host before anything is enqueued.  Errors only visible on the device (an index
+ *    outside the cache, an output row outside `o`, a pipeline wait that timed out) never
+ *    fault or trap the GPU: the offending access is skipped and a bit is set in the
+ *    workspace error word, read by mla_check_error.
+ *  - Strides are in elements.
+ */
+#ifndef PAGED_MLA_H_
+#define PAGED_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA runtime headers. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+    MLA_DTYPE_FP8_E4M3FN = 1, /* 1-byte float8 e4m3fn codes */
+    MLA_DTYPE_BF16 = 2,
+    MLA_DTYPE_FP32 = 3,
+    MLA_DTYPE_INT32 = 4
+} mla_dtype_t;
+
+/* A strided view of device memory.  shape/stride entries past ndim are ignored. */
+typedef struct {
+    void* ptr;
+    int32_t ndim;      /* 0..4 (0 = scalar) */
+    int32_t dtype;     /* mla_dtype_t */
+    int64_t shape[4];
+    int64_t stride[4]; /* in elements */
+} mla_tensor_t;
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,         /* null pointer, wrong dtype/shape/stride, bad size */
+    MLA_ERR_UNSUPPORTED = 2,         /* valid request outside what the kernels implement */
+    MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+    MLA_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed */
+    MLA_ERR_BAD_INDEX = 5,           /* device-side: index or indptr outside its buffer */
+    MLA_ERR_TIMEOUT = 6,             /* device-side: a pipeline wait gave up (no fault) */
+    MLA_ERR_BAD_INPUT = 7            /* mla_validate: indptr not monotone, kv_len < q_len,
+                                        or kv_last_page_lens != 1 */
+} mla_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(int status);
+
+/*
+ * Bytes of workspace mla_decode needs for a call with these sizes.
+ *   batch_size    B (requests)
+ *   num_heads     H (query heads per call: 12, 16, 96 ...)
+ *   max_seqlen_q  largest T_b in the call (1 for plain decode)
+ *   num_kv_splits <= 0: automatic split-KV scheduling; k >= 1: every request is split
+ *                 into exactly k contiguous pieces of its positions (1 = never split)
+ *   num_sms       SM count to plan for; <= 0 queries the current device.
+ * The result is an upper bound for any call with the same (B, H, max_seqlen_q,
+ * num_kv_splits) on that device.  The first 256 bytes of the workspace hold the device
+ * error words and must be zero before first use (mla_check_error clears them again).
+ */
+int mla_get_workspace_size(int32_t batch_size, int32_t num_heads, int32_t max_seqlen_q,
+                           int32_t num_kv_splits, int32_t num_sms, size_t* bytes_out);
+
+/*
+ * Latent-MLA decode.  The first 13 arguments follow the captured decode call (issue §3,
+ * §4.1); the last three are this library's.
+ *   q                 (sum_T, H, 576) FP8_E4M3FN, contiguous; 16-byte aligned.
+ *   kv_buffer         (N_rows, 576) or (N_rows, 1, 1, 576) FP8_E4M3FN; last dim
+ *                     contiguous, row stride a multiple of 16 bytes; 16-byte aligned.
+ *   o                 (sum_T, H, 512) BF16 or FP32, last dim contiguous (written).
+ *   qo_indptr         (B+1,) INT32: query-token CSR; qo_indptr[B] = sum_T.
+ *   kv_indptr         (B+1,) INT32: cache-position CSR in tokens (page_size 1).
+ *   kv_indices        (n,) INT32 with n >= kv_indptr[B]; only [kv_indptr[0], kv_indptr[B])
+ *                     is read.  Entries must lie in [0, N_rows).
+ *   kv_last_page_lens (B,) INT32 or NULL ptr; accepted for interface parity, must be all 1
+ *                     (checked by mla_validate only).
+ *   max_seqlen_q      >= every T_b, 1..64.
+ *   sm_scale          softmax scale (1/sqrt(192) for the captured model).
+ *   q_scale, kv_scale 0-dim (or 1-element) FP32 device tensors: per-tensor dequant scales.
+ *   num_kv_splits     see mla_get_workspace_size.
+ *   lse_out           (sum_T, H) FP32 contiguous, or NULL (not written).
+ *   workspace         device scratch of at least mla_get_workspace_size(...) bytes,
+ *                     256-byte aligned, first 256 bytes zero before first use.
+ * Device-side errors are reported through mla_check_error on the same workspace.
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
+               const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
+               const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
+               int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
+               const mla_tensor_t* kv_scale, int32_t num_kv_splits, const mla_tensor_t* lse_out,
+               void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * Softmax-weighted merge of partial results ("Scaling Kimi K3 on AMD Instinct MI355X",
+ * §1: each partial answer carries its normalisation, so shards merge exactly):
+ *   for output row r < n_out and head h, over the partial rows
+ *   P_r = reduce_idx[reduce_indptr[r] .. reduce_indptr[r+1]):
+ *     M = max lse_parts[i,h];  w_i = exp(lse_parts[i,h] - M)
+ *     o[r,h,:]   = sum w_i o_parts[i,h,:] / sum w_i
+ *     lse[r,h]   = M + ln sum w_i
+ *   Partials with lse = -inf weigh 0; if every partial is -inf (or P_r is empty) the
+ *   row gets o = 0 and lse = -inf.
+ *   o_parts        (P, H, 512) FP32, last dim contiguous
+ *   lse_parts      (P, H) FP32, contiguous
+ *   reduce_indptr  (n_out+1,) INT32;  reduce_idx (m,) INT32 entries in [0, P)
+ *   o              (n_out, H, 512) BF16 or FP32, last dim contiguous (written)
+ *   lse_out        (n_out, H) FP32 contiguous, or NULL
+ * The reduce map lives on the device and is not read by the host; an entry outside
+ * [0, P) is skipped and flagged in `error_word` (an int on the device, may be NULL).
+ */
+int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_parts,
+                       const mla_tensor_t* reduce_indptr, const mla_tensor_t* reduce_idx,
+                       const mla_tensor_t* o, const mla_tensor_t* lse_out, int32_t* error_word,
+                       mla_stream_t stream);
+
+/*
+ * Debug check of a decode call's index inputs on the device, then a host status:
+ * MLA_OK, MLA_ERR_BAD_INPUT (indptr not monotone or not starting at 0 for qo, kv_len <
+ * q_len, kv_last_page_lens != 1, qo_indptr[B] != sum_T) or MLA_ERR_BAD_INDEX (kv_indptr[B]
+ * beyond kv_indices, or an attended index outside [0, N_rows)).  Same arguments as
+ * mla_decode minus the arithmetic ones.  Synchronises `stream`.
+ */
+int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
+                 const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
+                 const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
+                 void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * Synchronises `stream`, returns the first device-side error recorded in the
+ * workspace's error words since the last check (MLA_OK if none) and clears them.
+ */
+int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_MLA_H_ */

@@ -1,0 +1,187 @@
+"""Python binding of the GB300 paged latent-MLA decode library (argument marshalling only).
+
+Every function here has the name of the C entry point it calls in
+``include/paged_mla.h``; each converts torch tensors to ``mla_tensor_t`` descriptors
+(pointer, dtype, shape, strides) and passes the current CUDA stream.  All arithmetic runs
+in the library's CUDA kernels; there is no Python or CPU fallback: if the library cannot
+be loaded, importing this package raises.
+
+The operation ("[Kimi-K3 MLA TP8] MLA performance", §2-§5; "Scaling Kimi K3 on AMD
+Instinct MI355X", §1 and §4): absorbed MLA decode over a page_size=1 FP8 cache, each
+query head scoring every 576-wide latent row, softmax over the request's positions
+(causal within draft tokens), 512-wide BF16 latent output plus optional FP32 lse, and the
+softmax-weighted merge of split-KV or context-shard partials.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MlaError", "mla_decode", "mla_merge_partials", "mla_validate", "mla_check_error",
+    "mla_get_workspace_size", "mla_status_string", "make_workspace", "library_path",
+]
+
+MLA_DTYPE_FP8_E4M3FN = 1
+MLA_DTYPE_BF16 = 2
+MLA_DTYPE_FP32 = 3
+MLA_DTYPE_INT32 = 4
+
+STATUS_NAMES = {
+    0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+    3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_BAD_INDEX",
+    6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_BAD_INPUT",
+}
+
+
+class MlaTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("ndim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.build()   # no-op when the in-tree library is up to date
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(MlaTensor)
+    c_i32, c_sz, vp = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_get_workspace_size.restype = ctypes.c_int
+    lib.mla_get_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
+    lib.mla_decode.restype = ctypes.c_int
+    lib.mla_decode.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, c_sz, vp]
+    lib.mla_merge_partials.restype = ctypes.c_int
+    lib.mla_merge_partials.argtypes = [P, P, P, P, P, P, vp, vp]
+    lib.mla_validate.restype = ctypes.c_int
+    lib.mla_validate.argtypes = [P, P, P, P, P, P, vp, c_sz, vp]
+    lib.mla_check_error.restype = ctypes.c_int
+    lib.mla_check_error.argtypes = [vp, c_sz, vp]
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+_DTYPES = {
+    torch.uint8: MLA_DTYPE_FP8_E4M3FN,           # raw e4m3fn codes
+    torch.float8_e4m3fn: MLA_DTYPE_FP8_E4M3FN,
+    torch.bfloat16: MLA_DTYPE_BF16,
+    torch.float32: MLA_DTYPE_FP32,
+    torch.int32: MLA_DTYPE_INT32,
+}
+
+
+def _desc(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    try:
+        code = _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+    d = MlaTensor()
+    d.ptr = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+    d.ndim = t.dim()
+    d.dtype = code
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream, device):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MlaError(rc, where)
+
+
+def mla_status_string(status: int) -> str:
+    return _lib.mla_status_string(int(status)).decode()
+
+
+def mla_get_workspace_size(batch_size: int, num_heads: int, max_seqlen_q: int = 1,
+                           num_kv_splits: int = 0, num_sms: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.mla_get_workspace_size(batch_size, num_heads, max_seqlen_q, num_kv_splits,
+                                       num_sms, ctypes.byref(out)), "mla_get_workspace_size")
+    return int(out.value)
+
+
+def make_workspace(batch_size: int, num_heads: int, max_seqlen_q: int = 1,
+                   num_kv_splits: int = 0, device=None) -> torch.Tensor:
+    """A zero-initialised device workspace large enough for such calls."""
+    device = torch.device(device or "cuda")
+    with torch.cuda.device(device):
+        n = mla_get_workspace_size(batch_size, num_heads, max_seqlen_q, num_kv_splits)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+
+
+def mla_decode(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+               max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits=0, lse_out=None,
+               workspace=None, stream=None):
+    """Enqueue one decode call (see include/paged_mla.h).  Returns the workspace used."""
+    if workspace is None:
+        workspace = make_workspace(len(kv_indptr) - 1, q.shape[1], max_seqlen_q,
+                                   num_kv_splits, q.device)
+    descs = [_desc(t) for t in (q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
+                                kv_last_page_lens, q_scale, kv_scale, lse_out)]
+    dq, dkv, do, dqo, dkvp, didx, dlast, dqs, dks, dlse = descs
+    rc = _lib.mla_decode(_ref(dq), _ref(dkv), _ref(do), _ref(dqo), _ref(dkvp), _ref(didx),
+                         _ref(dlast), int(max_seqlen_q), float(sm_scale), _ref(dqs), _ref(dks),
+                         int(num_kv_splits), _ref(dlse), ctypes.c_void_p(workspace.data_ptr()),
+                         workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    _check(rc, "mla_decode")
+    return workspace
+
+
+def mla_merge_partials(o_parts, lse_parts, reduce_indptr, reduce_idx, o, lse_out=None,
+                       error_word=None, stream=None):
+    """Softmax-weighted merge of partials with a CSR reduce map (see include/paged_mla.h)."""
+    descs = [_desc(t) for t in (o_parts, lse_parts, reduce_indptr, reduce_idx, o, lse_out)]
+    ew = ctypes.c_void_p(error_word.data_ptr()) if error_word is not None else None
+    rc = _lib.mla_merge_partials(*[_ref(d) for d in descs], ew, _stream(stream, o.device))
+    _check(rc, "mla_merge_partials")
+
+
+def mla_validate(q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                 workspace, stream=None) -> int:
+    """Device-side check of the index inputs; returns the status code (synchronises)."""
+    descs = [_desc(t) for t in (q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens)]
+    return int(_lib.mla_validate(*[_ref(d) for d in descs], ctypes.c_void_p(workspace.data_ptr()),
+                                 workspace.numel(), _stream(stream, q.device)))
+
+
+def mla_check_error(workspace, stream=None) -> int:
+    """First device-side error recorded in the workspace since the last check (clears it)."""
+    return int(_lib.mla_check_error(ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                    _stream(stream, workspace.device)))

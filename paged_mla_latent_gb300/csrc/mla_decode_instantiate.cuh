@@ -1,0 +1,35 @@
+// Shared body of the per-instantiation launcher translation units.
+#pragma once
+
+#include <mutex>
+
+#include "../../include/paged_mla.h"
+#include "mla_decode_launch.h"
+
+namespace pmla {
+
+template <int NG, int STAGES>
+int launch_decode_impl(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
+                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+                       const DecodeParams& prm, int grid, cudaStream_t stream) {
+  using LY = DecodeLayout<NG, STAGES>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(mla_decode_kernel<NG, STAGES>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LY::kSmemBytes) != cudaSuccess)
+        return MLA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  mla_decode_kernel<NG, STAGES><<<grid, 192, LY::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
+                                                                        q_rope, prm);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace pmla

@@ -1,0 +1,536 @@
+// Absorbed (latent) MLA decode over a page_size=1 FP8 cache on sm_103a.
+//
+// What it computes: "[Kimi-K3 MLA TP8] MLA performance" §2 (576-wide latent entry per
+// token shared by every head, sm_scale = 1/sqrt(192)), §4.1 (fp8 q and cache, float32
+// q_scale / kv_scale), §5.2 (page_size 1: one row id per position); softmax partials
+// and their merge: "Scaling Kimi K3 on AMD Instinct MI355X" §1 "Cache" and §4 "MLA".
+//
+// One persistent CTA per SM walks the pieces the scheduler (mla_sched.cuh) gives it.
+// Per tile of 128 cache positions:
+//   producer warp   : loads the 128 row ids, TMA tile::gather4 of the rows into a
+//                     3- (or 2-) stage shared-memory ring.  Latent columns land in four
+//                     128-byte swizzled blocks, rope columns in one 64-byte swizzled
+//                     block.  Positions past the piece gather an out-of-range row and
+//                     read zeros.
+//   MMA thread      : S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
+//                     M = 128 positions, N = NG query rows, K = 576; FP32 in TMEM),
+//                     then O^T[c, n] += V^T[c, pos] . P^T[pos, n] for the four 128-wide
+//                     value blocks (A = the same cache rows read MN-major).
+//   softmax warps   : read S^T from TMEM (one position per thread), scale, mask,
+//                     online softmax in the exp2 domain with a lazily moved reference
+//                     max, and write P as two FP8 planes: hi = e4m3(p) and
+//                     lo = e4m3(256 * (p - hi)), so P reaches the tensor core with
+//                     ~2^-8 relative precision while staying an FP8 x FP8 product.
+//                     At the end of a piece they normalise O and write o / lse (or a
+//                     normalised partial for the merge kernel).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "mla_sched.cuh"
+#include "ptx.cuh"
+
+namespace pmla {
+
+struct DecodeParams {
+  SchedParams sp;
+  const int32_t* kv_indices;
+  int64_t kv_indices_len;
+  int64_t n_kv_rows;
+  int64_t n_q_rows;        // sum_T * H
+  const float* q_scale;
+  const float* kv_scale;
+  float sm_scale;
+  void* o;                 // (sum_T, H, 512), bf16 or fp32
+  int o_fp32;
+  int64_t o_stride_tok;    // elements
+  int64_t o_stride_head;   // elements
+  float* lse_out;          // (sum_T, H) or null
+  float* part_o;           // (slots, NG, 512) normalised partial o (kv_scale applied)
+  float* part_lse;         // (slots, NG) natural-log lse of each partial
+  int64_t n_slots;
+  int* err;
+};
+
+template <int NG, int STAGES>
+struct DecodeLayout {
+  static constexpr int kNPV = 2 * NG;                 // PV N: hi plane + lo plane
+  static constexpr int kStageBytes = kTile * kD;      // 73,728
+  static constexpr int kLatBlock = kTile * 128;       // one 128-column latent block
+  static constexpr int kRopeOff = 4 * kLatBlock;      // rope block inside a stage
+  // P (2*NG rows x 128 positions) fits in the stage's rope block once QK has read it.
+  static constexpr bool kPInRope = kNPV * 128 <= kTile * 64;
+  static constexpr int kQOff = STAGES * kStageBytes;
+  static constexpr int kQBytes = NG * kD;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kPBytes = kPInRope ? 0 : 2 * kNPV * 128;
+  static constexpr int kMiscOff = kPOff + kPBytes;
+  static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 2048;
+  static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
+  // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
+  static constexpr int kSStride = (NG + 31) / 32 * 32;
+  static constexpr int kOBase = 2 * kSStride;
+  static constexpr int kTmemCols = (kOBase + 4 * kNPV <= 256) ? 256 : 512;
+  static_assert(kOBase + 4 * kNPV <= 512, "tensor memory overflow");
+  static_assert(kSmemBytes <= 232448, "shared memory overflow");
+  static_assert(NG % 16 == 0 && NG <= 48, "group rows must be 16, 32 or 48");
+};
+
+// Misc region offsets (bytes from kMiscOff).
+enum : int {
+  kMiscFull = 0,      // full[STAGES]   (8 B each, STAGES <= 4)
+  kMiscEmpty = 32,    // empty[STAGES]
+  kMiscSFull = 64,    // s_full[2]
+  kMiscPFull = 80,    // p_full[2]
+  kMiscPv = 96,       // pv_done
+  kMiscQFull = 104,
+  kMiscQEmpty = 112,
+  kMiscDrain = 120,
+  kMiscTmem = 128,    // u32 tensor memory base
+  kMiscAbort = 132,   // int abort flag
+  kMiscRed = 256,     // float red[4][NG], then float bcast[NG]
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// The reference max moves only when a logit exceeds it by more than kTau (log2 units),
+// so P stays <= 2^kTau = 256 < 448 (e4m3 max) and O is rescaled rarely.
+constexpr float kTau = 8.0f;
+constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
+
+template <int NG, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
+                      const __grid_constant__ CUtensorMap tm_kv_rope,
+                      const __grid_constant__ CUtensorMap tm_q_lat,
+                      const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams prm) {
+  using LY = DecodeLayout<NG, STAGES>;
+  constexpr int NPV = LY::kNPV;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t mbase = sbase + LY::kMiscOff;
+  uint8_t* misc = smem + LY::kMiscOff;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + kMiscTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + kMiscAbort);
+  float* red = reinterpret_cast<float*>(misc + kMiscRed);
+
+  if ((sbase & 1023u) != 0) {   // the swizzled layouts need a 1024-byte aligned window
+    if (threadIdx.x == 0) atomicOr(prm.err, kErrMisaligned);
+    return;
+  }
+
+  PieceIter iter;
+  iter.init(prm.sp, blockIdx.x);
+  {
+    PieceIter probe;
+    probe.init(prm.sp, blockIdx.x);
+    Piece pc;
+    int bad = 0;
+    if (!probe.next(pc, &bad)) {    // no work for this CTA (uniform across the block)
+      if (bad && threadIdx.x == 0) atomicOr(prm.err, kErrBadIndptr);
+      return;
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(mbase + kMiscFull + 8 * s, 1);
+      mbar_init(mbase + kMiscEmpty + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(mbase + kMiscSFull + 8 * s, 1);
+      mbar_init(mbase + kMiscPFull + 8 * s, 4);
+    }
+    mbar_init(mbase + kMiscPv, 1);
+    mbar_init(mbase + kMiscQFull, 1);
+    mbar_init(mbase + kMiscQEmpty, 1);
+    mbar_init(mbase + kMiscDrain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc + kMiscTmem), LY::kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32 * 0) {
+    prefetch_tensormap(&tm_kv_lat);
+    prefetch_tensormap(&tm_kv_rope);
+    prefetch_tensormap(&tm_q_lat);
+    prefetch_tensormap(&tm_q_rope);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sQ = sbase + LY::kQOff;
+  int bad = 0;
+
+  if (warp == 0) {
+    // ===================================================== producer (whole warp)
+    uint32_t it_g = 0;
+    int n_piece = 0;
+    int q_loads = 0;
+    bool aborted = false;
+    Piece pc;
+    const int oob_row = static_cast<int>(prm.n_kv_rows < 0x7FFFFFFF ? prm.n_kv_rows : 0x7FFFFFFF);
+    while (!aborted && iter.next(pc, &bad)) {
+      const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+      if (n_piece > 0 &&
+          !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
+        aborted = true;
+        break;
+      }
+      if (lane == 0) {
+        const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
+        mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
+        tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
+      }
+      ++q_loads;
+      const int64_t kvbase = prm.sp.kv_indptr[pc.b];
+      for (int t = 0; t < nt; ++t, ++it_g) {
+        const int stage = static_cast<int>(it_g % STAGES);
+        const uint32_t use = it_g / STAGES;
+        // row ids of this lane's four positions (before waiting: overlaps the wait)
+        int rowid[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int pos = pc.j0 + t * kTile + 4 * lane + k;
+          int r = oob_row;
+          if (pos < pc.j1) {
+            const int64_t gi = kvbase + pos;
+            if (gi < 0 || gi >= prm.kv_indices_len) {
+              atomicOr(prm.err, kErrBadIndex);
+            } else {
+              const int v = __ldg(prm.kv_indices + gi);
+              if (v < 0 || static_cast<int64_t>(v) >= prm.n_kv_rows)
+                atomicOr(prm.err, kErrBadRowId);
+              else
+                r = v;
+            }
+          }
+          rowid[k] = r;
+        }
+        if (use > 0 &&
+            !mbar_wait(mbase + kMiscEmpty + 8 * stage, (use - 1) & 1, abort_flag, prm.err)) {
+          aborted = true;
+          break;
+        }
+        const uint32_t full = mbase + kMiscFull + 8 * stage;
+        if (lane == 0) mbar_arrive_expect_tx(full, LY::kStageBytes);
+        __syncwarp();
+        const uint32_t st = sbase + stage * LY::kStageBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_gather4(st + c * LY::kLatBlock + lane * 512, &tm_kv_lat, c * 128, rowid[0], rowid[1],
+                      rowid[2], rowid[3], full);
+        tma_gather4(st + LY::kRopeOff + lane * 256, &tm_kv_rope, 512, rowid[0], rowid[1], rowid[2],
+                    rowid[3], full);
+      }
+      ++n_piece;
+    }
+    // Drain: every copy this warp issued must land before the CTA may exit.
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        if (it_g > static_cast<uint32_t>(s)) {
+          const uint32_t last_use = (it_g - 1 - s) / STAGES;
+          mbar_wait_drain(mbase + kMiscFull + 8 * s, last_use & 1);
+        }
+      }
+      if (q_loads > 0) mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
+      constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, false);
+      uint32_t it_g = 0;
+      int n_piece = 0;
+      bool aborted = false;
+      Piece pc;
+      auto issue_pv = [&](uint32_t i, bool first_of_piece) -> bool {
+        const int sb = i & 1;
+        const int stage = static_cast<int>(i % STAGES);
+        if (!mbar_wait(mbase + kMiscPFull + 8 * sb, (i >> 1) & 1, abort_flag, prm.err)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + stage * LY::kStageBytes;
+        const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * 128;
+#pragma unroll
+        for (int bk = 0; bk < 4; ++bk) {
+          const uint32_t d = tmem + LY::kOBase + bk * NPV;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
+            const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
+            // B = P: NPV rows x 32 positions (K-major, 128-byte swizzle)
+            const uint64_t b = smem_desc(pbuf + kk * 32, 16, 1024, kSw128);
+            mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit(mbase + kMiscEmpty + 8 * stage);
+        mma_commit(mbase + kMiscPv);
+        return true;
+      };
+      while (!aborted && iter.next(pc, &bad)) {
+        const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+        if (!mbar_wait(mbase + kMiscQFull, n_piece & 1, abort_flag, prm.err)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        for (int t = 0; t < nt; ++t, ++it_g) {
+          const int stage = static_cast<int>(it_g % STAGES);
+          const uint32_t use = it_g / STAGES;
+          if (!mbar_wait(mbase + kMiscFull + 8 * stage, use & 1, abort_flag, prm.err)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + stage * LY::kStageBytes;
+          const uint32_t d = tmem + (it_g & 1) * LY::kSStride;
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {   // latent columns 0..511, 32 per MMA
+            const uint64_t a = smem_desc(st + (kk >> 2) * LY::kLatBlock + (kk & 3) * 32, 16, 1024, kSw128);
+            const uint64_t b = smem_desc(sQ + (kk >> 2) * NG * 128 + (kk & 3) * 32, 16, 1024, kSw128);
+            mma_f8(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {    // rope columns 512..575
+            const uint64_t a = smem_desc(st + LY::kRopeOff + kk * 32, 16, 512, kSw64);
+            const uint64_t b = smem_desc(sQ + 4 * NG * 128 + kk * 32, 16, 512, kSw64);
+            mma_f8(d, a, b, idesc_qk, 1u);
+          }
+          mma_commit(mbase + kMiscSFull + 8 * (it_g & 1));
+          if (t == nt - 1) mma_commit(mbase + kMiscQEmpty);
+          if (t > 0 && !issue_pv(it_g - 1, t == 1)) {
+            aborted = true;
+            break;
+          }
+        }
+        if (aborted) break;
+        if (!issue_pv(it_g - 1, nt == 1)) {
+          aborted = true;
+          break;
+        }
+        ++n_piece;
+      }
+      // Drain: all MMAs must complete before tensor memory is released.
+      mma_commit(mbase + kMiscDrain);
+      mbar_wait_drain(mbase + kMiscDrain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ===================================================== softmax + epilogue (4 warps)
+    const int q4 = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int prow = 32 * q4 + lane;         // position within the tile == TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const float kv_scale = *prm.kv_scale;
+    const float scale_log2 = prm.sm_scale * (*prm.q_scale) * kv_scale * kLog2e;
+    const int H = prm.sp.H;
+    // byte offsets of this position's column inside the 8 rows of a swizzle atom
+    uint32_t poff[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      poff[r] = r * 128 + ((((prow >> 4) ^ r) & 7) << 4) + (prow & 15);
+
+    uint32_t it_g = 0;
+    Piece pc;
+    float m_ref[NG];
+    float l_acc[NG];
+    while (iter.next(pc, &bad)) {
+      const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+#pragma unroll
+      for (int n = 0; n < NG; ++n) {
+        m_ref[n] = -INFINITY;
+        l_acc[n] = 0.f;
+      }
+      const int causal_from = pc.L - pc.T;   // positions beyond this need the causal test
+      for (int t = 0; t < nt; ++t, ++it_g) {
+        const int sb = it_g & 1;
+        mbar_wait(mbase + kMiscSFull + 8 * sb, (it_g >> 1) & 1, abort_flag, prm.err);
+        tc_fence_after();
+        float x[NG];
+#pragma unroll
+        for (int c = 0; c < NG / 16; ++c) tmem_ld16(tl + sb * LY::kSStride + 16 * c, x + 16 * c);
+        tmem_wait_ld();
+
+        const int pos = pc.j0 + t * kTile + prow;
+        const bool in_piece = pos < pc.j1;
+        bool exceed = false;
+#pragma unroll
+        for (int n = 0; n < NG; ++n) {
+          float v = in_piece ? x[n] * scale_log2 : -INFINITY;
+          if (in_piece && pos > causal_from) {
+            const int tq = (pc.g * NG + n) / H;
+            if (pos > causal_from + tq) v = -INFINITY;
+          }
+          if (n >= pc.rows) v = 0.f;        // padding rows: any finite value, discarded
+          x[n] = v;
+          exceed |= (v - m_ref[n] > kTau);
+        }
+        exceed = bar_red_or(1, 128, exceed);
+        if (exceed) {
+          // rare: move the reference max to this tile's column maxima
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {
+            float v = x[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[q4 * NG + n] = v;
+          }
+          bar_sync(1, 128);
+          float alpha[NG];
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {
+            const float tmax = fmaxf(fmaxf(red[n], red[NG + n]), fmaxf(red[2 * NG + n], red[3 * NG + n]));
+            const float m_new = fmaxf(m_ref[n], tmax);
+            alpha[n] = (m_ref[n] == -INFINITY) ? 0.f : ex2_approx(m_ref[n] - m_new);
+            l_acc[n] *= alpha[n];
+            m_ref[n] = m_new;
+          }
+          bar_sync(1, 128);
+          if (t > 0) {
+            // O holds this piece's earlier tiles: wait for the last PV, then rescale
+            mbar_wait(mbase + kMiscPv, (it_g - 1) & 1, abort_flag, prm.err);
+            tc_fence_after();
+#pragma unroll
+            for (int bk = 0; bk < 4; ++bk) {
+#pragma unroll
+              for (int c = 0; c < NPV / 16; ++c) {
+                float v[16];
+                const uint32_t a = tl + LY::kOBase + bk * NPV + 16 * c;
+                tmem_ld16(a, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const int col = 16 * c + k;
+                  v[k] *= alpha[col < NG ? col : col - NG];
+                }
+                tmem_st16(a, v);
+              }
+            }
+            tmem_wait_st();
+          }
+        }
+        // probabilities relative to the reference, split into two FP8 planes
+        const int stage = static_cast<int>(it_g % STAGES);
+        uint8_t* pb = LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
+                                   : smem + LY::kPOff + sb * NPV * 128;
+#pragma unroll
+        for (int n = 0; n < NG; n += 2) {
+          const float m0 = (m_ref[n] == -INFINITY) ? 0.f : m_ref[n];
+          const float m1 = (m_ref[n + 1] == -INFINITY) ? 0.f : m_ref[n + 1];
+          const float p0 = ex2_approx(x[n] - m0);
+          const float p1 = ex2_approx(x[n + 1] - m1);
+          l_acc[n] += p0;
+          l_acc[n + 1] += p1;
+          const uint16_t hi = f32x2_to_e4m3x2(p1, p0);
+          const float2 hf = e4m3x2_to_f32x2(hi);
+          const uint16_t lo = f32x2_to_e4m3x2((p1 - hf.y) * kLoScale, (p0 - hf.x) * kLoScale);
+          pb[((n) >> 3) * 1024 + poff[(n) & 7]] = static_cast<uint8_t>(hi & 0xFF);
+          pb[((n + 1) >> 3) * 1024 + poff[(n + 1) & 7]] = static_cast<uint8_t>(hi >> 8);
+          pb[((NG + n) >> 3) * 1024 + poff[(NG + n) & 7]] = static_cast<uint8_t>(lo & 0xFF);
+          pb[((NG + n + 1) >> 3) * 1024 + poff[(NG + n + 1) & 7]] = static_cast<uint8_t>(lo >> 8);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mbase + kMiscPFull + 8 * sb);
+
+        if (t == nt - 1) {
+          // ------------------------------------------------ piece epilogue
+          mbar_wait(mbase + kMiscPv, it_g & 1, abort_flag, prm.err);
+          tc_fence_after();
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {
+            float v = l_acc[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[q4 * NG + n] = v;
+          }
+          bar_sync(1, 128);
+          float scale_n[NG];
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {
+            const float l = (red[n] + red[NG + n]) + (red[2 * NG + n] + red[3 * NG + n]);
+            scale_n[n] = (l > 0.f) ? kv_scale / l : 0.f;
+            l_acc[n] = l;   // keep the total for the lse below
+          }
+          bar_sync(1, 128);
+          const int64_t row0 = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) * H + pc.g * NG;
+          const bool direct = pc.direct;
+          const bool slot_ok = direct || (pc.slot >= 0 && pc.slot < prm.n_slots);
+          if (!slot_ok && threadIdx.x == 64) atomicOr(prm.err, kErrBadOutput);
+#pragma unroll
+          for (int bk = 0; bk < 4; ++bk) {
+            const int c = bk * 128 + prow;
+#pragma unroll
+            for (int ch = 0; ch < NG / 16; ++ch) {
+              float hi[16], lo[16];
+              tmem_ld16(tl + LY::kOBase + bk * NPV + 16 * ch, hi);
+              tmem_ld16(tl + LY::kOBase + bk * NPV + NG + 16 * ch, lo);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const int n = 16 * ch + k;
+                if (n < pc.rows) {
+                  const float val = (hi[k] + lo[k] * (1.0f / kLoScale)) * scale_n[n];
+                  if (direct) {
+                    const int64_t r = row0 + n;
+                    if (r < prm.n_q_rows) {
+                      const int64_t off = (r / H) * prm.o_stride_tok + (r % H) * prm.o_stride_head + c;
+                      if (prm.o_fp32)
+                        reinterpret_cast<float*>(prm.o)[off] = val;
+                      else
+                        reinterpret_cast<__nv_bfloat16*>(prm.o)[off] = __float2bfloat16_rn(val);
+                    }
+                  } else if (slot_ok) {
+                    prm.part_o[(pc.slot * NG + n) * kDV + c] = val;
+                  }
+                }
+              }
+            }
+          }
+          if (prow < pc.rows) {
+            const int n = prow;
+            float l = 0.f, m = 0.f;
+#pragma unroll
+            for (int k = 0; k < NG; ++k)
+              if (k == n) {
+                l = l_acc[k];
+                m = m_ref[k];
+              }
+            const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+            if (direct) {
+              const int64_t r = row0 + n;
+              if (r < prm.n_q_rows) {
+                if (prm.lse_out) prm.lse_out[r] = lse;
+              } else {
+                atomicOr(prm.err, kErrBadOutput);
+              }
+            } else if (slot_ok) {
+              prm.part_lse[pc.slot * NG + n] = lse;
+            }
+          }
+          tc_fence_before();
+        }
+      }
+    }
+  }
+
+  if (bad && (threadIdx.x & 31) == 0) atomicOr(prm.err, kErrBadIndptr);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, LY::kTmemCols);
+  }
+}
+
+}  // namespace pmla

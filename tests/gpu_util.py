@@ -1,0 +1,90 @@
+"""Helpers shared by the GPU tests: run the CUDA path on a workload, run the oracle on the
+same bytes, compare with the tolerance the decode must meet."""
+import math
+
+import numpy as np
+import torch
+
+import mla_inputs
+import oracle
+
+# max|o - o_ref| <= O_ATOL + O_RTOL * |o_ref| elementwise, and |lse - lse_ref| <= LSE_ATOL.
+O_ATOL = 1e-2
+O_RTOL = 1e-2
+LSE_ATOL = 1e-3
+
+
+def to_device(case, device="cuda"):
+    for f in ("q", "kv", "qo_indptr", "kv_indptr", "kv_indices", "kv_last_page_lens", "q_scale",
+              "kv_scale"):
+        setattr(case, f, getattr(case, f).to(device))
+    return case
+
+
+def run_gpu(case, num_kv_splits=0, o_dtype=torch.bfloat16, with_lse=True, workspace=None,
+            kv_view=None, q_override=None):
+    import paged_mla_latent_gb300 as pm
+    q = case.q if q_override is None else q_override
+    n_tok, H = q.shape[0], q.shape[1]
+    o = torch.full((n_tok, H, 512), float("nan"), dtype=o_dtype, device=q.device)
+    lse = torch.full((n_tok, H), float("nan"), dtype=torch.float32, device=q.device) if with_lse else None
+    if workspace is None:
+        workspace = pm.make_workspace(case.B, H, case.max_seqlen_q, num_kv_splits, q.device)
+    kv = case.kv if kv_view is None else kv_view
+    pm.mla_decode(q, kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                  case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
+                  case.kv_scale, num_kv_splits=num_kv_splits, lse_out=lse, workspace=workspace)
+    torch.cuda.synchronize()
+    status = pm.mla_check_error(workspace)
+    return o, lse, status
+
+
+def run_oracle(case, q_override=None):
+    sm, qs, ks = case.scales()
+    q = (case.q if q_override is None else q_override).cpu().numpy()
+    return oracle.decode(q, case.kv.cpu().numpy(), case.qo_indptr.cpu().numpy(),
+                         case.kv_indptr.cpu().numpy(), case.kv_indices.cpu().numpy(), sm, qs, ks)
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", rows_mask=None):
+    """Assert the tolerance; returns a dict of error statistics."""
+    o = o_gpu.float().cpu().numpy().astype(np.float64)
+    d = np.abs(o - o_ref)
+    bound = O_ATOL + O_RTOL * np.abs(o_ref)
+    stats = dict(max_abs=float(d.max()) if d.size else 0.0,
+                 worst_ratio=float((d / bound).max()) if d.size else 0.0,
+                 err_over_std=float(d.max() / max(o_ref.std(), 1e-30)) if d.size else 0.0)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    assert (d <= bound).all(), f"{what}: o error {stats}"
+    if lse_gpu is not None:
+        l = lse_gpu.cpu().numpy().astype(np.float64)
+        both_inf = np.isneginf(l) & np.isneginf(lse_ref)
+        dl = np.where(both_inf, 0.0, np.abs(l - lse_ref))
+        stats["lse_max_abs"] = float(dl.max()) if dl.size else 0.0
+        assert (dl <= LSE_ATOL).all(), f"{what}: lse error {stats}"
+    return stats
+
+
+def gather_rows(case, b):
+    """Host copy of the cache rows request b attends, in position order."""
+    s, e = int(case.kv_indptr[b]), int(case.kv_indptr[b + 1])
+    idx = case.kv_indices[s:e].long()
+    return case.kv.index_select(0, idx).cpu().numpy()
+
+
+def oracle_sampled(case, samples):
+    """Oracle for a few (request, token-within-request, head) triples of a large case."""
+    sm, qs, ks = case.scales()
+    out = []
+    q_host = {}
+    for b, t, h in samples:
+        rows = gather_rows(case, b)
+        L = rows.shape[0]
+        T = case.q_lens[b]
+        r = int(case.qo_indptr[b]) + t
+        if r not in q_host:
+            q_host[r] = case.q[r].cpu().numpy()
+        n_att = L - T + t + 1
+        o, lse = oracle.attend_one(q_host[r][h], rows, np.arange(n_att, dtype=np.int32), sm, qs, ks)
+        out.append((r, h, o, lse))
+    return out

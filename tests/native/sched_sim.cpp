@@ -1,0 +1,45 @@
+// Host simulation of the split-KV schedule (test-suite only): runs the decode kernel's
+// piece iterator for every CTA and the merge kernel's partial lookup for every unit,
+// exactly as the device code does, and reports them to Python.
+#include <stdint.h>
+
+#include "../../paged_mla_latent_gb300/csrc/mla_sched.cuh"
+
+extern "C" {
+
+// Writes up to max_out pieces as 8 int64 each: cta, b, g, j0, j1, rows, slot, direct.
+// Returns the number of pieces (or -1 if max_out was too small, -2 if an iterator
+// reported inconsistent indptr data).
+int64_t sched_pieces(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H, int NG,
+                     int groups, int splits, int grid, int64_t* out, int64_t max_out) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid};
+  int64_t n = 0;
+  for (int cta = 0; cta < grid; ++cta) {
+    pmla::PieceIter it;
+    it.init(sp, cta);
+    pmla::Piece pc;
+    int bad = 0;
+    while (it.next(pc, &bad)) {
+      if (n >= max_out) return -1;
+      int64_t* o = out + 8 * n;
+      o[0] = cta; o[1] = pc.b; o[2] = pc.g; o[3] = pc.j0; o[4] = pc.j1; o[5] = pc.rows;
+      o[6] = pc.slot; o[7] = pc.direct ? 1 : 0;
+      ++n;
+    }
+    if (bad) return -2;
+  }
+  return n;
+}
+
+// For unit (b, g): returns 1 and first/count if it needs a merge, else 0.
+int sched_unit_partials(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H, int NG,
+                        int groups, int splits, int grid, int b, int g, int64_t* first,
+                        int* count) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid};
+  return pmla::unit_partials(sp, b, g, first, count) ? 1 : 0;
+}
+
+int64_t sched_partial_slots(int B, int groups, int splits, int grid) {
+  return pmla::partial_slots(B, groups, splits, grid);
+}
+}

@@ -1,0 +1,156 @@
+"""The C-ABI library loads, exports what include/paged_mla.h declares, and rejects bad
+arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(mla_[A-Za-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import paged_mla_latent_gb300 as pm
+    return pm
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("mla_decode", "mla_merge_partials", "mla_get_workspace_size",
+                     "mla_validate", "mla_check_error", "mla_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = lib.library_path()
+    assert os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = _declared_functions() - exported
+    assert not missing, f"declared but not exported: {missing}"
+    so = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(so, name)
+
+
+def test_status_strings(lib):
+    assert lib.mla_status_string(0) == "MLA_OK"
+    assert lib.mla_status_string(5) == "MLA_ERR_BAD_INDEX"
+    assert lib.mla_status_string(6) == "MLA_ERR_TIMEOUT"
+    assert lib.mla_status_string(12345) == "MLA_ERR_UNKNOWN"
+
+
+def test_workspace_size_plan(lib):
+    # auto policy: (B*groups + SMs) partial slots of NG rows x (512 + 1) floats + header
+    sz = lib.mla_get_workspace_size(16, 12, 1, 0, 152)
+    ng, slots = 16, 16 + 152
+    assert sz >= 256 + slots * ng * 513 * 4
+    assert sz < 256 + 256 + slots * ng * 513 * 4 + 256
+    # 96 heads -> two groups of 48 rows
+    sz96 = lib.mla_get_workspace_size(1, 96, 1, 0, 152)
+    assert sz96 >= (2 + 152) * 48 * 513 * 4
+    # one split per request needs no partials
+    assert lib.mla_get_workspace_size(16, 12, 1, 1, 152) == 256
+    with pytest.raises(lib.MlaError):
+        lib.mla_get_workspace_size(16, 12, 0, 0, 152)     # max_seqlen_q < 1
+    with pytest.raises(lib.MlaError):
+        lib.mla_get_workspace_size(16, 0, 1, 0, 152)      # no heads
+
+
+def _t(ptr, dtype, shape, stride=None):
+    import paged_mla_latent_gb300 as pm
+    d = pm.MlaTensor()
+    d.ptr = ptr
+    d.ndim = len(shape)
+    d.dtype = dtype
+    if stride is None:
+        stride, acc = [], 1
+        for s in reversed(shape):
+            stride.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, stride)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _args(**over):
+    """Host-side descriptors with fake (never dereferenced) device addresses."""
+    F8, BF, F32, I32 = 1, 2, 3, 4
+    base = 1 << 40
+    a = dict(
+        q=_t(base, F8, [2, 12, 576]), kv=_t(base + (1 << 20), F8, [1024, 576]),
+        o=_t(base + (2 << 20), BF, [2, 12, 512]), qo=_t(base + (3 << 20), I32, [3]),
+        kvp=_t(base + (4 << 20), I32, [3]), idx=_t(base + (5 << 20), I32, [1024]),
+        last=_t(base + (6 << 20), I32, [2]), qs=_t(base + (7 << 20), F32, []),
+        ks=_t(base + (8 << 20), F32, []), lse=None, mq=1, sm=0.0721, splits=0,
+        ws=base + (9 << 20), ws_bytes=1 << 20)
+    a.update(over)
+    return a
+
+
+def _call(a):
+    import paged_mla_latent_gb300 as pm
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    return pm._lib.mla_decode(r(a["q"]), r(a["kv"]), r(a["o"]), r(a["qo"]), r(a["kvp"]),
+                              r(a["idx"]), r(a["last"]), a["mq"], a["sm"], r(a["qs"]), r(a["ks"]),
+                              a["splits"], r(a["lse"]), ctypes.c_void_p(a["ws"]), a["ws_bytes"],
+                              None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), 1),
+    (dict(q=_t(0, 1, [2, 12, 576])), 1),                                   # null pointer
+    (dict(q=_t(1 << 40, 3, [2, 12, 576])), 1),                             # q not fp8
+    (dict(q=_t(1 << 40, 1, [2, 12, 512])), 2),                             # head dim != 576
+    (dict(q=_t((1 << 40) + 8, 1, [2, 12, 576])), 1),                       # q not 16-B aligned
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [1024, 2, 1, 576])), 2),         # page_size != 1
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [1024, 576], [584, 1])), 1),    # pitch not 16-B multiple
+    (dict(o=_t((1 << 40) + (2 << 20), 2, [2, 12, 256])), 1),               # o width != 512
+    (dict(o=_t((1 << 40) + (2 << 20), 4, [2, 12, 512])), 1),               # o int32
+    (dict(kvp=_t((1 << 40) + (4 << 20), 4, [4])), 1),                      # indptr size mismatch
+    (dict(idx=_t((1 << 40) + (5 << 20), 3, [1024])), 1),                   # indices not int32
+    (dict(last=_t((1 << 40) + (6 << 20), 4, [5])), 1),                     # last_page_lens size
+    (dict(qs=_t((1 << 40) + (7 << 20), 3, [2])), 1),                       # q_scale not scalar
+    (dict(mq=0), 1),
+    (dict(mq=65), 1),
+    (dict(sm=float("nan")), 1),
+    (dict(ws=(1 << 40) + 8), 1),                                           # workspace misaligned
+    (dict(lse=_t(1 << 41, 3, [2, 11])), 1),                                # lse shape
+])
+def test_decode_rejects_bad_arguments_on_host(lib, over, expect):
+    assert _call(_args(**over)) == expect
+
+
+def test_merge_rejects_bad_arguments_on_host(lib):
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    F32, I32, BF = 3, 4, 2
+    base = 1 << 40
+    op = _t(base, F32, [8, 96, 512])
+    lp = _t(base + (32 << 20), F32, [8, 96])
+    ip = _t(base + (33 << 20), I32, [2])
+    ix = _t(base + (34 << 20), I32, [8])
+    o = _t(base + (35 << 20), BF, [1, 96, 512])
+    bad_o = _t(base + (35 << 20), BF, [1, 95, 512])
+    assert lib._lib.mla_merge_partials(r(op), r(lp), r(ip), r(ix), r(bad_o), None, None, None) == 1
+    bad_lp = _t(base + (32 << 20), F32, [7, 96])
+    assert lib._lib.mla_merge_partials(r(op), r(bad_lp), r(ip), r(ix), r(o), None, None, None) == 1
+    odd = _t(base + 4, F32, [8, 96, 512])
+    assert lib._lib.mla_merge_partials(r(odd), r(lp), r(ip), r(ix), r(o), None, None, None) == 1

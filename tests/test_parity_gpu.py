@@ -1,0 +1,277 @@
+"""Parity of the CUDA decode path (through the C ABI) with the FP64 oracle.
+
+Small cases are compared element by element; they span several 128-position tiles, a
+ragged tail, every row-group size (16 / 32 / 48 rows), causal drafts, split policies and
+poisoned memory.  Full-size workloads are checked on sampled outputs and invariants.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pm():
+    import paged_mla_latent_gb300 as m
+    return m
+
+
+def _check(case, **kw):
+    case = gu.to_device(case)
+    o, lse, status = gu.run_gpu(case, **kw)
+    assert status == 0, f"device error {status}"
+    o_ref, lse_ref = gu.run_oracle(case)
+    return gu.compare(o, lse, o_ref, lse_ref, what=case.name)
+
+
+def test_tiny_workload(pm):
+    _check(mla_inputs.make_case("tiny", seed=0))
+
+
+@pytest.mark.parametrize("stress", [False, True])
+def test_tiny_workload_stress_scales(pm, stress):
+    s = 1.0 if stress else 0.05
+    _check(mla_inputs.make_case("tiny", seed=1, q_scale=s, kv_scale=1.0 if stress else 0.1))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
+def test_multi_tile_ragged(pm, seed, scales):
+    case = mla_inputs.make_custom([1000, 2500, 130, 1, 257], H=12, seed=seed,
+                                  q_scale=scales[0], kv_scale=scales[1], name="ragged")
+    _check(case)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+def test_split_policies_agree_with_oracle(pm, splits):
+    case = mla_inputs.make_custom([3000, 700, 129], H=12, seed=3, q_scale=1.0, kv_scale=1.0,
+                                  name=f"splits{splits}")
+    _check(case, num_kv_splits=splits)
+
+
+def test_fp32_output(pm):
+    case = mla_inputs.make_custom([900, 40], H=12, seed=4, q_scale=1.0, kv_scale=1.0, name="fp32o")
+    _check(case, o_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("H", [16, 24, 40, 96])
+def test_head_counts(pm, H):
+    """16 -> one 16-row group, 24 -> 32-row group, 40 -> 48-row group, 96 -> two 48-row groups."""
+    case = mla_inputs.make_custom([1500, 333], H=H, seed=5, q_scale=1.0, kv_scale=1.0, name=f"H{H}")
+    _check(case)
+
+
+@pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
+def test_causal_drafts(pm, scales):
+    """q_len 4 (MTP): draft t attends positions 0 .. L-4+t; includes L == T and ragged tails."""
+    case = mla_inputs.make_custom([4, 130, 1000, 2049], q_lens=[4, 4, 4, 4], H=12, seed=6,
+                                  q_scale=scales[0], kv_scale=scales[1], name="mtp-small")
+    _check(case)
+
+
+def test_mixed_query_lengths(pm):
+    case = mla_inputs.make_custom([300, 800, 50, 1200], q_lens=[1, 3, 2, 4], H=12, seed=7,
+                                  q_scale=1.0, kv_scale=1.0, name="mixed-q")
+    _check(case)
+
+
+def test_shared_prefix(pm):
+    case = mla_inputs.make_custom([2000, 2100, 2222, 1900], H=12, seed=8, shared_prefix=1700,
+                                  index_buffer=10000, name="prefix")
+    _check(case)
+
+
+def test_poisoned_rows_and_index_tail(pm):
+    """Unattended rows hold fp8 NaN and the index buffer tail points outside the pool:
+    any stray read would surface as NaN or a device error."""
+    case = mla_inputs.make_custom([700, 129, 1], q_lens=[1, 4, 1], H=12, seed=9, poison=True,
+                                  index_buffer=5000, q_scale=1.0, kv_scale=1.0, name="poison")
+    _check(case)
+    for splits in (1, 3):
+        _check(case, num_kv_splits=splits)
+
+
+def test_zero_padded_heads_are_bit_identical(pm):
+    """P6: 12 heads vs the same 12 heads + 4 zero heads; real heads' o and lse identical."""
+    case = gu.to_device(mla_inputs.make_custom([1000, 300], H=12, seed=10, q_scale=1.0,
+                                               kv_scale=1.0))
+    o12, lse12, st = gu.run_gpu(case)
+    assert st == 0
+    q16 = torch.zeros((case.q.shape[0], 16, 576), dtype=torch.uint8, device="cuda")
+    q16[:, :12] = case.q
+    o16, lse16, st = gu.run_gpu(case, q_override=q16)
+    assert st == 0
+    assert torch.equal(o16[:, :12], o12)
+    assert torch.equal(lse16[:, :12], lse12)
+
+
+def test_identical_rows_mean_and_exact_counts(pm):
+    """P2: all attended rows equal -> o = kv_scale * v and exp(lse - s) = attended count,
+    which pins the attended set of every (request, draft) bit-exactly."""
+    lens, qlens = [1000, 37, 300], [1, 4, 2]
+    case = mla_inputs.make_custom(lens, q_lens=qlens, H=12, seed=11, q_scale=0.5, kv_scale=0.25)
+    row = case.kv[0].clone()
+    case.kv[:] = row
+    case = gu.to_device(case)
+    o, lse, st = gu.run_gpu(case, o_dtype=torch.float32)
+    assert st == 0
+    from tests import brute
+    v = brute.fp8_decode(row.numpy())
+    sm, qs, ks = case.scales()
+    o = o.cpu().numpy()
+    lse = lse.cpu().numpy()
+    qh = case.q.cpu().numpy()
+    for b, (L, T) in enumerate(zip(lens, qlens)):
+        for t in range(T):
+            r = int(case.qo_indptr[b]) + t
+            for h in range(12):
+                assert np.allclose(o[r, h], ks * v[:512], rtol=1e-2, atol=1e-4)
+                s = sm * qs * ks * float(brute.fp8_decode(qh[r, h]) @ v)
+                count = math.exp(lse[r, h] - s)
+                assert round(count) == L - T + t + 1, (b, t, h, count)
+
+
+def test_constant_logit_shift(pm):
+    """P3: every row shares its rope block; changing q's rope block shifts all logits of a
+    head by the same delta: o unchanged, lse moves by delta."""
+    case = mla_inputs.make_custom([900, 200], H=12, seed=12, q_scale=1.0, kv_scale=1.0)
+    case.kv[:, 512:] = case.kv[0, 512:]
+    q2 = case.q.clone()
+    q2[:, :, 512:] = torch.flip(case.q[:, :, 512:], dims=[1])
+    case = gu.to_device(case)
+    o1, l1, _ = gu.run_gpu(case, o_dtype=torch.float32)
+    o2, l2, _ = gu.run_gpu(case, o_dtype=torch.float32, q_override=q2.cuda())
+    from tests import brute
+    sm, qs, ks = case.scales()
+    kr = brute.fp8_decode(case.kv[0, 512:].cpu().numpy())
+    q1h, q2h = case.q.cpu().numpy(), q2.numpy()
+    for r in range(2):
+        for h in range(12):
+            delta = sm * qs * ks * (float(brute.fp8_decode(q2h[r, h, 512:]) @ kr) -
+                                    float(brute.fp8_decode(q1h[r, h, 512:]) @ kr))
+            assert abs((l2[r, h] - l1[r, h]).item() - delta) < 2e-3
+    assert torch.allclose(o1, o2, atol=2e-3, rtol=1e-2)
+
+
+def test_needle_position_and_causal_limit(pm):
+    """One row with a dominant logit and a one-hot value reveals which positions each
+    draft attends."""
+    L, T = 300, 4
+    case = mla_inputs.make_custom([L], q_lens=[T], H=12, seed=13, q_scale=1.0, kv_scale=1.0)
+    case.kv.zero_()
+    case.q.zero_()
+    big = torch.tensor([16.0]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    one = torch.tensor([1.0]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    case.q[:, :, 0] = big
+    needle_pos = L - 2
+    row = int(case.kv_indices[needle_pos])
+    case.kv[row, 0] = big
+    case.kv[row, 100] = one
+    case = gu.to_device(case)
+    o, lse, st = gu.run_gpu(case, o_dtype=torch.float32)
+    assert st == 0
+    for t in range(T):
+        sees = needle_pos <= L - T + t
+        for h in range(12):
+            val = o[t, h, 100].item()
+            assert (val > 0.99) == sees, (t, h, val)
+
+
+def test_empty_request_gives_zero_and_neg_inf(pm):
+    case = mla_inputs.make_custom([0, 400, 0], q_lens=[1, 1, 1], H=12, seed=14)
+    case = gu.to_device(case)
+    for splits in (0, 1, 4):
+        o, lse, st = gu.run_gpu(case, num_kv_splits=splits, o_dtype=torch.float32)
+        assert st == 0
+        assert torch.equal(o[0], torch.zeros_like(o[0])) and torch.equal(o[2], torch.zeros_like(o[2]))
+        assert torch.isneginf(lse[0]).all() and torch.isneginf(lse[2]).all()
+        o_ref, lse_ref = oracle.attend_one(case.q[1, 3].cpu().numpy(),
+                                           gu.gather_rows(case, 1), np.arange(400, dtype=np.int32),
+                                           *case.scales())
+        assert np.allclose(o[1, 3].cpu().numpy(), o_ref, atol=1e-2, rtol=1e-2)
+
+
+def test_bad_index_is_flagged_without_fault(pm):
+    case = mla_inputs.make_custom([500, 300], H=12, seed=15)
+    case.kv_indices[10] = case.kv.shape[0] + 123
+    case = gu.to_device(case)
+    o, lse, st = gu.run_gpu(case)
+    assert st == 5   # MLA_ERR_BAD_INDEX
+    torch.cuda.synchronize()   # the context is still usable
+    ws = pm.make_workspace(case.B, 12, 1, 0, "cuda")
+    assert pm.mla_validate(case.q, case.kv, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                           case.kv_last_page_lens, ws) == 5
+
+
+def test_validate(pm):
+    case = gu.to_device(mla_inputs.make_custom([500, 300], q_lens=[1, 2], H=12, seed=16))
+    ws = pm.make_workspace(case.B, 12, 2, 0, "cuda")
+    assert pm.mla_validate(case.q, case.kv, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                           case.kv_last_page_lens, ws) == 0
+    bad = case.kv_last_page_lens.clone()
+    bad[1] = 128
+    assert pm.mla_validate(case.q, case.kv, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                           bad, ws) == 7
+    short = torch.tensor([0, 500, 501], dtype=torch.int32, device="cuda")   # kv_len 1 < q_len 2
+    assert pm.mla_validate(case.q, case.kv, case.qo_indptr, short, case.kv_indices,
+                           case.kv_last_page_lens, ws) == 7
+
+
+def test_merge_partials_csr(pm):
+    """mla_merge_partials == oracle merge on random partials, including -inf ones and an
+    output row with no partials at all."""
+    rng = np.random.default_rng(17)
+    P, H = 9, 12
+    o_parts = rng.standard_normal((P, H, 512)).astype(np.float32)
+    lse_parts = (rng.standard_normal((P, H)) * 3).astype(np.float32)
+    lse_parts[2, :] = -np.inf
+    indptr = np.array([0, 3, 3, 9], dtype=np.int32)
+    idx = np.array([4, 2, 0, 1, 3, 5, 6, 7, 8], dtype=np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o = torch.empty((3, H, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((3, H), dtype=torch.float32, device="cuda")
+    pm.mla_merge_partials(dev(o_parts), dev(lse_parts), dev(indptr), dev(idx), o, lse)
+    torch.cuda.synchronize()
+    for r in range(3):
+        sel = idx[indptr[r]:indptr[r + 1]]
+        for h in range(H):
+            if sel.size == 0:
+                assert torch.equal(o[r, h].cpu(), torch.zeros(512))
+                assert math.isinf(lse[r, h].item()) and lse[r, h].item() < 0
+                continue
+            ro, rl = oracle.merge(o_parts[sel, h].astype(np.float64), lse_parts[sel, h].astype(np.float64))
+            assert np.allclose(o[r, h].cpu().numpy(), ro, rtol=1e-5, atol=1e-5)
+            assert abs(lse[r, h].item() - rl) < 1e-4
+
+
+def test_context_shard_merge_small(pm):
+    """8 context shards x 96 heads, each shard's partial (fp32 o, lse) merged by
+    mla_merge_partials, equals the unsplit 96-head call and the oracle."""
+    case = gu.to_device(mla_inputs.make_custom([4000], H=96, seed=18, q_scale=1.0, kv_scale=1.0))
+    o_ref, lse_ref = gu.run_oracle(case)
+    o_full, lse_full, st = gu.run_gpu(case, o_dtype=torch.float32)
+    assert st == 0
+    shards = mla_inputs.shard_views(case, 8)
+    o_parts = torch.empty((8, 96, 512), dtype=torch.float32, device="cuda")
+    lse_parts = torch.empty((8, 96), dtype=torch.float32, device="cuda")
+    ws = pm.make_workspace(1, 96, 1, 0, "cuda")
+    for s, (ip, idx, _) in enumerate(shards):
+        pm.mla_decode(case.q, case.kv, o_parts[s:s + 1], case.qo_indptr, ip, idx,
+                      case.kv_last_page_lens, 1, case.sm_scale, case.q_scale, case.kv_scale,
+                      lse_out=lse_parts[s:s + 1], workspace=ws)
+    o = torch.empty((1, 96, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 96), dtype=torch.float32, device="cuda")
+    pm.mla_merge_partials(o_parts, lse_parts, torch.tensor([0, 8], dtype=torch.int32, device="cuda"),
+                          torch.arange(8, dtype=torch.int32, device="cuda"), o, lse)
+    torch.cuda.synchronize()
+    assert pm.mla_check_error(ws) == 0
+    gu.compare(o, lse, o_ref, lse_ref, what="shard-merge")
+    assert torch.allclose(o.float(), o_full, atol=1e-2, rtol=1e-2)
+    assert torch.allclose(lse, lse_full, atol=1e-3)

@@ -1,0 +1,160 @@
+"""Host simulation of the split-KV schedule (CPU only).
+
+tests/native/sched_sim.cpp compiles the library's scheduling header with g++ and runs the
+decode kernel's piece iterator for every CTA and the merge kernel's partial lookup for
+every unit.  These tests check the properties the GPU path relies on: every attended
+position of every (request, row group) is covered exactly once, a unit is written
+directly iff one piece covers it, partial slots are unique and inside the workspace, and
+the merge finds exactly the slots the decode wrote.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "native", "sched_sim.cpp")
+HDR = os.path.join(os.path.dirname(HERE), "paged_mla_latent_gb300", "csrc", "mla_sched.cuh")
+LIB = os.path.join(HERE, "native", "_build", "libschedsim.so")
+
+
+@pytest.fixture(scope="module")
+def sim():
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    if (not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(SRC),
+                                                                  os.path.getmtime(HDR))):
+        tmp = LIB + f".{os.getpid()}"
+        subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-o", tmp, SRC], check=True)
+        os.replace(tmp, LIB)
+    lib = ctypes.CDLL(LIB)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.sched_pieces.restype = ctypes.c_int64
+    lib.sched_pieces.argtypes = [i32p, i32p] + [ctypes.c_int] * 6 + [i64p, ctypes.c_int64]
+    lib.sched_unit_partials.restype = ctypes.c_int
+    lib.sched_unit_partials.argtypes = [i32p, i32p] + [ctypes.c_int] * 8 + [i64p, ctypes.POINTER(ctypes.c_int)]
+    lib.sched_partial_slots.restype = ctypes.c_int64
+    lib.sched_partial_slots.argtypes = [ctypes.c_int] * 4
+    return lib
+
+
+def pick_ng(rows):
+    return 16 if rows <= 16 else (32 if rows <= 32 else 48)
+
+
+def simulate(sim, kv_lens, q_lens, H, splits, grid):
+    kvp = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
+    qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    B = len(kv_lens)
+    rows = max(q_lens) * H
+    NG = pick_ng(rows)
+    groups = (rows + NG - 1) // NG
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    cap = 8 * (grid + B * groups * max(splits, 1) + 16)
+    out = np.zeros(cap * 8, dtype=np.int64)
+    n = sim.sched_pieces(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, groups,
+                         splits, grid, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
+    assert n >= 0, f"simulation failed with {n}"
+    pieces = out[:8 * n].reshape(n, 8)
+    units = {}
+    for b in range(B):
+        for g in range(groups):
+            first = ctypes.c_int64(0)
+            count = ctypes.c_int(0)
+            need = sim.sched_unit_partials(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H,
+                                           NG, groups, splits, grid, b, g, ctypes.byref(first),
+                                           ctypes.byref(count))
+            units[(b, g)] = (need, first.value, count.value)
+    slots = sim.sched_partial_slots(B, groups, splits, grid)
+    return pieces, units, slots, NG, groups
+
+
+def check_schedule(sim, kv_lens, q_lens, H, splits, grid):
+    pieces, units, n_slots, NG, groups = simulate(sim, kv_lens, q_lens, H, splits, grid)
+    B = len(kv_lens)
+    by_unit = {}
+    for cta, b, g, j0, j1, rows, slot, direct in pieces:
+        assert 0 <= b < B and 0 <= g < groups and 0 <= j0 < j1 <= kv_lens[b]
+        assert rows == min(NG, q_lens[b] * H - g * NG) and rows > 0
+        by_unit.setdefault((b, g), []).append((j0, j1, slot, direct, cta))
+    partial_slots = [p[6] for p in pieces if not p[7]]
+    assert len(partial_slots) == len(set(partial_slots)), "partial slot written twice"
+    assert all(0 <= s < n_slots for s in partial_slots)
+    for b in range(B):
+        for g in range(groups):
+            real = q_lens[b] * H - g * NG > 0
+            ps = sorted(by_unit.get((b, g), []))
+            need, first, count = units[(b, g)]
+            if not real or kv_lens[b] == 0:
+                assert not ps
+                continue
+            # exact cover of [0, L)
+            pos = 0
+            for j0, j1, *_ in ps:
+                assert j0 == pos, f"gap/overlap in unit {(b, g)}"
+                pos = j1
+            assert pos == kv_lens[b]
+            if len(ps) == 1 and ps[0][3]:
+                assert need == 0          # written directly, no merge
+            else:
+                assert need == 1 and not any(p[3] for p in ps)
+                expect = set(range(first, first + count))
+                got = {p[2] for p in ps}
+                assert got <= expect
+                if splits <= 0:
+                    assert got == expect
+                else:   # fixed policy: missing slots are exactly the empty pieces
+                    empty = {first + k for k in range(count)
+                             if (k + 1) * kv_lens[b] // splits <= k * kv_lens[b] // splits}
+                    assert got == expect - empty
+    return pieces
+
+
+CASES = [
+    ([1], [1], 12), ([2], [1], 12), ([128], [1], 12), ([300], [1], 12),
+    ([256, 300], [1, 1], 12), ([1000, 2500, 130, 1, 257], [1] * 5, 12),
+    ([3000, 700, 129], [1, 1, 1], 12), ([0, 400, 0], [1, 1, 1], 12),
+    ([4, 130, 1000, 2049], [4] * 4, 12), ([300, 800, 50, 1200], [1, 3, 2, 4], 12),
+    ([1500, 333], [1, 1], 96), ([1500, 333], [1, 1], 24), ([142000], [1], 12),
+    ([68174] * 16, [1] * 16, 12), ([17750], [1], 96),
+]
+
+
+@pytest.mark.parametrize("kv_lens,q_lens,H", CASES)
+@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+@pytest.mark.parametrize("grid", [1, 5, 152])
+def test_schedule_covers_every_position_once(sim, kv_lens, q_lens, H, splits, grid):
+    check_schedule(sim, kv_lens, q_lens, H, splits, grid)
+
+
+def test_auto_policy_balances_rows(sim):
+    kv_lens = [68174 + i for i in range(16)]
+    pieces = check_schedule(sim, kv_lens, [1] * 16, 12, 0, 152)
+    per_cta = np.zeros(152, dtype=np.int64)
+    for cta, b, g, j0, j1, *_ in pieces:
+        per_cta[cta] += j1 - j0
+    W = sum(kv_lens)
+    assert per_cta.max() - per_cta.min() <= 1
+    assert per_cta.sum() == W
+
+
+def test_batch1_long_context_fills_every_sm(sim):
+    pieces = check_schedule(sim, [142000], [1], 12, 0, 152)
+    assert len({p[0] for p in pieces}) == 152
+
+
+def test_random_batches(sim):
+    rng = np.random.default_rng(0)
+    for _ in range(40):
+        B = int(rng.integers(1, 20))
+        T = int(rng.integers(1, 5))
+        kv = [int(x) for x in rng.integers(0, 3000, size=B)]
+        q = [int(min(t, L)) if L > 0 else 0 for t, L in zip(rng.integers(1, T + 1, size=B), kv)]
+        H = int(rng.choice([12, 16, 24, 96]))
+        if max(q) == 0:
+            continue
+        for splits in (0, 1, 3):
+            for grid in (1, 7, 152):
+                check_schedule(sim, kv, q, H, splits, grid)
