@@ -1,0 +1,388 @@
+"""Benchmark of paged latent-MLA decode on GB300.
+
+One step = one mla_decode call (split-KV scheduler + tcgen05 decode + LSE merge) over
+one synthetic decode batch whose inputs are resident in HBM.  L2 is flushed (a 512 MB
+write) before every step, outside the timed region.  Metric: effective KV-cache GB/s
+(576 bytes per attended position / time) and microseconds per call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c16] [--impl reference]
+
+--impl reference times the FP64 CPU oracle on a bounded sample of the same workload
+(the reference arm); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import glob
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import mla_inputs
+
+METRIC = "MLA decode effective KV-cache GB/s (% of GB300 HBM peak) and µs per decode call"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_TEXT = {
+    "tiny": "tiny decode: batch 2, 12 heads, q_len 1, kv_lens {256, 300}, 1,024-row fp8 pool",
+    "c16": "concurrency-16 decode: batch 16, 12 heads, q_len 1, 63,911 shared-prefix + 4,089 "
+           "unique + U[0,350) positions per request (~68.2K), 5,283,840-row fp8 pool",
+    "c24": "concurrency-24 decode: batch 24, otherwise as c16",
+    "long": "long single request: batch 1, 12 heads, kv_len 142,000, 2^18-row fp8 pool",
+    "long96": "long single request, 96 heads (context-shard reference shape), kv_len 142,000",
+    "mtp": "multi-token verification: batch 64, 12 heads, q_len 4 causal, kv_len "
+           "log-uniform [2,048, 65,536], 2^22-row fp8 pool",
+}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_mla_latent_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(config: str):
+    """dram bytes per decode call from a committed ncu summary, if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(config)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return world, rank, local, dist
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local, None
+
+
+def oracle_sample(case, n_requests: int, n_heads: int):
+    """Host copies of a bounded sample: the first n_requests requests, n_heads heads each."""
+    reqs = list(range(min(n_requests, case.B)))
+    rows, idx, kvp, qop, q = [], [], [0], [0], []
+    off = 0
+    for b in reqs:
+        s, e = int(case.kv_indptr[b]), int(case.kv_indptr[b + 1])
+        r = case.kv.index_select(0, case.kv_indices[s:e].long()).cpu().numpy()
+        rows.append(r)
+        idx.append(np.arange(off, off + r.shape[0], dtype=np.int32))
+        off += r.shape[0]
+        kvp.append(off)
+        t0, t1 = int(case.qo_indptr[b]), int(case.qo_indptr[b + 1])
+        q.append(case.q[t0:t1, :n_heads].cpu().numpy())
+        qop.append(qop[-1] + (t1 - t0))
+    return (np.concatenate(q), np.concatenate(rows), np.array(qop, np.int32),
+            np.array(kvp, np.int32), np.concatenate(idx), off)
+
+
+def time_oracle(case, n_requests, n_heads):
+    import oracle
+    q, kv, qop, kvp, idx, positions = oracle_sample(case, n_requests, n_heads)
+    sm, qs, ks = case.scales()
+    t0 = time.perf_counter()
+    oracle.decode(q, kv, qop, kvp, idx, sm, qs, ks)
+    dt = time.perf_counter() - t0
+    # bytes of cache the oracle consumed, scaled to the GPU call's head count
+    sample_bytes = 576 * positions * n_heads / case.H
+    return dt, sample_bytes, oracle.max_threads(), positions
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the FP64 CPU oracle, bounded sample per step, on the host cores."""
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = mla_inputs.make_case(args.config, seed=args.seed, device=dev)
+    n_req, n_heads = args.ref_requests, args.ref_heads
+    for _ in range(args.warmup):
+        time_oracle(case, n_req, n_heads)
+    times, sb = [], 0.0
+    cores = 1
+    for _ in range(args.steps):
+        dt, sb, cores, pos = time_oracle(case, n_req, n_heads)
+        times.append(dt)
+    mean = sum(times) / len(times)
+    value = sb / mean / 1e9
+    sample = (f"first {n_req} request(s) x {n_heads} of {case.H} heads of the {args.config} "
+              f"workload per step ({pos} positions); GB/s scaled to all {case.H} heads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="c16", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--num-kv-splits", type=int, default=0)
+    ap.add_argument("--q-scale", type=float, default=mla_inputs.DEFAULT_Q_SCALE)
+    ap.add_argument("--kv-scale", type=float, default=mla_inputs.DEFAULT_KV_SCALE)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-l2-flush", action="store_true")
+    ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--ref-heads", type=int, default=12)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    world, rank, local, dist = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import paged_mla_latent_gb300 as pm
+    dev = torch.device("cuda", local)
+    case = mla_inputs.make_case(args.config, seed=args.seed + rank, device=dev,
+                                q_scale=args.q_scale, kv_scale=args.kv_scale)
+    n_tok, H = case.q.shape[0], case.q.shape[1]
+    o = torch.empty((n_tok, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
+    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(q=case.q, qo=case.qo_indptr, kvp=case.kv_indptr, idx=case.kv_indices,
+             last=case.kv_last_page_lens, out=o, l=lse):
+        pm.mla_decode(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q, case.sm_scale,
+                      case.q_scale, case.kv_scale, num_kv_splits=args.num_kv_splits,
+                      lse_out=l, workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        if not args.no_l2_flush:
+            flush.fill_(i & 0xFF)
+        call()
+    torch.cuda.synchronize(dev)
+    st = pm.mla_check_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {pm.mla_status_string(st)}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            if not args.no_l2_flush:
+                flush.fill_((i + 7) & 0xFF)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if dist is not None:
+        dist.barrier()
+    st = pm.mla_check_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {pm.mla_status_string(st)}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if dist is not None:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+
+    gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
+    algo = mla_inputs.algorithmic_bytes(case)
+    value = world * gathered / (mean_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = algo / (mean_ms * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        used = case.total_kv
+        host = {
+            "q": case.q.cpu().pin_memory(), "qo": case.qo_indptr.cpu().pin_memory(),
+            "kvp": case.kv_indptr.cpu().pin_memory(), "idx": case.kv_indices[:used].cpu().pin_memory(),
+            "last": case.kv_last_page_lens.cpu().pin_memory(),
+        }
+        d_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size()
+        e_ms = []
+        n_e2e = max(5, min(args.steps, 20))
+        for i in range(n_e2e + 2):
+            if not args.no_l2_flush:
+                flush.fill_(i & 0xFF)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for k in host:
+                d_in[k].copy_(host[k], non_blocking=True)
+            call(q=d_in["q"], qo=d_in["qo"], kvp=d_in["kvp"], idx=d_in["idx"], last=d_in["last"])
+            h_o.copy_(o, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                e_ms.append((time.perf_counter() - t0) * 1e3)
+        e_mean = sum(e_ms) / len(e_ms)
+        e2e = {"value": world * gathered / (e_mean * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_mean}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        dt, sb, cores, pos = time_oracle(case, args.ref_requests, args.ref_heads)
+        cpu_base = {"value": sb / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+                    "sample": f"first {args.ref_requests} request(s) x {args.ref_heads} heads of "
+                              f"this workload ({pos} positions), GB/s scaled to all {H} heads",
+                    "cpu": cpu_model()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "us_per_call": mean_ms * 1e3,
+            "pct_of_peak_measured": 100.0 * value / world / peak,
+            "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                       "seed": args.seed, "requests": case.B, "heads": H,
+                       "q_len": case.max_seqlen_q, "positions": case.total_kv,
+                       "gathered_kv_bytes": gathered, "algorithmic_bytes": algo,
+                       "num_kv_splits": args.num_kv_splits,
+                       "l2": "flushed before every step (512 MB write, outside the timed region)"
+                             if not args.no_l2_flush else "not flushed",
+                       "parallelism": f"{world} independent replicas (one batch per GPU)"},
+            "roofline": {"bound": "hbm", "kernel": "mla_decode call (decode + merge kernels)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                         "traffic": recorded_traffic(args.config)},
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": t_wall,
+            "kernel_source_hash": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

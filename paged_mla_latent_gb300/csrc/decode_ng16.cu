@@ -2,9 +2,8 @@
 #include "mla_decode_instantiate.cuh"
 
 namespace pmla {
-int launch_decode_ng16(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
-                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+int launch_decode_ng16(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream) {
-  return launch_decode_impl<16, 3>(kv_lat, kv_rope, q_lat, q_rope, prm, grid, stream);
+  return launch_decode_impl<16, 3>(q_lat, q_rope, prm, grid, stream);
 }
 }  // namespace pmla

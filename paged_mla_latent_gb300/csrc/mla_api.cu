@@ -252,14 +252,8 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   if ((rc = make_plan(cs.B, cs.H, max_seqlen_q, num_kv_splits, sms, &plan))) return rc;
   if (workspace_bytes < plan.bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
 
-  CUtensorMap kv_lat, kv_rope, q_lat, q_rope;
+  CUtensorMap q_lat, q_rope;
   const int64_t q_rows = cs.n_tok * cs.H;
-  if ((rc = make_map(&kv_lat, kv_buffer->ptr, cs.n_kv_rows, cs.kv_pitch, 128, 1,
-                     CU_TENSOR_MAP_SWIZZLE_128B)))
-    return rc;
-  if ((rc = make_map(&kv_rope, kv_buffer->ptr, cs.n_kv_rows, cs.kv_pitch, 64, 1,
-                     CU_TENSOR_MAP_SWIZZLE_64B)))
-    return rc;
   if ((rc = make_map(&q_lat, q->ptr, q_rows, kD, 128, plan.NG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
   if ((rc = make_map(&q_rope, q->ptr, q_rows, kD, 64, plan.NG, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
 
@@ -273,6 +267,8 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.sp.groups = plan.groups;
   prm.sp.splits = plan.splits;
   prm.sp.grid = plan.grid;
+  prm.kv = static_cast<const uint8_t*>(kv_buffer->ptr);
+  prm.kv_pitch = cs.kv_pitch;
   prm.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
   prm.kv_indices_len = cs.kv_indices_len;
   prm.n_kv_rows = cs.n_kv_rows;
@@ -291,9 +287,9 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.err = reinterpret_cast<int*>(ws);
 
   switch (plan.NG) {
-    case 16: rc = launch_decode_ng16(kv_lat, kv_rope, q_lat, q_rope, prm, plan.grid, stream); break;
-    case 32: rc = launch_decode_ng32(kv_lat, kv_rope, q_lat, q_rope, prm, plan.grid, stream); break;
-    default: rc = launch_decode_ng48(kv_lat, kv_rope, q_lat, q_rope, prm, plan.grid, stream); break;
+    case 16: rc = launch_decode_ng16(q_lat, q_rope, prm, plan.grid, stream); break;
+    case 32: rc = launch_decode_ng32(q_lat, q_rope, prm, plan.grid, stream); break;
+    default: rc = launch_decode_ng48(q_lat, q_rope, prm, plan.grid, stream); break;
   }
   if (rc) return rc;
 

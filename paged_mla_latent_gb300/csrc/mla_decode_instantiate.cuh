@@ -9,8 +9,7 @@
 namespace pmla {
 
 template <int NG, int STAGES>
-int launch_decode_impl(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
-                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream) {
   using LY = DecodeLayout<NG, STAGES>;
   static std::mutex mu;
@@ -27,8 +26,8 @@ int launch_decode_impl(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
       attr_set[dev] = true;
     }
   }
-  mla_decode_kernel<NG, STAGES><<<grid, 192, LY::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
-                                                                        q_rope, prm);
+  mla_decode_kernel<NG, STAGES><<<grid, kDecodeThreads, LY::kSmemBytes, stream>>>(q_lat, q_rope,
+                                                                                   prm);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

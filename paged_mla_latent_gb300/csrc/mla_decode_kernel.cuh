@@ -7,16 +7,20 @@
 //
 // One persistent CTA per SM walks the pieces the scheduler (mla_sched.cuh) gives it.
 // Per tile of 128 cache positions:
-//   producer warp   : loads the 128 row ids, TMA tile::gather4 of the rows into a
-//                     3- (or 2-) stage shared-memory ring.  Latent columns land in four
-//                     128-byte swizzled blocks, rope columns in one 64-byte swizzled
-//                     block.  Positions past the piece gather an out-of-range row and
-//                     read zeros.
-//   MMA thread      : S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
+//   producer warps  : four warps, 32 rows each: load the row ids, then copy every row
+//     (0-3)           with 16-byte cp.async (one instruction per row of latent columns,
+//                     lanes along the row; one per 8 rows of rope columns) straight into
+//                     a 3- (or 2-) stage ring in the 128-byte (latent) / 64-byte (rope)
+//                     swizzled layouts the tensor core reads.  Positions past the piece
+//                     and invalid row ids are zero-filled.  (A TMA tile::gather4 of 128-
+//                     byte boxes issues 5 requests per 4 rows and measured 2-4 TB/s on
+//                     this access pattern; per-thread copies from four warps reach the
+//                     random-row gather limit of ~5.3 TB/s.)
+//   MMA thread      : (warp 4) S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
 //                     M = 128 positions, N = NG query rows, K = 576; FP32 in TMEM),
 //                     then O^T[c, n] += V^T[c, pos] . P^T[pos, n] for the four 128-wide
 //                     value blocks (A = the same cache rows read MN-major).
-//   softmax warps   : read S^T from TMEM (one position per thread), scale, mask,
+//   softmax warps   : (warps 5-8) read S^T from TMEM (one position per thread), scale, mask,
 //                     online softmax in the exp2 domain with a lazily moved reference
 //                     max, and write P as two FP8 planes: hi = e4m3(p) and
 //                     lo = e4m3(256 * (p - hi)), so P reaches the tensor core with
@@ -34,6 +38,8 @@ namespace pmla {
 
 struct DecodeParams {
   SchedParams sp;
+  const uint8_t* kv;       // cache rows, 576 bytes each at a pitch of kv_pitch bytes
+  int64_t kv_pitch;
   const int32_t* kv_indices;
   int64_t kv_indices_len;
   int64_t n_kv_rows;
@@ -91,6 +97,12 @@ enum : int {
   kMiscRed = 256,     // float red[4][NG], then float bcast[NG]
 };
 
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
+constexpr int kDecodeThreads = 32 * (kSoftmaxWarp0 + 4);   // 288
+constexpr int kSoftmaxThread0 = 32 * kSoftmaxWarp0;
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // The reference max moves only when a logit exceeds it by more than kTau (log2 units),
@@ -99,10 +111,8 @@ constexpr float kTau = 8.0f;
 constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
 
 template <int NG, int STAGES>
-__global__ void __launch_bounds__(192, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
-                      const __grid_constant__ CUtensorMap tm_kv_rope,
-                      const __grid_constant__ CUtensorMap tm_q_lat,
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
                       const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams prm) {
   using LY = DecodeLayout<NG, STAGES>;
   constexpr int NPV = LY::kNPV;
@@ -137,7 +147,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(mbase + kMiscFull + 8 * s, 1);
+      mbar_init(mbase + kMiscFull + 8 * s, 32 * kProducerWarps);   // one cp.async arrival per producer thread
       mbar_init(mbase + kMiscEmpty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -151,13 +161,11 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(misc + kMiscTmem), LY::kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32 * 0) {
-    prefetch_tensormap(&tm_kv_lat);
-    prefetch_tensormap(&tm_kv_rope);
+  if (threadIdx.x == 0) {
     prefetch_tensormap(&tm_q_lat);
     prefetch_tensormap(&tm_q_rope);
   }
@@ -168,84 +176,98 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = sbase + LY::kQOff;
   int bad = 0;
 
-  if (warp == 0) {
-    // ===================================================== producer (whole warp)
+  if (warp < kProducerWarps) {
+    // ===================================================== producers (warps 0-3)
     uint32_t it_g = 0;
     int n_piece = 0;
     int q_loads = 0;
     bool aborted = false;
     Piece pc;
-    const int oob_row = static_cast<int>(prm.n_kv_rows < 0x7FFFFFFF ? prm.n_kv_rows : 0x7FFFFFFF);
+    const uint8_t* kv = prm.kv;
+    const int64_t pitch = prm.kv_pitch;
+    const int my_row = 32 * warp + lane;   // this lane's row within a tile (index loads)
     while (!aborted && iter.next(pc, &bad)) {
       const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
-      if (n_piece > 0 &&
-          !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
-        aborted = true;
-        break;
-      }
-      if (lane == 0) {
-        const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
-        mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
+      if (warp == 0 && lane == 0) {
+        // q rows of this piece: one TMA tile load per 128-byte latent block + rope block.
+        // Rows past the unit's real rows belong to other requests (or are out of range and
+        // read zeros); their columns are discarded.
+        if (n_piece > 0 &&
+            !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
+          aborted = true;
+        } else {
+          const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
+          mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
-        tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
+          tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
+          ++q_loads;
+        }
       }
-      ++q_loads;
+      aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
+      if (aborted) break;
       const int64_t kvbase = prm.sp.kv_indptr[pc.b];
+      // row id of this lane's position in tile t (-1: past the piece or invalid)
+      auto load_row = [&](int t) -> int {
+        const int pos = pc.j0 + t * kTile + my_row;
+        if (pos >= pc.j1) return -1;
+        const int64_t gi = kvbase + pos;
+        if (gi < 0 || gi >= prm.kv_indices_len) {
+          atomicOr(prm.err, kErrBadIndex);
+          return -1;
+        }
+        const int v = __ldg(prm.kv_indices + gi);
+        if (v < 0 || static_cast<int64_t>(v) >= prm.n_kv_rows) {
+          atomicOr(prm.err, kErrBadRowId);
+          return -1;
+        }
+        return v;
+      };
+      int rid_next = load_row(0);
       for (int t = 0; t < nt; ++t, ++it_g) {
         const int stage = static_cast<int>(it_g % STAGES);
         const uint32_t use = it_g / STAGES;
-        // row ids of this lane's four positions (before waiting: overlaps the wait)
-        int rowid[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int pos = pc.j0 + t * kTile + 4 * lane + k;
-          int r = oob_row;
-          if (pos < pc.j1) {
-            const int64_t gi = kvbase + pos;
-            if (gi < 0 || gi >= prm.kv_indices_len) {
-              atomicOr(prm.err, kErrBadIndex);
-            } else {
-              const int v = __ldg(prm.kv_indices + gi);
-              if (v < 0 || static_cast<int64_t>(v) >= prm.n_kv_rows)
-                atomicOr(prm.err, kErrBadRowId);
-              else
-                r = v;
-            }
-          }
-          rowid[k] = r;
-        }
+        const int rid = rid_next;
+        if (t + 1 < nt) rid_next = load_row(t + 1);   // overlaps the wait below
         if (use > 0 &&
             !mbar_wait(mbase + kMiscEmpty + 8 * stage, (use - 1) & 1, abort_flag, prm.err)) {
           aborted = true;
           break;
         }
-        const uint32_t full = mbase + kMiscFull + 8 * stage;
-        if (lane == 0) mbar_arrive_expect_tx(full, LY::kStageBytes);
-        __syncwarp();
         const uint32_t st = sbase + stage * LY::kStageBytes;
+        // latent columns: one row per instruction, lane = 16-byte chunk (coalesced 512 B)
+        const uint32_t blk = (lane >> 3) * LY::kLatBlock;
+        const uint32_t chunk = lane & 7;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+          const int r = 32 * warp + j;
+          const int v = __shfl_sync(0xffffffffu, rid, j);
+          const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 16 * lane;
+          const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
+          cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+        }
+        // rope columns: 8 rows x 4 chunks per instruction
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_gather4(st + c * LY::kLatBlock + lane * 512, &tm_kv_lat, c * 128, rowid[0], rowid[1],
-                      rowid[2], rowid[3], full);
-        tma_gather4(st + LY::kRopeOff + lane * 256, &tm_kv_rope, 512, rowid[0], rowid[1], rowid[2],
-                    rowid[3], full);
+        for (int j = 0; j < 4; ++j) {
+          const int rl = 8 * j + (lane >> 2);
+          const int r = 32 * warp + rl;
+          const int c = lane & 3;
+          const int v = __shfl_sync(0xffffffffu, rid, rl);
+          const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 512 + 16 * c;
+          const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+          cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(mbase + kMiscFull + 8 * stage);
       }
       ++n_piece;
     }
     // Drain: every copy this warp issued must land before the CTA may exit.
-    if (lane == 0) {
-      for (int s = 0; s < STAGES; ++s) {
-        if (it_g > static_cast<uint32_t>(s)) {
-          const uint32_t last_use = (it_g - 1 - s) / STAGES;
-          mbar_wait_drain(mbase + kMiscFull + 8 * s, last_use & 1);
-        }
-      }
-      if (q_loads > 0) mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
-    }
+    cp_async_wait_all();
+    if (warp == 0 && lane == 0 && q_loads > 0)
+      mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ===================================================== MMA issuer (one thread)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
@@ -291,6 +313,9 @@ __global__ void __launch_bounds__(192, 1)
             aborted = true;
             break;
           }
+          // the stage was written by cp.async (generic proxy); the tensor core reads it
+          // through the async proxy
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t st = sbase + stage * LY::kStageBytes;
           const uint32_t d = tmem + (it_g & 1) * LY::kSStride;
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(192, 1)
           const int64_t row0 = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) * H + pc.g * NG;
           const bool direct = pc.direct;
           const bool slot_ok = direct || (pc.slot >= 0 && pc.slot < prm.n_slots);
-          if (!slot_ok && threadIdx.x == 64) atomicOr(prm.err, kErrBadOutput);
+          if (!slot_ok && threadIdx.x == kSoftmaxThread0) atomicOr(prm.err, kErrBadOutput);
 #pragma unroll
           for (int bk = 0; bk < 4; ++bk) {
             const int c = bk * 128 + prow;
@@ -527,7 +552,7 @@ __global__ void __launch_bounds__(192, 1)
   if (bad && (threadIdx.x & 31) == 0) atomicOr(prm.err, kErrBadIndptr);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, LY::kTmemCols);
   }

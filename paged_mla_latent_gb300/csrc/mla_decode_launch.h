@@ -10,14 +10,11 @@ namespace pmla {
 
 // Launch mla_decode_kernel<NG, stages> on `grid` CTAs; sets the kernel's dynamic shared
 // memory limit on first use per device.  Returns 0 or an mla_status_t.
-int launch_decode_ng16(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
-                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+int launch_decode_ng16(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream);
-int launch_decode_ng32(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
-                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+int launch_decode_ng32(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream);
-int launch_decode_ng48(const CUtensorMap& kv_lat, const CUtensorMap& kv_rope,
-                       const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+int launch_decode_ng48(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream);
 
 }  // namespace pmla
