@@ -306,8 +306,19 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
   const int64_t units = static_cast<int64_t>(cs.B) * plan.groups;
-  dim3 mgrid(static_cast<unsigned>(units * plan.NG), kDV / kMergeCols);
-  mla_split_merge_kernel<<<mgrid, 256, 0, stream>>>(mp);
+  // Programmatic dependent launch: the merge grid is scheduled while the decode grid
+  // runs and waits on the device (griddepcontrol.wait) for the partials.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), kDV / kMergeCols);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla_split_merge_kernel, mp) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -353,7 +364,7 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
   prm.lse_out = lse_out ? static_cast<float*>(lse_out->ptr) : nullptr;
   prm.err = error_word;
   dim3 grid(static_cast<unsigned>(n_out * H), kDV / kMergeCols);
-  mla_csr_merge_kernel<<<grid, 256, 0, stream>>>(prm);
+  mla_csr_merge_kernel<<<grid, kMergeThreads, 0, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -58,6 +58,23 @@ struct DecodeParams {
   int* err;
 };
 
+// Misc region offsets (bytes from kMiscOff).
+enum : int {
+  kMiscFull = 0,      // full[STAGES]   (8 B each, STAGES <= 4)
+  kMiscEmpty = 32,    // empty[STAGES]
+  kMiscSFull = 64,    // s_full[2]
+  kMiscPFull = 80,    // p_full[2]
+  kMiscPv = 96,       // pv_done[2]: PV of even / odd tiles (a single barrier would let a
+                      // waiter two completions behind mistake an old phase for its own)
+  kMiscQFull = 112,
+  kMiscQEmpty = 120,
+  kMiscDrain = 184,
+  kMiscTmem = 128,    // u32 tensor memory base
+  kMiscAbort = 132,   // int abort flag
+  kMiscRowOff = 192,  // int64 row output offsets [NG] (NG <= 48 -> 384 bytes, to 576)
+  kMiscRed = 640,     // float red[4][NG], then float scale[NG]
+};
+
 template <int NG, int STAGES>
 struct DecodeLayout {
   static constexpr int kNPV = 2 * NG;                 // PV N: hi plane + lo plane
@@ -72,6 +89,7 @@ struct DecodeLayout {
   static constexpr int kPBytes = kPInRope ? 0 : 2 * kNPV * 128;
   static constexpr int kMiscOff = kPOff + kPBytes;
   static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 2048;
+  static_assert(kMiscRed + 5 * NG * 4 <= kMiscBytes, "misc region overflow");
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
   // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
   static constexpr int kSStride = (NG + 31) / 32 * 32;
@@ -82,25 +100,21 @@ struct DecodeLayout {
   static_assert(NG % 16 == 0 && NG <= 48, "group rows must be 16, 32 or 48");
 };
 
-// Misc region offsets (bytes from kMiscOff).
-enum : int {
-  kMiscFull = 0,      // full[STAGES]   (8 B each, STAGES <= 4)
-  kMiscEmpty = 32,    // empty[STAGES]
-  kMiscSFull = 64,    // s_full[2]
-  kMiscPFull = 80,    // p_full[2]
-  kMiscPv = 96,       // pv_done
-  kMiscQFull = 104,
-  kMiscQEmpty = 112,
-  kMiscDrain = 120,
-  kMiscTmem = 128,    // u32 tensor memory base
-  kMiscAbort = 132,   // int abort flag
-  kMiscRed = 256,     // float red[4][NG], then float bcast[NG]
-};
 
-constexpr int kProducerWarps = 4;
+// Twelve warps in three warpgroups.  Warpgroups 0 and 1 (producers + MMA issuer) give
+// registers back with setmaxnreg.dec; warpgroup 2 (softmax) takes them with .inc.
+//   warps 0-3, 5-7 : producers (7 warps)      warp 4 : MMA issuer, TMEM owner
+//   warps 8-11     : softmax / epilogue (TMEM lane quadrants 0-3)
+constexpr int kProducerWarps = 7;
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kRowsPerProducer = (kTile + kProducerWarps - 1) / kProducerWarps;   // 19
 constexpr int kMmaWarp = 4;
-constexpr int kSoftmaxWarp0 = 5;
-constexpr int kDecodeThreads = 32 * (kSoftmaxWarp0 + 4);   // 288
+constexpr int kSoftmaxWarp0 = 8;
+constexpr int kDecodeThreads = 32 * (kSoftmaxWarp0 + 4);   // 384
+constexpr int kRegsLow = 120;     // producers and MMA issuer
+constexpr int kRegsHigh = 224;   // softmax
+static_assert(8 * 32 * kRegsLow + 4 * 32 * kRegsHigh <= kDecodeThreads * 168,
+              "register split exceeds the launch allocation");
 constexpr int kSoftmaxThread0 = 32 * kSoftmaxWarp0;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(mbase + kMiscFull + 8 * s, 32 * kProducerWarps);   // one cp.async arrival per producer thread
+      mbar_init(mbase + kMiscFull + 8 * s, kProducerThreads);   // one cp.async arrival per producer thread
       mbar_init(mbase + kMiscEmpty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -155,6 +169,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(mbase + kMiscPFull + 8 * s, 4);
     }
     mbar_init(mbase + kMiscPv, 1);
+    mbar_init(mbase + kMiscPv + 8, 1);
     mbar_init(mbase + kMiscQFull, 1);
     mbar_init(mbase + kMiscQEmpty, 1);
     mbar_init(mbase + kMiscDrain, 1);
@@ -172,185 +187,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Let the merge grid (launched with programmatic serialization) get scheduled; it
+  // waits for this grid's completion before reading anything it wrote.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   const uint32_t tmem = *tmem_slot;
   const uint32_t sQ = sbase + LY::kQOff;
   int bad = 0;
 
-  if (warp < kProducerWarps) {
-    // ===================================================== producers (warps 0-3)
-    uint32_t it_g = 0;
-    int n_piece = 0;
-    int q_loads = 0;
-    bool aborted = false;
-    Piece pc;
-    const uint8_t* kv = prm.kv;
-    const int64_t pitch = prm.kv_pitch;
-    const int my_row = 32 * warp + lane;   // this lane's row within a tile (index loads)
-    while (!aborted && iter.next(pc, &bad)) {
-      const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
-      if (warp == 0 && lane == 0) {
-        // q rows of this piece: one TMA tile load per 128-byte latent block + rope block.
-        // Rows past the unit's real rows belong to other requests (or are out of range and
-        // read zeros); their columns are discarded.
-        if (n_piece > 0 &&
-            !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
-          aborted = true;
-        } else {
-          const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
-          mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
-          tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
-          ++q_loads;
-        }
-      }
-      aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
-      if (aborted) break;
-      const int64_t kvbase = prm.sp.kv_indptr[pc.b];
-      // row id of this lane's position in tile t (-1: past the piece or invalid)
-      auto load_row = [&](int t) -> int {
-        const int pos = pc.j0 + t * kTile + my_row;
-        if (pos >= pc.j1) return -1;
-        const int64_t gi = kvbase + pos;
-        if (gi < 0 || gi >= prm.kv_indices_len) {
-          atomicOr(prm.err, kErrBadIndex);
-          return -1;
-        }
-        const int v = __ldg(prm.kv_indices + gi);
-        if (v < 0 || static_cast<int64_t>(v) >= prm.n_kv_rows) {
-          atomicOr(prm.err, kErrBadRowId);
-          return -1;
-        }
-        return v;
-      };
-      int rid_next = load_row(0);
-      for (int t = 0; t < nt; ++t, ++it_g) {
-        const int stage = static_cast<int>(it_g % STAGES);
-        const uint32_t use = it_g / STAGES;
-        const int rid = rid_next;
-        if (t + 1 < nt) rid_next = load_row(t + 1);   // overlaps the wait below
-        if (use > 0 &&
-            !mbar_wait(mbase + kMiscEmpty + 8 * stage, (use - 1) & 1, abort_flag, prm.err)) {
-          aborted = true;
-          break;
-        }
-        const uint32_t st = sbase + stage * LY::kStageBytes;
-        // latent columns: one row per instruction, lane = 16-byte chunk (coalesced 512 B)
-        const uint32_t blk = (lane >> 3) * LY::kLatBlock;
-        const uint32_t chunk = lane & 7;
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-          const int r = 32 * warp + j;
-          const int v = __shfl_sync(0xffffffffu, rid, j);
-          const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 16 * lane;
-          const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
-          cp_async_16(dst, src, v >= 0 ? 16u : 0u);
-        }
-        // rope columns: 8 rows x 4 chunks per instruction
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rl = 8 * j + (lane >> 2);
-          const int r = 32 * warp + rl;
-          const int c = lane & 3;
-          const int v = __shfl_sync(0xffffffffu, rid, rl);
-          const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 512 + 16 * c;
-          const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-          cp_async_16(dst, src, v >= 0 ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(mbase + kMiscFull + 8 * stage);
-      }
-      ++n_piece;
-    }
-    // Drain: every copy this warp issued must land before the CTA may exit.
-    cp_async_wait_all();
-    if (warp == 0 && lane == 0 && q_loads > 0)
-      mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ===================================================== MMA issuer (one thread)
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
-      constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, false);
-      uint32_t it_g = 0;
-      int n_piece = 0;
-      bool aborted = false;
-      Piece pc;
-      auto issue_pv = [&](uint32_t i, bool first_of_piece) -> bool {
-        const int sb = i & 1;
-        const int stage = static_cast<int>(i % STAGES);
-        if (!mbar_wait(mbase + kMiscPFull + 8 * sb, (i >> 1) & 1, abort_flag, prm.err)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + stage * LY::kStageBytes;
-        const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * 128;
-#pragma unroll
-        for (int bk = 0; bk < 4; ++bk) {
-          const uint32_t d = tmem + LY::kOBase + bk * NPV;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
-            const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
-            // B = P: NPV rows x 32 positions (K-major, 128-byte swizzle)
-            const uint64_t b = smem_desc(pbuf + kk * 32, 16, 1024, kSw128);
-            mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
-          }
-        }
-        mma_commit(mbase + kMiscEmpty + 8 * stage);
-        mma_commit(mbase + kMiscPv);
-        return true;
-      };
-      while (!aborted && iter.next(pc, &bad)) {
-        const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
-        if (!mbar_wait(mbase + kMiscQFull, n_piece & 1, abort_flag, prm.err)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        for (int t = 0; t < nt; ++t, ++it_g) {
-          const int stage = static_cast<int>(it_g % STAGES);
-          const uint32_t use = it_g / STAGES;
-          if (!mbar_wait(mbase + kMiscFull + 8 * stage, use & 1, abort_flag, prm.err)) {
-            aborted = true;
-            break;
-          }
-          // the stage was written by cp.async (generic proxy); the tensor core reads it
-          // through the async proxy
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t st = sbase + stage * LY::kStageBytes;
-          const uint32_t d = tmem + (it_g & 1) * LY::kSStride;
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {   // latent columns 0..511, 32 per MMA
-            const uint64_t a = smem_desc(st + (kk >> 2) * LY::kLatBlock + (kk & 3) * 32, 16, 1024, kSw128);
-            const uint64_t b = smem_desc(sQ + (kk >> 2) * NG * 128 + (kk & 3) * 32, 16, 1024, kSw128);
-            mma_f8(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {    // rope columns 512..575
-            const uint64_t a = smem_desc(st + LY::kRopeOff + kk * 32, 16, 512, kSw64);
-            const uint64_t b = smem_desc(sQ + 4 * NG * 128 + kk * 32, 16, 512, kSw64);
-            mma_f8(d, a, b, idesc_qk, 1u);
-          }
-          mma_commit(mbase + kMiscSFull + 8 * (it_g & 1));
-          if (t == nt - 1) mma_commit(mbase + kMiscQEmpty);
-          if (t > 0 && !issue_pv(it_g - 1, t == 1)) {
-            aborted = true;
-            break;
-          }
-        }
-        if (aborted) break;
-        if (!issue_pv(it_g - 1, nt == 1)) {
-          aborted = true;
-          break;
-        }
-        ++n_piece;
-      }
-      // Drain: all MMAs must complete before tensor memory is released.
-      mma_commit(mbase + kMiscDrain);
-      mbar_wait_drain(mbase + kMiscDrain, 0);
-    }
-    __syncwarp();
-  } else {
+  if (warp >= kSoftmaxWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ===================================================== softmax + epilogue (4 warps)
     const int q4 = warp & 3;                 // TMEM lane quadrant this warp may access
     const int prow = 32 * q4 + lane;         // position within the tile == TMEM lane
@@ -422,7 +268,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           bar_sync(1, 128);
           if (t > 0) {
             // O holds this piece's earlier tiles: wait for the last PV, then rescale
-            mbar_wait(mbase + kMiscPv, (it_g - 1) & 1, abort_flag, prm.err);
+            mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag, prm.err);
             tc_fence_after();
 #pragma unroll
             for (int bk = 0; bk < 4; ++bk) {
@@ -470,7 +316,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
         if (t == nt - 1) {
           // ------------------------------------------------ piece epilogue
-          mbar_wait(mbase + kMiscPv, it_g & 1, abort_flag, prm.err);
+          mbar_wait(mbase + kMiscPv + 8 * (it_g & 1), (it_g >> 1) & 1, abort_flag, prm.err);
           tc_fence_after();
 #pragma unroll
           for (int n = 0; n < NG; ++n) {
@@ -480,22 +326,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (lane == 0) red[q4 * NG + n] = v;
           }
           bar_sync(1, 128);
-          float scale_n[NG];
-#pragma unroll
-          for (int n = 0; n < NG; ++n) {
-            const float l = (red[n] + red[NG + n]) + (red[2 * NG + n] + red[3 * NG + n]);
-            scale_n[n] = (l > 0.f) ? kv_scale / l : 0.f;
-            l_acc[n] = l;   // keep the total for the lse below
-          }
-          bar_sync(1, 128);
-          const int64_t row0 = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) * H + pc.g * NG;
+          // one thread per row: normaliser, lse and output offset of that row
+          float* s_scale = red + 4 * NG;                                   // [NG]
+          int64_t* s_off = reinterpret_cast<int64_t*>(misc + kMiscRowOff);  // [NG]
           const bool direct = pc.direct;
           const bool slot_ok = direct || (pc.slot >= 0 && pc.slot < prm.n_slots);
-          if (!slot_ok && threadIdx.x == kSoftmaxThread0) atomicOr(prm.err, kErrBadOutput);
+          if (prow < NG) {
+            const int n = prow;
+            const float l = (red[n] + red[NG + n]) + (red[2 * NG + n] + red[3 * NG + n]);
+            float m = 0.f;
 #pragma unroll
+            for (int k = 0; k < NG; ++k) m = (k == n) ? m_ref[k] : m;
+            const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+            int64_t off = -1;
+            if (n < pc.rows) {
+              if (direct) {
+                const int64_t r = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) * H + pc.g * NG + n;
+                if (r < prm.n_q_rows) {
+                  off = (r / H) * prm.o_stride_tok + (r % H) * prm.o_stride_head;
+                  if (prm.lse_out) prm.lse_out[r] = lse;
+                } else {
+                  atomicOr(prm.err, kErrBadOutput);
+                }
+              } else if (slot_ok) {
+                off = (pc.slot * NG + n) * kDV;
+                prm.part_lse[pc.slot * NG + n] = lse;
+              } else {
+                atomicOr(prm.err, kErrBadOutput);
+              }
+            }
+            s_scale[n] = (l > 0.f) ? kv_scale / l : 0.f;
+            s_off[n] = off;
+          }
+          bar_sync(1, 128);
+          // normalised output: thread = value column c within each 128-wide block
+          const bool to_bf16 = direct && !prm.o_fp32;
+          float* fdst = direct ? reinterpret_cast<float*>(prm.o) : prm.part_o;
+          __nv_bfloat16* hdst = reinterpret_cast<__nv_bfloat16*>(prm.o);
+#pragma unroll 1
           for (int bk = 0; bk < 4; ++bk) {
             const int c = bk * 128 + prow;
-#pragma unroll
+#pragma unroll 1
             for (int ch = 0; ch < NG / 16; ++ch) {
               float hi[16], lo[16];
               tmem_ld16(tl + LY::kOBase + bk * NPV + 16 * ch, hi);
@@ -504,51 +375,232 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
               for (int k = 0; k < 16; ++k) {
                 const int n = 16 * ch + k;
-                if (n < pc.rows) {
-                  const float val = (hi[k] + lo[k] * (1.0f / kLoScale)) * scale_n[n];
-                  if (direct) {
-                    const int64_t r = row0 + n;
-                    if (r < prm.n_q_rows) {
-                      const int64_t off = (r / H) * prm.o_stride_tok + (r % H) * prm.o_stride_head + c;
-                      if (prm.o_fp32)
-                        reinterpret_cast<float*>(prm.o)[off] = val;
-                      else
-                        reinterpret_cast<__nv_bfloat16*>(prm.o)[off] = __float2bfloat16_rn(val);
-                    }
-                  } else if (slot_ok) {
-                    prm.part_o[(pc.slot * NG + n) * kDV + c] = val;
-                  }
+                const int64_t off = s_off[n];
+                if (off >= 0) {
+                  const float val = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[n];
+                  if (to_bf16)
+                    hdst[off + c] = __float2bfloat16_rn(val);
+                  else
+                    fdst[off + c] = val;
                 }
               }
             }
           }
-          if (prow < pc.rows) {
-            const int n = prow;
-            float l = 0.f, m = 0.f;
-#pragma unroll
-            for (int k = 0; k < NG; ++k)
-              if (k == n) {
-                l = l_acc[k];
-                m = m_ref[k];
-              }
-            const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
-            if (direct) {
-              const int64_t r = row0 + n;
-              if (r < prm.n_q_rows) {
-                if (prm.lse_out) prm.lse_out[r] = lse;
-              } else {
-                atomicOr(prm.err, kErrBadOutput);
-              }
-            } else if (slot_ok) {
-              prm.part_lse[pc.slot * NG + n] = lse;
-            }
-          }
+          bar_sync(1, 128);   // s_off / s_scale are rewritten by the next piece
           tc_fence_before();
         }
       }
     }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp != kMmaWarp) {
+      // ===================================================== producers (7 warps)
+      const int pw = warp < kMmaWarp ? warp : warp - 1;   // producer index 0..6
+      uint32_t it_g = 0;
+      int n_piece = 0;
+      int q_loads = 0;
+      bool aborted = false;
+      Piece pc;
+      const uint8_t* kv = prm.kv;
+      const int64_t pitch = prm.kv_pitch;
+      // Producer pw copies tile rows r = pw + 7 j (j < rows_w); lane j loads row j's id.
+      const int rows_w = (kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 19 or 18
+      while (!aborted && iter.next(pc, &bad)) {
+        const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+        if (warp == 0 && lane == 0) {
+          // q rows of this piece: one TMA tile load per 128-byte latent block + rope block.
+          // Rows past the unit's real rows belong to other requests (or are out of range and
+          // read zeros); their columns are discarded.
+          if (n_piece > 0 &&
+              !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
+            aborted = true;
+          } else {
+            const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
+            mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
+  #pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
+            tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
+            ++q_loads;
+          }
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
+        if (aborted) break;
+        const int64_t kvbase = prm.sp.kv_indptr[pc.b];
+        // row id of row j of this warp in tile t (-1: past the piece or invalid)
+        auto load_row = [&](int t, int j) -> int {
+          if (j >= rows_w) return -1;
+          const int pos = pc.j0 + t * kTile + pw + kProducerWarps * j;
+          if (pos >= pc.j1) return -1;
+          const int64_t gi = kvbase + pos;
+          if (gi < 0 || gi >= prm.kv_indices_len) {
+            atomicOr(prm.err, kErrBadIndex);
+            return -1;
+          }
+          const int v = __ldg(prm.kv_indices + gi);
+          if (v < 0 || static_cast<int64_t>(v) >= prm.n_kv_rows) {
+            atomicOr(prm.err, kErrBadRowId);
+            return -1;
+          }
+          return v;
+        };
+        int nxt = load_row(0, lane);
+        for (int t = 0; t < nt; ++t, ++it_g) {
+          const int stage = static_cast<int>(it_g % STAGES);
+          const uint32_t use = it_g / STAGES;
+          const int rid = nxt;
+          if (t + 1 < nt) nxt = load_row(t + 1, lane);   // next tile's row ids overlap the wait
+          if (use > 0 &&
+              !mbar_wait(mbase + kMiscEmpty + 8 * stage, (use - 1) & 1, abort_flag, prm.err)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t st = sbase + stage * LY::kStageBytes;
+          // latent columns: one row per instruction, lane = 16-byte chunk (coalesced 512 B)
+          const uint32_t blk = (lane >> 3) * LY::kLatBlock;
+          const uint32_t chunk = lane & 7;
+  #pragma unroll 4
+          for (int j = 0; j < rows_w; ++j) {
+            const int r = pw + kProducerWarps * j;
+            const int v = __shfl_sync(0xffffffffu, rid, j);
+            const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 16 * lane;
+            const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
+            cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+          }
+          // rope columns: 8 rows x 4 chunks per instruction
+  #pragma unroll
+          for (int m = 0; m < (kRowsPerProducer + 7) / 8; ++m) {
+            const int j = 8 * m + (lane >> 2);
+            const int c = lane & 3;
+            const int v = __shfl_sync(0xffffffffu, rid, j);
+            if (j < rows_w) {
+              const int r = pw + kProducerWarps * j;
+              const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 512 + 16 * c;
+              const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+              cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(mbase + kMiscFull + 8 * stage);
+        }
+        ++n_piece;
+      }
+      // Drain: every copy this warp issued must land before the CTA may exit.
+      cp_async_wait_all();
+      if (warp == 0 && lane == 0 && q_loads > 0)
+        mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
+      __syncwarp();
+    } else {
+      // ===================================================== MMA issuer (one thread)
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
+        constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, false);
+        int n_piece = 0;
+        Piece pc;
+        auto issue_pv = [&](uint32_t i, bool first_of_piece) {
+          const int sb = i & 1;
+          const int stage = static_cast<int>(i % STAGES);
+          tc_fence_after();
+          const uint32_t st = sbase + stage * LY::kStageBytes;
+          const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * 128;
+  #pragma unroll
+          for (int bk = 0; bk < 4; ++bk) {
+            const uint32_t d = tmem + LY::kOBase + bk * NPV;
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
+              const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
+              // B = P: NPV rows x 32 positions (K-major, 128-byte swizzle)
+              const uint64_t b = smem_desc(pbuf + kk * 32, 16, 1024, kSw128);
+              mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(mbase + kMiscEmpty + 8 * stage);
+          mma_commit(mbase + kMiscPv + 8 * (i & 1));
+        };
+        auto issue_qk = [&](uint32_t i) {
+          const int stage = static_cast<int>(i % STAGES);
+          // the stage was written by cp.async (generic proxy); the tensor core reads it
+          // through the async proxy
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t st = sbase + stage * LY::kStageBytes;
+          const uint32_t d = tmem + (i & 1) * LY::kSStride;
+  #pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {   // latent columns 0..511, 32 per MMA
+            const uint64_t a = smem_desc(st + (kk >> 2) * LY::kLatBlock + (kk & 3) * 32, 16, 1024, kSw128);
+            const uint64_t b = smem_desc(sQ + (kk >> 2) * NG * 128 + (kk & 3) * 32, 16, 1024, kSw128);
+            mma_f8(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+  #pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {    // rope columns 512..575
+            const uint64_t a = smem_desc(st + LY::kRopeOff + kk * 32, 16, 512, kSw64);
+            const uint64_t b = smem_desc(sQ + 4 * NG * 128 + kk * 32, 16, 512, kSw64);
+            mma_f8(d, a, b, idesc_qk, 1u);
+          }
+          mma_commit(mbase + kMiscSFull + 8 * (i & 1));
+        };
+        // Issue loop.  QK of tile q needs its cache rows (full), the piece's q rows and a
+        // free S buffer (PV of tile q-2 issued); PV of tile p needs P (p_full).  Whichever
+        // is ready goes first, PV preferred: it releases a ring stage to the producers.
+        bool pv_first[2] = {false, false};
+        uint32_t q_next = 0, p_next = 0;   // next tile for QK / PV (CTA-wide numbering)
+        bool have_piece = false, q_ready = false;
+        int nt = 0, t_in = 0;
+        unsigned long long idle_since = 0;
+        while (true) {
+          while (!have_piece || t_in >= nt) {
+            if (!iter.next(pc, &bad)) {
+              have_piece = false;
+              break;
+            }
+            have_piece = true;
+            nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+            t_in = 0;
+            q_ready = false;
+          }
+          if (!have_piece && p_next == q_next) break;   // everything issued
+          bool progressed = false;
+          if (p_next < q_next && mbar_test(mbase + kMiscPFull + 8 * (p_next & 1), (p_next >> 1) & 1)) {
+            issue_pv(p_next, pv_first[p_next & 1]);
+            ++p_next;
+            progressed = true;
+          } else if (have_piece && q_next <= p_next + 1) {
+            if (t_in == 0 && !q_ready) q_ready = mbar_test(mbase + kMiscQFull, n_piece & 1);
+            const int stage = static_cast<int>(q_next % STAGES);
+            if ((t_in > 0 || q_ready) &&
+                mbar_test(mbase + kMiscFull + 8 * stage, (q_next / STAGES) & 1)) {
+              issue_qk(q_next);
+              pv_first[q_next & 1] = (t_in == 0);
+              if (t_in == nt - 1) {
+                mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q rows
+                ++n_piece;
+              }
+              ++q_next;
+              ++t_in;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            idle_since = 0;
+          } else {
+            if (*abort_flag) break;
+            const unsigned long long now = globaltimer_ns();
+            if (idle_since == 0) {
+              idle_since = now;
+            } else if (now - idle_since > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(prm.err, kErrTimeout);
+              break;
+            }
+          }
+        }
+        // Drain: all MMAs must complete before tensor memory is released.
+        mma_commit(mbase + kMiscDrain);
+        mbar_wait_drain(mbase + kMiscDrain, 0);
+      }
+      __syncwarp();
+    }
   }
-
   if (bad && (threadIdx.x & 31) == 0) atomicOr(prm.err, kErrBadIndptr);
   tc_fence_before();
   __syncthreads();

@@ -18,8 +18,10 @@
 
 namespace pmla {
 
-constexpr int kMergeWarps = 8;
-constexpr int kMergeCols = 128;   // columns per block (32 lanes x 4)
+constexpr int kMergeThreads = 512;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeCols = 32;           // value columns per block (one per lane)
+constexpr int kMergeMaxParts = 1024;     // partials held in shared memory per pass
 
 struct MergeOut {
   void* o;
@@ -28,71 +30,94 @@ struct MergeOut {
   float* lse;         // element for this (row, head), or null
 };
 
-// Merge `count` partials given by slot(k); partial k's o row starts at o_of(k) and its lse
-// is lse_of(k).  Called by all threads of a 256-thread block.
+// Merge `count` partials of one (row, head) for columns col0 .. col0+31.  lse_of(k) and
+// o_of(k) give partial k's log-sum-exp and the start of its 512 normalised values.
+// The block first turns the lse values into weights w_k = exp(lse_k - M) (shared by
+// all its threads), then warp w accumulates partials w, w+8, ... with one column per lane,
+// every load of a warp independent of the others.
 template <class OOf, class LseOf>
 __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const MergeOut& out,
                                      int col0) {
+  __shared__ float s_w[kMergeMaxParts];
+  __shared__ float s_red[kMergeWarps];
   __shared__ float s_acc[kMergeWarps][kMergeCols];
-  __shared__ float s_m[kMergeWarps];
-  __shared__ float s_w[kMergeWarps];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  float m = -INFINITY, wsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = warp; k < count; k += kMergeWarps) {
-    const float l = lse_of(k);
-    if (l == -INFINITY) continue;
-    const float4 v = *reinterpret_cast<const float4*>(o_of(k) + col0 + 4 * lane);
-    if (l > m) {
-      const float f = (m == -INFINITY) ? 0.f : __expf(m - l);
-      wsum = wsum * f + 1.f;
-      acc.x = acc.x * f + v.x;
-      acc.y = acc.y * f + v.y;
-      acc.z = acc.z * f + v.z;
-      acc.w = acc.w * f + v.w;
-      m = l;
-    } else {
-      const float w = __expf(l - m);
-      wsum += w;
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+  float acc = 0.f, M = -INFINITY, wsum = 0.f;
+  for (int base = 0; base < count || base == 0; base += kMergeMaxParts) {
+    const int n = min(count - base, kMergeMaxParts);
+    // 1. max of this pass's lse values
+    float m = -INFINITY;
+    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
+      const float l = lse_of(base + k);
+      s_w[k] = l;
+      m = fmaxf(m, l);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float pm = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) pm = fmaxf(pm, s_red[w]);
+    __syncthreads();
+    if (pm == -INFINITY) continue;            // nothing attended in this pass
+    // rescale what earlier passes accumulated to the new running max
+    const float M_new = fmaxf(M, pm);
+    const float f = (M == -INFINITY) ? 0.f : __expf(M - M_new);
+    acc *= f;
+    wsum *= f;
+    M = M_new;
+    // 2. weights
+    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
+      const float l = s_w[k];
+      s_w[k] = (l == -INFINITY) ? 0.f : __expf(l - M);
+    }
+    __syncthreads();
+    float ws = 0.f;
+    for (int k = lane; k < n; k += 32) ws += s_w[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    wsum += ws;   // every warp computes the same total
+    // 3. weighted sum of the value rows: up to 8 independent loads in flight per warp
+    float a = 0.f;
+    for (int k0 = warp; k0 < n; k0 += 8 * kMergeWarps) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * kMergeWarps;
+        v[u] = (k < n) ? o_of(base + k)[col0 + lane] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * kMergeWarps;
+        if (k < n) a += s_w[k] * v[u];
+      }
+    }
+    acc += a;
+    __syncthreads();   // s_w is rewritten by the next pass
   }
-  s_acc[warp][4 * lane + 0] = acc.x;
-  s_acc[warp][4 * lane + 1] = acc.y;
-  s_acc[warp][4 * lane + 2] = acc.z;
-  s_acc[warp][4 * lane + 3] = acc.w;
-  if (lane == 0) {
-    s_m[warp] = m;
-    s_w[warp] = wsum;
-  }
+  s_acc[warp][lane] = acc;
   __syncthreads();
   if (threadIdx.x < kMergeCols) {
-    float M = -INFINITY;
+    float val = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
-    float tot = 0.f, val = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kMergeWarps; ++w) {
-        if (s_m[w] == -INFINITY) continue;
-        const float f = __expf(s_m[w] - M);
-        tot += s_w[w] * f;
-        val += s_acc[w][threadIdx.x] * f;
-      }
-      val /= tot;
-    }
+    for (int w = 0; w < kMergeWarps; ++w) val += s_acc[w][threadIdx.x];
+    val = (wsum > 0.f) ? val / wsum : 0.f;
     const int64_t off = out.o_off + col0 + threadIdx.x;
     if (out.o_fp32)
       reinterpret_cast<float*>(out.o)[off] = val;
     else
       reinterpret_cast<__nv_bfloat16*>(out.o)[off] = __float2bfloat16_rn(val);
     if (threadIdx.x == 0 && out.lse != nullptr && col0 == 0)
-      *out.lse = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
+      *out.lse = (wsum > 0.f) ? M + __logf(wsum) : -INFINITY;
   }
+}
+
+// Wait until the grid this one depends on (launched before it on the stream with
+// programmatic serialization) has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 struct SplitMergeParams {
@@ -108,10 +133,10 @@ struct SplitMergeParams {
   int* err;
 };
 
-// grid = (units * NG, 4), block = 256.  Merges the units the scheduler split and writes
+// grid = (units * NG, 512 / 32), block = 256.  Merges the units the scheduler split and writes
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
-__global__ void __launch_bounds__(256) mla_split_merge_kernel(const SplitMergeParams prm) {
+__global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const SplitMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
   const int64_t u = blockIdx.x / NG;
@@ -143,9 +168,10 @@ __global__ void __launch_bounds__(256) mla_split_merge_kernel(const SplitMergePa
       return;
     }
   }
+  grid_dependency_wait();   // partials come from the decode kernel
   // (L == 0: no partial exists; count = 0 writes o = 0, lse = -inf)
   const int splits = sp.splits;
-  auto o_of = [&](int k) { return prm.part_o + ((first + k) * NG + n) * kDV; };
+  auto o_of = [&](int k) -> const float* { return prm.part_o + ((first + k) * NG + n) * kDV; };
   auto lse_of = [&](int k) -> float {
     if (splits > 0) {   // fixed policy: piece k of a short unit may be empty
       int j0, j1;
@@ -173,8 +199,8 @@ struct CsrMergeParams {
   int* err;
 };
 
-// grid = (n_out * H, 4), block = 256.  Public merge with an explicit reduce map.
-__global__ void __launch_bounds__(256) mla_csr_merge_kernel(const CsrMergeParams prm) {
+// grid = (n_out * H, 512 / 32), block = 256.  Public merge with an explicit reduce map.
+__global__ void __launch_bounds__(kMergeThreads) mla_csr_merge_kernel(const CsrMergeParams prm) {
   const int64_t rr = blockIdx.x / prm.H;
   const int h = static_cast<int>(blockIdx.x - rr * prm.H);
   const int col0 = blockIdx.y * kMergeCols;
@@ -190,7 +216,7 @@ __global__ void __launch_bounds__(256) mla_csr_merge_kernel(const CsrMergeParams
     const int64_t s = prm.reduce_idx[beg + k];
     return s;
   };
-  auto o_of = [&](int k) {
+  auto o_of = [&](int k) -> const float* {
     int64_t s = slot(k);
     if (s < 0 || s >= prm.P) s = 0;   // flagged by lse_of, weight 0
     return prm.o_parts + s * prm.op_stride_p + h * prm.op_stride_h;

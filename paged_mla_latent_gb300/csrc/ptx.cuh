@@ -68,11 +68,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false (without
-// waiting) once the CTA's abort flag is up, and raises it itself after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err_word) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Slow path of mbar_wait: poll until the phase completes, the CTA's abort flag goes up, or
+// kWaitLimitNs passes (then raise the flag and the device error bit).  Kept out of line
+// so that the many call sites stay small.
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            int* err_word) {
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (*abort_flag) return false;
@@ -83,6 +96,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (without
+// waiting) once the CTA's abort flag is up, and raises it itself after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err_word);
 }
 
 // Same, ignoring the abort flag: used only while draining in-flight copies / MMAs

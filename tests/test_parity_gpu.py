@@ -275,3 +275,26 @@ def test_context_shard_merge_small(pm):
     gu.compare(o, lse, o_ref, lse_ref, what="shard-merge")
     assert torch.allclose(o.float(), o_full, atol=1e-2, rtol=1e-2)
     assert torch.allclose(lse, lse_full, atol=1e-3)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_running_max_rescale_every_tile(pm, splits):
+    """Cache rows rise tile by tile so that, for heads 0-5, every 128-position tile's logits
+    exceed the previous tile's by ~10 nats (more than the 2^8 headroom of the reference
+    max): the kernel must move its reference and rescale the accumulated output on every
+    tile.  Heads 6-11 see a slow rise (no rescale).  Values carry random latent parts."""
+    L = 15 * 128 + 37
+    case = mla_inputs.make_custom([L, 300], H=12, seed=19, q_scale=1.0, kv_scale=1.0)
+    f8 = lambda x: torch.tensor([x]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    idx = case.kv_indices[:L].long()
+    rise = torch.tensor([f8(0.25 * min(j // 128, 15)) for j in range(L)], dtype=torch.uint8)
+    keys = case.kv.clone()
+    keys[idx, :] = rise[:, None].expand(L, 576)          # constant rows rising per tile
+    keys[idx, 300:512] = case.kv[idx, 300:512]           # random value columns (not in logits)
+    q = case.q.clone()
+    q[0, :6, :] = f8(1.0)
+    q[0, 6:, :] = f8(0.125)
+    q[0, :, 300:512] = 0                                  # those columns do not enter the logits
+    case.kv = keys
+    case.q = q
+    _check(case, num_kv_splits=splits)
