@@ -72,7 +72,7 @@ enum : int {
   kMiscTmem = 128,    // u32 tensor memory base
   kMiscAbort = 132,   // int abort flag
   kMiscRowOff = 192,  // int64 row output offsets [NG] (NG <= 48 -> 384 bytes, to 576)
-  kMiscRed = 640,     // float red[4][NG], then float scale[NG]
+  kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG], then int lim[NG]
 };
 
 template <int NG, int STAGES>
@@ -89,7 +89,8 @@ struct DecodeLayout {
   static constexpr int kPBytes = kPInRope ? 0 : 2 * kNPV * 128;
   static constexpr int kMiscOff = kPOff + kPBytes;
   static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 2048;
-  static_assert(kMiscRed + 5 * NG * 4 <= kMiscBytes, "misc region overflow");
+  static constexpr int kMiscLim = kMiscRed + 5 * NG * 4;        // int causal limit [NG]
+  static_assert(kMiscLim + 4 * NG <= kMiscBytes, "misc region overflow");
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
   // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
   static constexpr int kSStride = (NG + 31) / 32 * 32;
@@ -116,6 +117,10 @@ constexpr int kRegsHigh = 224;   // softmax
 static_assert(8 * 32 * kRegsLow + 4 * 32 * kRegsHigh <= kDecodeThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kSoftmaxThread0 = 32 * kSoftmaxWarp0;
+
+// P tile in shared memory: MN-major, no swizzle.  Position j's bytes for columns
+// 16m .. 16m+15 are at m * kPGroup + (j / 8) * 128 + (j % 8) * 16.
+constexpr int kPGroup = kTile * 16;   // 2048
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -204,11 +209,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const float kv_scale = *prm.kv_scale;
     const float scale_log2 = prm.sm_scale * (*prm.q_scale) * kv_scale * kLog2e;
     const int H = prm.sp.H;
-    // byte offsets of this position's column inside the 8 rows of a swizzle atom
-    uint32_t poff[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      poff[r] = r * 128 + ((((prow >> 4) ^ r) & 7) << 4) + (prow & 15);
+    // P is stored MN-major without swizzle (see the PV descriptor): this position's 16
+    // bytes of columns 16m .. 16m+15 sit at pofs + m * kPGroup.
+    const uint32_t pofs = (prow >> 3) * 128 + (prow & 7) * 16;
+    float* s_alpha = red + 4 * NG;
+    int* s_lim = reinterpret_cast<int*>(misc + LY::kMiscLim);
 
     uint32_t it_g = 0;
     Piece pc;
@@ -222,92 +227,137 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         l_acc[n] = 0.f;
       }
       const int causal_from = pc.L - pc.T;   // positions beyond this need the causal test
+      // draft t of this group's row n sees positions <= L - T + t
+      if (prow < NG) s_lim[prow] = causal_from + (pc.g * NG + prow) / H;
+      bar_sync(1, 128);
       for (int t = 0; t < nt; ++t, ++it_g) {
         const int sb = it_g & 1;
         mbar_wait(mbase + kMiscSFull + 8 * sb, (it_g >> 1) & 1, abort_flag, prm.err);
         tc_fence_after();
-        float x[NG];
-#pragma unroll
-        for (int c = 0; c < NG / 16; ++c) tmem_ld16(tl + sb * LY::kSStride + 16 * c, x + 16 * c);
-        tmem_wait_ld();
-
         const int pos = pc.j0 + t * kTile + prow;
         const bool in_piece = pos < pc.j1;
+        const bool causal = in_piece && pos > causal_from;
+        const uint32_t s_tm = tl + sb * LY::kSStride;
+        // scaled logit (log2 units) of column n, with masks: past the piece or beyond the
+        // draft's causal limit -> -inf; padding rows -> 0 (finite, discarded)
+        auto xform = [&](float sraw, int n) -> float {
+          float v = in_piece ? sraw * scale_log2 : -INFINITY;
+          if (causal && pos > s_lim[n]) v = -INFINITY;
+          return (n >= pc.rows) ? 0.f : v;
+        };
+        constexpr int kCh = NG / 16;
+        // One chunk of 16 columns stays in registers when NG == 16; wider groups re-read
+        // S from tensor memory in each pass.
+        float x0[16];
         bool exceed = false;
 #pragma unroll
-        for (int n = 0; n < NG; ++n) {
-          float v = in_piece ? x[n] * scale_log2 : -INFINITY;
-          if (in_piece && pos > causal_from) {
-            const int tq = (pc.g * NG + n) / H;
-            if (pos > causal_from + tq) v = -INFINITY;
+        for (int ch = 0; ch < kCh; ++ch) {
+          float xs[16];
+          tmem_ld16(s_tm + 16 * ch, xs);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int n = 16 * ch + k;
+            xs[k] = xform(xs[k], n);
+            exceed |= (xs[k] - m_ref[n] > kTau);
+            if (ch == 0) x0[k] = xs[k];
           }
-          if (n >= pc.rows) v = 0.f;        // padding rows: any finite value, discarded
-          x[n] = v;
-          exceed |= (v - m_ref[n] > kTau);
         }
         exceed = bar_red_or(1, 128, exceed);
         if (exceed) {
           // rare: move the reference max to this tile's column maxima
+#pragma unroll 1
+          for (int ch = 0; ch < kCh; ++ch) {
+            float xs[16];
+            if (kCh == 1) {
 #pragma unroll
-          for (int n = 0; n < NG; ++n) {
-            float v = x[n];
+              for (int k = 0; k < 16; ++k) xs[k] = x0[k];
+            } else {
+              tmem_ld16(s_tm + 16 * ch, xs);
+              tmem_wait_ld();
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[q4 * NG + n] = v;
+              for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], 16 * ch + k);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float v = xs[k];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) red[q4 * NG + 16 * ch + k] = v;
+            }
           }
           bar_sync(1, 128);
-          float alpha[NG];
 #pragma unroll
           for (int n = 0; n < NG; ++n) {
             const float tmax = fmaxf(fmaxf(red[n], red[NG + n]), fmaxf(red[2 * NG + n], red[3 * NG + n]));
             const float m_new = fmaxf(m_ref[n], tmax);
-            alpha[n] = (m_ref[n] == -INFINITY) ? 0.f : ex2_approx(m_ref[n] - m_new);
-            l_acc[n] *= alpha[n];
+            const float alpha = (m_ref[n] == -INFINITY) ? 0.f : ex2_approx(m_ref[n] - m_new);
+            l_acc[n] *= alpha;
             m_ref[n] = m_new;
+            if (prow == 0) s_alpha[n] = alpha;
           }
           bar_sync(1, 128);
           if (t > 0) {
             // O holds this piece's earlier tiles: wait for the last PV, then rescale
             mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag, prm.err);
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int bk = 0; bk < 4; ++bk) {
-#pragma unroll
+#pragma unroll 1
               for (int c = 0; c < NPV / 16; ++c) {
                 float v[16];
                 const uint32_t a = tl + LY::kOBase + bk * NPV + 16 * c;
                 tmem_ld16(a, v);
                 tmem_wait_ld();
+                const int n0 = (16 * c) % NG;   // hi and lo planes share the row's alpha
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const int col = 16 * c + k;
-                  v[k] *= alpha[col < NG ? col : col - NG];
-                }
+                for (int k = 0; k < 16; ++k) v[k] *= s_alpha[n0 + k];
                 tmem_st16(a, v);
               }
             }
             tmem_wait_st();
           }
         }
-        // probabilities relative to the reference, split into two FP8 planes
+        // probabilities relative to the reference, split into two FP8 planes:
+        // hi = e4m3(p), lo = e4m3(256 (p - hi)); 16-byte stores of 16 columns per plane
         const int stage = static_cast<int>(it_g % STAGES);
-        uint8_t* pb = LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
-                                   : smem + LY::kPOff + sb * NPV * 128;
+        uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
+                                    : smem + LY::kPOff + sb * NPV * 128) + pofs;
 #pragma unroll
-        for (int n = 0; n < NG; n += 2) {
-          const float m0 = (m_ref[n] == -INFINITY) ? 0.f : m_ref[n];
-          const float m1 = (m_ref[n + 1] == -INFINITY) ? 0.f : m_ref[n + 1];
-          const float p0 = ex2_approx(x[n] - m0);
-          const float p1 = ex2_approx(x[n + 1] - m1);
-          l_acc[n] += p0;
-          l_acc[n + 1] += p1;
-          const uint16_t hi = f32x2_to_e4m3x2(p1, p0);
-          const float2 hf = e4m3x2_to_f32x2(hi);
-          const uint16_t lo = f32x2_to_e4m3x2((p1 - hf.y) * kLoScale, (p0 - hf.x) * kLoScale);
-          pb[((n) >> 3) * 1024 + poff[(n) & 7]] = static_cast<uint8_t>(hi & 0xFF);
-          pb[((n + 1) >> 3) * 1024 + poff[(n + 1) & 7]] = static_cast<uint8_t>(hi >> 8);
-          pb[((NG + n) >> 3) * 1024 + poff[(NG + n) & 7]] = static_cast<uint8_t>(lo & 0xFF);
-          pb[((NG + n + 1) >> 3) * 1024 + poff[(NG + n + 1) & 7]] = static_cast<uint8_t>(lo >> 8);
+        for (int ch = 0; ch < kCh; ++ch) {
+          float xs[16];
+          if (kCh == 1) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) xs[k] = x0[k];
+          } else {
+            tmem_ld16(s_tm + 16 * ch, xs);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], 16 * ch + k);
+          }
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 16; k += 2) {
+            const int n = 16 * ch + k;
+            const float m0 = (m_ref[n] == -INFINITY) ? 0.f : m_ref[n];
+            const float m1 = (m_ref[n + 1] == -INFINITY) ? 0.f : m_ref[n + 1];
+            const float p0 = ex2_approx(xs[k] - m0);
+            const float p1 = ex2_approx(xs[k + 1] - m1);
+            l_acc[n] += p0;
+            l_acc[n + 1] += p1;
+            const uint32_t hi = f32x2_to_e4m3x2(p1, p0);      // byte 0: p0, byte 1: p1
+            const float2 hf = e4m3x2_to_f32x2(static_cast<uint16_t>(hi));
+            const uint32_t lo = f32x2_to_e4m3x2((p1 - hf.y) * kLoScale, (p0 - hf.x) * kLoScale);
+            if ((k & 2) == 0) {
+              hw[k >> 2] = hi;
+              lw[k >> 2] = lo;
+            } else {
+              hw[k >> 2] |= hi << 16;
+              lw[k >> 2] |= lo << 16;
+            }
+          }
+          *reinterpret_cast<uint4*>(pb + ch * kPGroup) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(pb + (kCh + ch) * kPGroup) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -493,7 +543,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // ===================================================== MMA issuer (one thread)
       if (lane == 0) {
         constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
-        constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, false);
+        constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, true);
         int n_piece = 0;
         Piece pc;
         auto issue_pv = [&](uint32_t i, bool first_of_piece) {
@@ -509,8 +559,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int kk = 0; kk < 4; ++kk) {
               // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
               const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
-              // B = P: NPV rows x 32 positions (K-major, 128-byte swizzle)
-              const uint64_t b = smem_desc(pbuf + kk * 32, 16, 1024, kSw128);
+              // B = P, MN-major without swizzle: 32 positions (K) in 8-position core
+              // matrices of 128 bytes, 128 bytes apart (leading byte offset); NPV columns
+              // (MN) in groups of 16, kPGroup apart (stride byte offset)
+              const uint64_t b = smem_desc(pbuf + kk * 4 * 128, 128, kPGroup, kSwNone);
               mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
             }
           }
