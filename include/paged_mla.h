@@ -28,8 +28,9 @@
  * Conventions for every entry point
  *  - Ownership: the caller owns every buffer.  All tensor pointers are DEVICE pointers
  *    on the current CUDA device.  The library never allocates device memory; scratch
- *    comes from the caller's workspace.  It keeps only per-device caches of device
- *    attributes and kernel attributes.
+ *    comes from the caller's workspace (mla_decode_noalloc: from a fixed array inside the
+ *    library).  It keeps only per-device caches of device attributes, kernel attributes
+ *    and that array's address.
  *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream) and the
  *    call returns without waiting, except mla_validate and mla_check_error, which
  *    synchronise `stream`.
@@ -169,6 +170,39 @@ int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
  * workspace's error words since the last check (MLA_OK if none) and clears them.
  */
 int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Size of the fixed device scratch array behind mla_decode_noalloc (16 MiB). */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * mla_decode without a workspace, for callers that cannot allocate device memory: code
+ * living inside a framework whose device memory is owned by that framework's own
+ * allocator, or a hook that is handed only its input and output tensors and has no way to
+ * obtain scratch space.  (The pages have no counterpart of this entry point; it is part of
+ * this library's interface only.)
+ *
+ * Arguments are those of mla_decode, minus workspace / workspace_bytes, plus:
+ *   error_out  NULL, or a device int32 that receives this call's raw device error bits
+ *              (0 = none; any other value is an error mla_check_error would report).
+ *
+ * Scratch: the split-KV partials and error words live in one file-scope device array of
+ * MLA_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library until the process
+ * exits.  A call whose mla_get_workspace_size(...) exceeds that returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL without enqueuing anything (on a 152-SM GPU the automatic
+ * split fits up to ~350 requests with 12-16 heads and q_len 1, and ~18 requests with 12
+ * heads and q_len 4; num_kv_splits = 1 fits any batch).  Nothing is allocated: the first call on each device looks up the array's
+ * device address (so make that first call before any stream capture), and every call
+ * clears the error words and then runs the ordinary decode on `stream`.
+ * All calls on a device share the array and it keeps the last call's contents: calls
+ * that may overlap on the GPU (different streams without ordering) race on it.
+ */
+int mla_decode_noalloc(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
+                       const mla_tensor_t* o, const mla_tensor_t* qo_indptr,
+                       const mla_tensor_t* kv_indptr, const mla_tensor_t* kv_indices,
+                       const mla_tensor_t* kv_last_page_lens, int32_t max_seqlen_q,
+                       float sm_scale, const mla_tensor_t* q_scale, const mla_tensor_t* kv_scale,
+                       int32_t num_kv_splits, const mla_tensor_t* lse_out, int32_t* error_out,
+                       mla_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MlaError", "mla_decode", "mla_merge_partials", "mla_validate", "mla_check_error",
+    "MlaError", "mla_decode", "mla_decode_noalloc", "mla_merge_partials", "mla_validate", "mla_check_error",
     "mla_get_workspace_size", "mla_status_string", "make_workspace", "library_path",
 ]
 
@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_get_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     lib.mla_decode.restype = ctypes.c_int
     lib.mla_decode.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, c_sz, vp]
+    lib.mla_decode_noalloc.restype = ctypes.c_int
+    lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, vp]
     lib.mla_merge_partials.restype = ctypes.c_int
     lib.mla_merge_partials.argtypes = [P, P, P, P, P, P, vp, vp]
     lib.mla_validate.restype = ctypes.c_int
@@ -162,6 +164,27 @@ def mla_decode(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_l
                          workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     _check(rc, "mla_decode")
     return workspace
+
+
+def mla_decode_noalloc(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                       max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits=0, lse_out=None,
+                       error_out=None, stream=None):
+    """Decode without a workspace: scratch lives in the library's fixed device array.
+
+    For callers that cannot allocate device memory.  error_out: optional int32 device
+    tensor receiving the call's raw device error bits.  Raises MlaError on a host-side
+    error, including MLA_ERR_WORKSPACE_TOO_SMALL when the call needs more scratch than
+    the fixed array holds.
+    """
+    descs = [_desc(t) for t in (q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
+                                kv_last_page_lens, q_scale, kv_scale, lse_out)]
+    dq, dkv, do, dqo, dkvp, didx, dlast, dqs, dks, dlse = descs
+    ew = ctypes.c_void_p(error_out.data_ptr()) if error_out is not None else None
+    rc = _lib.mla_decode_noalloc(_ref(dq), _ref(dkv), _ref(do), _ref(dqo), _ref(dkvp), _ref(didx),
+                                 _ref(dlast), int(max_seqlen_q), float(sm_scale), _ref(dqs),
+                                 _ref(dks), int(num_kv_splits), _ref(dlse), ew,
+                                 _stream(stream, q.device))
+    _check(rc, "mla_decode_noalloc")
 
 
 def mla_merge_partials(o_parts, lse_parts, reduce_indptr, reduce_idx, o, lse_out=None,
