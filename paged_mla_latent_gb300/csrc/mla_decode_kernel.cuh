@@ -128,6 +128,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // so P stays <= 2^kTau = 256 < 448 (e4m3 max) and O is rescaled rarely.
 constexpr float kTau = 8.0f;
 constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
+// Initial reference max: finite, so that p = 2^(x - ref) needs no special case (masked
+// logits are -inf and give 0) and the first tile always moves it (x - ref > kTau).
+constexpr float kRefInit = -1.0e30f;
 
 template <int NG, int STAGES>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
 #pragma unroll
       for (int n = 0; n < NG; ++n) {
-        m_ref[n] = -INFINITY;
+        m_ref[n] = kRefInit;
         l_acc[n] = 0.f;
       }
       const int causal_from = pc.L - pc.T;   // positions beyond this need the causal test
@@ -246,108 +249,80 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           return (n >= pc.rows) ? 0.f : v;
         };
         constexpr int kCh = NG / 16;
-        // One chunk of 16 columns stays in registers when NG == 16; wider groups re-read
-        // S from tensor memory in each pass.
-        float x0[16];
-        bool exceed = false;
+        const int stage = static_cast<int>(it_g % STAGES);
+        // P tile: this position's 16-byte vectors (see kPGroup)
+        uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
+                                    : smem + LY::kPOff + sb * NPV * 128) + pofs;
+        bool pv_prev_done = (t == 0);   // O holds nothing yet on a piece's first tile
+        // Columns are independent heads: each 16-column chunk is finished in one pass.
 #pragma unroll
         for (int ch = 0; ch < kCh; ++ch) {
           float xs[16];
           tmem_ld16(s_tm + 16 * ch, xs);
           tmem_wait_ld();
+          float dmax = -INFINITY;
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int n = 16 * ch + k;
-            xs[k] = xform(xs[k], n);
-            exceed |= (xs[k] - m_ref[n] > kTau);
-            if (ch == 0) x0[k] = xs[k];
+            xs[k] = xform(xs[k], 16 * ch + k);
+            dmax = fmaxf(dmax, xs[k] - m_ref[16 * ch + k]);
           }
-        }
-        exceed = bar_red_or(1, 128, exceed);
-        if (exceed) {
-          // rare: move the reference max to this tile's column maxima
-#pragma unroll 1
-          for (int ch = 0; ch < kCh; ++ch) {
-            float xs[16];
-            if (kCh == 1) {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) xs[k] = x0[k];
-            } else {
-              tmem_ld16(s_tm + 16 * ch, xs);
-              tmem_wait_ld();
-#pragma unroll
-              for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], 16 * ch + k);
-            }
+          if (bar_red_or(1, 128, dmax > kTau)) {
+            // rare: move these columns' reference to their tile maxima
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               float v = xs[k];
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) red[q4 * NG + 16 * ch + k] = v;
+              if (lane == 0) red[q4 * 16 + k] = v;
             }
-          }
-          bar_sync(1, 128);
+            bar_sync(1, 128);
 #pragma unroll
-          for (int n = 0; n < NG; ++n) {
-            const float tmax = fmaxf(fmaxf(red[n], red[NG + n]), fmaxf(red[2 * NG + n], red[3 * NG + n]));
-            const float m_new = fmaxf(m_ref[n], tmax);
-            const float alpha = (m_ref[n] == -INFINITY) ? 0.f : ex2_approx(m_ref[n] - m_new);
-            l_acc[n] *= alpha;
-            m_ref[n] = m_new;
-            if (prow == 0) s_alpha[n] = alpha;
-          }
-          bar_sync(1, 128);
-          if (t > 0) {
-            // O holds this piece's earlier tiles: wait for the last PV, then rescale
-            mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag, prm.err);
-            tc_fence_after();
+            for (int k = 0; k < 16; ++k) {
+              const int n = 16 * ch + k;
+              const float tmax = fmaxf(fmaxf(red[k], red[16 + k]), fmaxf(red[32 + k], red[48 + k]));
+              const float m_new = fmaxf(m_ref[n], tmax);
+              const float alpha = ex2_approx(m_ref[n] - m_new);   // 0 from the initial reference
+              l_acc[n] *= alpha;
+              m_ref[n] = m_new;
+              if (prow == 0) s_alpha[k] = alpha;
+            }
+            bar_sync(1, 128);
+            if (t > 0) {
+              // O holds this piece's earlier tiles: wait for the last PV, then rescale the
+              // chunk's hi and lo columns in the four value blocks
+              if (!pv_prev_done) {
+                mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag,
+                          prm.err);
+                tc_fence_after();
+                pv_prev_done = true;
+              }
 #pragma unroll 1
-            for (int bk = 0; bk < 4; ++bk) {
-#pragma unroll 1
-              for (int c = 0; c < NPV / 16; ++c) {
+              for (int bp = 0; bp < 8; ++bp) {
                 float v[16];
-                const uint32_t a = tl + LY::kOBase + bk * NPV + 16 * c;
+                const uint32_t a = tl + LY::kOBase + (bp >> 1) * NPV + (bp & 1) * NG + 16 * ch;
                 tmem_ld16(a, v);
                 tmem_wait_ld();
-                const int n0 = (16 * c) % NG;   // hi and lo planes share the row's alpha
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] *= s_alpha[n0 + k];
+                for (int k = 0; k < 16; ++k) v[k] *= s_alpha[k];
                 tmem_st16(a, v);
               }
+              tmem_wait_st();
             }
-            tmem_wait_st();
           }
-        }
-        // probabilities relative to the reference, split into two FP8 planes:
-        // hi = e4m3(p), lo = e4m3(256 (p - hi)); 16-byte stores of 16 columns per plane
-        const int stage = static_cast<int>(it_g % STAGES);
-        uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
-                                    : smem + LY::kPOff + sb * NPV * 128) + pofs;
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) {
-          float xs[16];
-          if (kCh == 1) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) xs[k] = x0[k];
-          } else {
-            tmem_ld16(s_tm + 16 * ch, xs);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], 16 * ch + k);
-          }
+          // probabilities relative to the reference (<= 2^kTau), split into two FP8 planes:
+          // hi = e4m3(p), lo = e4m3(256 (p - hi)), the residual taken in f16x2
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
             const int n = 16 * ch + k;
-            const float m0 = (m_ref[n] == -INFINITY) ? 0.f : m_ref[n];
-            const float m1 = (m_ref[n + 1] == -INFINITY) ? 0.f : m_ref[n + 1];
-            const float p0 = ex2_approx(xs[k] - m0);
-            const float p1 = ex2_approx(xs[k + 1] - m1);
+            const float p0 = ex2_approx(xs[k] - m_ref[n]);
+            const float p1 = ex2_approx(xs[k + 1] - m_ref[n + 1]);
             l_acc[n] += p0;
             l_acc[n + 1] += p1;
-            const uint32_t hi = f32x2_to_e4m3x2(p1, p0);      // byte 0: p0, byte 1: p1
-            const float2 hf = e4m3x2_to_f32x2(static_cast<uint16_t>(hi));
-            const uint32_t lo = f32x2_to_e4m3x2((p1 - hf.y) * kLoScale, (p0 - hf.x) * kLoScale);
+            const uint32_t p16 = f32x2_to_f16x2(p1, p0);          // low half: p0
+            const uint32_t hi = f16x2_to_e4m3x2(p16);             // byte 0: p0, byte 1: p1
+            const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), 0x5C005C00u);
+            const uint32_t lo = f16x2_to_e4m3x2(r16);              // 256 (p - hi)
             if ((k & 2) == 0) {
               hw[k >> 2] = hi;
               lw[k >> 2] = lo;
@@ -391,9 +366,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             int64_t off = -1;
             if (n < pc.rows) {
               if (direct) {
-                const int64_t r = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) * H + pc.g * NG + n;
+                const int rr = pc.g * NG + n;              // row within the request
+                const int64_t tok = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) + rr / H;
+                const int64_t r = tok * H + rr % H;
                 if (r < prm.n_q_rows) {
-                  off = (r / H) * prm.o_stride_tok + (r % H) * prm.o_stride_head;
+                  off = tok * prm.o_stride_tok + (rr % H) * prm.o_stride_head;
                   if (prm.lse_out) prm.lse_out[r] = lse;
                 } else {
                   atomicOr(prm.err, kErrBadOutput);

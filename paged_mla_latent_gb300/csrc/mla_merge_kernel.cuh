@@ -18,10 +18,10 @@
 
 namespace pmla {
 
-constexpr int kMergeThreads = 512;
+constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeCols = 32;           // value columns per block (one per lane)
-constexpr int kMergeMaxParts = 1024;     // partials held in shared memory per pass
+constexpr int kMergeCols = 128;          // value columns per block (32 lanes x float4)
+constexpr int kMergeUnroll = 4;          // partials in flight per warp
 
 struct MergeOut {
   void* o;
@@ -30,87 +30,73 @@ struct MergeOut {
   float* lse;         // element for this (row, head), or null
 };
 
-// Merge `count` partials of one (row, head) for columns col0 .. col0+31.  lse_of(k) and
+// Merge `count` partials of one (row, head) for columns col0 .. col0+127.  lse_of(k) and
 // o_of(k) give partial k's log-sum-exp and the start of its 512 normalised values.
-// The block first turns the lse values into weights w_k = exp(lse_k - M) (shared by
-// all its threads), then warp w accumulates partials w, w+8, ... with one column per lane,
-// every load of a warp independent of the others.
+// Warp w takes partials w, w+8, ..., kMergeUnroll at a time with every load (its lse and a
+// float4 of values per lane) independent of the others, and keeps a running max, weight
+// sum and weighted sum; the eight warps are then combined through shared memory.
 template <class OOf, class LseOf>
 __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const MergeOut& out,
                                      int col0) {
-  __shared__ float s_w[kMergeMaxParts];
-  __shared__ float s_red[kMergeWarps];
-  __shared__ float s_acc[kMergeWarps][kMergeCols];
+  __shared__ float s_m[kMergeWarps];
+  __shared__ float s_w[kMergeWarps];
+  __shared__ float4 s_acc[kMergeWarps][32];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  float acc = 0.f, M = -INFINITY, wsum = 0.f;
-  for (int base = 0; base < count || base == 0; base += kMergeMaxParts) {
-    const int n = min(count - base, kMergeMaxParts);
-    // 1. max of this pass's lse values
-    float m = -INFINITY;
-    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
-      const float l = lse_of(base + k);
-      s_w[k] = l;
-      m = fmaxf(m, l);
+  float m = -INFINITY, wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = warp; k0 < count; k0 += kMergeUnroll * kMergeWarps) {
+    float l[kMergeUnroll];
+    float4 v[kMergeUnroll];
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int k = k0 + u * kMergeWarps;
+      l[u] = (k < count) ? lse_of(k) : -INFINITY;
+      v[u] = (k < count) ? *reinterpret_cast<const float4*>(o_of(k) + col0 + 4 * lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    float pm = s_red[0];
-#pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) pm = fmaxf(pm, s_red[w]);
-    __syncthreads();
-    if (pm == -INFINITY) continue;            // nothing attended in this pass
-    // rescale what earlier passes accumulated to the new running max
-    const float M_new = fmaxf(M, pm);
-    const float f = (M == -INFINITY) ? 0.f : __expf(M - M_new);
-    acc *= f;
-    wsum *= f;
-    M = M_new;
-    // 2. weights
-    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
-      const float l = s_w[k];
-      s_w[k] = (l == -INFINITY) ? 0.f : __expf(l - M);
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      if (l[u] == -INFINITY) continue;    // nothing attended in that partial: weight 0
+      const float m_new = fmaxf(m, l[u]);
+      const float f = (m == -INFINITY) ? 0.f : __expf(m - m_new);
+      const float w = __expf(l[u] - m_new);
+      wsum = wsum * f + w;
+      acc.x = acc.x * f + w * v[u].x;
+      acc.y = acc.y * f + w * v[u].y;
+      acc.z = acc.z * f + w * v[u].z;
+      acc.w = acc.w * f + w * v[u].w;
+      m = m_new;
     }
-    __syncthreads();
-    float ws = 0.f;
-    for (int k = lane; k < n; k += 32) ws += s_w[k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-    wsum += ws;   // every warp computes the same total
-    // 3. weighted sum of the value rows: up to 8 independent loads in flight per warp
-    float a = 0.f;
-    for (int k0 = warp; k0 < n; k0 += 8 * kMergeWarps) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * kMergeWarps;
-        v[u] = (k < n) ? o_of(base + k)[col0 + lane] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * kMergeWarps;
-        if (k < n) a += s_w[k] * v[u];
-      }
-    }
-    acc += a;
-    __syncthreads();   // s_w is rewritten by the next pass
   }
   s_acc[warp][lane] = acc;
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_w[warp] = wsum;
+  }
   __syncthreads();
   if (threadIdx.x < kMergeCols) {
-    float val = 0.f;
+    float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) val += s_acc[w][threadIdx.x];
-    val = (wsum > 0.f) ? val / wsum : 0.f;
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
+    float tot = 0.f, val = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kMergeWarps; ++w) {
+        if (s_m[w] == -INFINITY) continue;
+        const float f = __expf(s_m[w] - M);
+        tot += s_w[w] * f;
+        val += reinterpret_cast<const float*>(&s_acc[w][0])[threadIdx.x] * f;
+      }
+      val /= tot;
+    }
     const int64_t off = out.o_off + col0 + threadIdx.x;
     if (out.o_fp32)
       reinterpret_cast<float*>(out.o)[off] = val;
     else
       reinterpret_cast<__nv_bfloat16*>(out.o)[off] = __float2bfloat16_rn(val);
     if (threadIdx.x == 0 && out.lse != nullptr && col0 == 0)
-      *out.lse = (wsum > 0.f) ? M + __logf(wsum) : -INFINITY;
+      *out.lse = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
   }
 }
 
@@ -133,7 +119,7 @@ struct SplitMergeParams {
   int* err;
 };
 
-// grid = (units * NG, 512 / 32), block = 256.  Merges the units the scheduler split and writes
+// grid = (units * NG, 512 / 128), block = 256.  Merges the units the scheduler split and writes
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
 __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const SplitMergeParams prm) {
@@ -199,7 +185,7 @@ struct CsrMergeParams {
   int* err;
 };
 
-// grid = (n_out * H, 512 / 32), block = 256.  Public merge with an explicit reduce map.
+// grid = (n_out * H, 512 / 128), block = 256.  Public merge with an explicit reduce map.
 __global__ void __launch_bounds__(kMergeThreads) mla_csr_merge_kernel(const CsrMergeParams prm) {
   const int64_t rr = blockIdx.x / prm.H;
   const int h = static_cast<int>(blockIdx.x - rr * prm.H);

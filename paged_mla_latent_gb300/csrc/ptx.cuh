@@ -302,6 +302,35 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(a), "f"(b));
   return r;
 }
+// Two floats to f16x2 (round to nearest): `a` in the high half, `b` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
+// f16x2 to two e4m3fn codes (round to nearest even, saturating): high half -> high byte.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
+}
+// Two e4m3fn codes (low 16 bits) to f16x2 (exact): low byte -> low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(v)));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Two e4m3fn codes back to floats (exact): .x from the low byte, .y from the high byte.
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
   uint32_t h2;
