@@ -306,10 +306,11 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
   const int64_t units = static_cast<int64_t>(cs.B) * plan.groups;
+  const int lanes = merge_lanes_for(units > 0 ? plan.slots / units : 1);
   // Programmatic dependent launch: the merge grid is scheduled while the decode grid
   // runs and waits on the device (griddepcontrol.wait) for the partials.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), kDV / kMergeCols);
+  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), lanes / 2);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -318,7 +319,14 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_split_merge_kernel, mp) != cudaSuccess) return MLA_ERR_CUDA;
+  cudaError_t e;
+  switch (lanes) {
+    case 64: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<64>, mp); break;
+    case 32: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<32>, mp); break;
+    case 16: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<16>, mp); break;
+    default: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<8>, mp); break;
+  }
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -363,8 +371,14 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
   prm.o_stride_h = o->stride[1];
   prm.lse_out = lse_out ? static_cast<float*>(lse_out->ptr) : nullptr;
   prm.err = error_word;
-  dim3 grid(static_cast<unsigned>(n_out * H), kDV / kMergeCols);
-  mla_csr_merge_kernel<<<grid, kMergeThreads, 0, stream>>>(prm);
+  const int lanes = merge_lanes_for(m / n_out);
+  dim3 grid(static_cast<unsigned>(n_out * H), lanes / 2);
+  switch (lanes) {
+    case 64: mla_csr_merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    case 32: mla_csr_merge_kernel<32><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    case 16: mla_csr_merge_kernel<16><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    default: mla_csr_merge_kernel<8><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+  }
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

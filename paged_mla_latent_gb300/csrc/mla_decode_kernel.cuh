@@ -7,20 +7,23 @@
 //
 // One persistent CTA per SM walks the pieces the scheduler (mla_sched.cuh) gives it.
 // Per tile of 128 cache positions:
-//   producer warps  : four warps, 32 rows each: load the row ids, then copy every row
-//     (0-3)           with 16-byte cp.async (one instruction per row of latent columns,
-//                     lanes along the row; one per 8 rows of rope columns) straight into
-//                     a 3- (or 2-) stage ring in the 128-byte (latent) / 64-byte (rope)
-//                     swizzled layouts the tensor core reads.  Positions past the piece
-//                     and invalid row ids are zero-filled.  (A TMA tile::gather4 of 128-
-//                     byte boxes issues 5 requests per 4 rows and measured 2-4 TB/s on
-//                     this access pattern; per-thread copies from four warps reach the
-//                     random-row gather limit of ~5.3 TB/s.)
+//   producer warps  : seven warps (0-3, 5-7), rows r = w + 7 j: load the row ids, then
+//                     copy every row with 16-byte cp.async (one instruction per row of
+//                     latent columns, lanes along the row; one per 8 rows of rope columns)
+//                     straight into a 3- (or 2-) stage ring in the 128-byte (latent) /
+//                     64-byte (rope) swizzled layouts the tensor core reads.  Positions
+//                     past the piece and invalid row ids are zero-filled.  (Prefetching
+//                     later tiles' rows into L2 measured slower: the extra requests cost
+//                     more than the latency they hide.)  (A TMA tile::gather4 of
+//                     128-byte boxes issues 5 requests per 4 rows and measured 2-4 TB/s on
+//                     this access pattern; per-thread copies reach the random-row gather
+//                     limit of ~5.3 TB/s.)
 //   MMA thread      : (warp 4) S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
 //                     M = 128 positions, N = NG query rows, K = 576; FP32 in TMEM),
 //                     then O^T[c, n] += V^T[c, pos] . P^T[pos, n] for the four 128-wide
-//                     value blocks (A = the same cache rows read MN-major).
-//   softmax warps   : (warps 5-8) read S^T from TMEM (one position per thread), scale, mask,
+//                     value blocks (A = the same cache rows read MN-major; N = 2 NG: the
+//                     two P planes side by side).
+//   softmax warps   : (warps 8-11) read S^T from TMEM (one position per thread), scale, mask,
 //                     online softmax in the exp2 domain with a lazily moved reference
 //                     max, and write P as two FP8 planes: hi = e4m3(p) and
 //                     lo = e4m3(256 * (p - hi)), so P reaches the tensor core with

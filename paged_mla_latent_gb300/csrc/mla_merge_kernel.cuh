@@ -4,11 +4,14 @@
 // "Scaling Kimi K3 on AMD Instinct MI355X" §1 "Cache": each partial answer carries the
 // normalisation information that lets shards (or split-KV pieces) merge exactly.
 //
-// One block handles one (output row, head) and a 128-column quarter of the 512 value
-// columns.  Its 8 warps take the partials round-robin (lane = 4 columns, float4), each
-// keeping a running max and weight sum; the warps are then combined through shared
-// memory.  Used twice: after the decode kernel, for the units the scheduler split, and
-// by the public merge of context-parallel shards with an explicit reduce map.
+// One block handles one (output row, head) and a slice of the 512 value columns.  Its 256
+// threads are P partial lanes x 256/P column quads (4 columns, one float4, per thread); a
+// thread takes partials p, p+P, ... with several loads in flight, keeping a running max,
+// weight sum and weighted sum.  P is picked per launch from the partials per row: many
+// partials (batch 1, long history) want many lanes and few columns per block, so that the
+// partials are read in one round; few partials want wide column slices.  Used twice:
+// after the decode kernel, for the units the scheduler split, and by the public merge of
+// context-parallel shards with an explicit reduce map.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -20,8 +23,12 @@ namespace pmla {
 
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeCols = 128;          // value columns per block (32 lanes x float4)
-constexpr int kMergeUnroll = 4;          // partials in flight per warp
+constexpr int kMergeUnroll = 4;          // partials in flight per thread
+
+// Partial lanes for an average of `per_row` partials per merged row: 8, 16, 32 or 64.
+inline int merge_lanes_for(int64_t per_row) {
+  return per_row >= 96 ? 64 : per_row >= 40 ? 32 : per_row >= 16 ? 16 : 8;
+}
 
 struct MergeOut {
   void* o;
@@ -30,63 +37,87 @@ struct MergeOut {
   float* lse;         // element for this (row, head), or null
 };
 
-// Merge `count` partials of one (row, head) for columns col0 .. col0+127.  lse_of(k) and
-// o_of(k) give partial k's log-sum-exp and the start of its 512 normalised values.
-// Warp w takes partials w, w+8, ..., kMergeUnroll at a time with every load (its lse and a
-// float4 of values per lane) independent of the others, and keeps a running max, weight
-// sum and weighted sum; the eight warps are then combined through shared memory.
-template <class OOf, class LseOf>
+// Running softmax-weighted state: max m, weight sum w, weighted sum a (4 columns).
+struct MergeState {
+  float m, w;
+  float4 a;
+};
+
+__device__ __forceinline__ void merge_combine(MergeState& x, float m2, float w2, float4 a2) {
+  if (m2 == -INFINITY) return;            // nothing in the other state
+  const float M = fmaxf(x.m, m2);
+  const float f1 = (x.m == -INFINITY) ? 0.f : __expf(x.m - M);
+  const float f2 = __expf(m2 - M);
+  x.w = x.w * f1 + w2 * f2;
+  x.a.x = x.a.x * f1 + a2.x * f2;
+  x.a.y = x.a.y * f1 + a2.y * f2;
+  x.a.z = x.a.z * f1 + a2.z * f2;
+  x.a.w = x.a.w * f1 + a2.w * f2;
+  x.m = M;
+}
+
+// Merge `count` partials of one (row, head) for columns col0 .. col0 + 1024/P - 1.
+// lse_of(k) and o_of(k) give partial k's log-sum-exp and the start of its 512 normalised
+// values.  Lanes of one warp that share a column quad combine by shuffles, the eight warps
+// through shared memory.
+template <int P, class OOf, class LseOf>
 __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const MergeOut& out,
                                      int col0) {
-  __shared__ float s_m[kMergeWarps];
-  __shared__ float s_w[kMergeWarps];
-  __shared__ float4 s_acc[kMergeWarps][32];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  float m = -INFINITY, wsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = warp; k0 < count; k0 += kMergeUnroll * kMergeWarps) {
+  constexpr int Q = kMergeThreads / P;    // column quads per block
+  constexpr int kCols = 4 * Q;
+  static_assert(Q <= 32 && Q * P == kMergeThreads, "bad merge shape");
+  __shared__ float s_m[kMergeWarps][Q];
+  __shared__ float s_w[kMergeWarps][Q];
+  __shared__ float4 s_acc[kMergeWarps][Q];
+  const int c = threadIdx.x % Q;
+  const int p = threadIdx.x / Q;
+  MergeState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int k0 = p; k0 < count; k0 += kMergeUnroll * P) {
     float l[kMergeUnroll];
     float4 v[kMergeUnroll];
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
-      const int k = k0 + u * kMergeWarps;
+      const int k = k0 + u * P;
       l[u] = (k < count) ? lse_of(k) : -INFINITY;
-      v[u] = (k < count) ? *reinterpret_cast<const float4*>(o_of(k) + col0 + 4 * lane)
+      v[u] = (k < count) ? *reinterpret_cast<const float4*>(o_of(k) + col0 + 4 * c)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
-      if (l[u] == -INFINITY) continue;    // nothing attended in that partial: weight 0
-      const float m_new = fmaxf(m, l[u]);
-      const float f = (m == -INFINITY) ? 0.f : __expf(m - m_new);
-      const float w = __expf(l[u] - m_new);
-      wsum = wsum * f + w;
-      acc.x = acc.x * f + w * v[u].x;
-      acc.y = acc.y * f + w * v[u].y;
-      acc.z = acc.z * f + w * v[u].z;
-      acc.w = acc.w * f + w * v[u].w;
-      m = m_new;
-    }
+    for (int u = 0; u < kMergeUnroll; ++u) merge_combine(st, l[u], 1.f, v[u]);
   }
-  s_acc[warp][lane] = acc;
-  if (lane == 0) {
-    s_m[warp] = m;
-    s_w[warp] = wsum;
+  // lanes q, q + Q, q + 2Q, ... of a warp hold the same columns
+#pragma unroll
+  for (int off = Q; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, st.m, off);
+    const float w2 = __shfl_xor_sync(0xffffffffu, st.w, off);
+    float4 a2;
+    a2.x = __shfl_xor_sync(0xffffffffu, st.a.x, off);
+    a2.y = __shfl_xor_sync(0xffffffffu, st.a.y, off);
+    a2.z = __shfl_xor_sync(0xffffffffu, st.a.z, off);
+    a2.w = __shfl_xor_sync(0xffffffffu, st.a.w, off);
+    merge_combine(st, m2, w2, a2);
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (lane < Q) {
+    s_m[warp][lane] = st.m;
+    s_w[warp][lane] = st.w;
+    s_acc[warp][lane] = st.a;
   }
   __syncthreads();
-  if (threadIdx.x < kMergeCols) {
+  if (threadIdx.x < kCols) {
+    const int cq = threadIdx.x >> 2;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w][cq]);
     float tot = 0.f, val = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kMergeWarps; ++w) {
-        if (s_m[w] == -INFINITY) continue;
-        const float f = __expf(s_m[w] - M);
-        tot += s_w[w] * f;
-        val += reinterpret_cast<const float*>(&s_acc[w][0])[threadIdx.x] * f;
+        if (s_m[w][cq] == -INFINITY) continue;
+        const float f = __expf(s_m[w][cq] - M);
+        tot += s_w[w][cq] * f;
+        val += reinterpret_cast<const float*>(&s_acc[w][cq])[threadIdx.x & 3] * f;
       }
       val /= tot;
     }
@@ -119,9 +150,10 @@ struct SplitMergeParams {
   int* err;
 };
 
-// grid = (units * NG, 512 / 128), block = 256.  Merges the units the scheduler split and writes
+// grid = (units * NG, P / 2), block = 256.  Merges the units the scheduler split and writes
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
+template <int P>
 __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const SplitMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
@@ -129,7 +161,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const Sp
   const int n = static_cast<int>(blockIdx.x - u * NG);
   const int b = static_cast<int>(u / sp.groups);
   const int g = static_cast<int>(u - static_cast<int64_t>(b) * sp.groups);
-  const int col0 = blockIdx.y * kMergeCols;
+  const int col0 = blockIdx.y * (4 * kMergeThreads / P);
   const int T = sp.qo_indptr[b + 1] - sp.qo_indptr[b];
   const int rows = T * sp.H - g * NG;
   if (n >= rows || n >= NG) return;
@@ -166,7 +198,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const Sp
     }
     return prm.part_lse[(first + k) * NG + n];
   };
-  merge_partials_block(count, o_of, lse_of, out, col0);
+  merge_partials_block<P>(count, o_of, lse_of, out, col0);
 }
 
 struct CsrMergeParams {
@@ -185,11 +217,12 @@ struct CsrMergeParams {
   int* err;
 };
 
-// grid = (n_out * H, 512 / 128), block = 256.  Public merge with an explicit reduce map.
+// grid = (n_out * H, P / 2), block = 256.  Public merge with an explicit reduce map.
+template <int P>
 __global__ void __launch_bounds__(kMergeThreads) mla_csr_merge_kernel(const CsrMergeParams prm) {
   const int64_t rr = blockIdx.x / prm.H;
   const int h = static_cast<int>(blockIdx.x - rr * prm.H);
-  const int col0 = blockIdx.y * kMergeCols;
+  const int col0 = blockIdx.y * (4 * kMergeThreads / P);
   const int beg = prm.reduce_indptr[rr];
   const int end = prm.reduce_indptr[rr + 1];
   const int count = end > beg ? end - beg : 0;
@@ -215,7 +248,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_csr_merge_kernel(const CsrM
     }
     return prm.lse_parts[s * prm.lp_stride_p + h * prm.lp_stride_h];
   };
-  merge_partials_block(count, o_of, lse_of, out, col0);
+  merge_partials_block<P>(count, o_of, lse_of, out, col0);
 }
 
 struct ValidateParams {
