@@ -279,6 +279,11 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.o = o->ptr;
   prm.o_fp32 = o->dtype == MLA_DTYPE_FP32;
   prm.o_stride_tok = o->stride[0];
+  {
+    // 16-byte stores cover 8 bf16 / 4 fp32 columns starting at a multiple of that count
+    const int64_t run = o->dtype == MLA_DTYPE_FP32 ? 4 : 8;
+    prm.o_vec16 = is_aligned(o->ptr, 16) && o->stride[0] % run == 0 && o->stride[1] % run == 0;
+  }
   prm.o_stride_head = o->stride[1];
   prm.lse_out = lse_out ? static_cast<float*>(lse_out->ptr) : nullptr;
   prm.part_lse = reinterpret_cast<float*>(ws + plan.lse_off);

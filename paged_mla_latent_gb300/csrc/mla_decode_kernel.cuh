@@ -54,6 +54,7 @@ struct DecodeParams {
   int o_fp32;
   int64_t o_stride_tok;    // elements
   int64_t o_stride_head;   // elements
+  int o_vec16;             // o's base and strides allow 16-byte stores of 16-byte runs
   float* lse_out;          // (sum_T, H) or null
   float* part_o;           // (slots, NG, 512) normalised partial o (kv_scale applied)
   float* part_lse;         // (slots, NG) natural-log lse of each partial
@@ -135,6 +136,55 @@ constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
 // logits are -inf and give 0) and the first tile always moves it (x - ref > kTau).
 constexpr float kRefInit = -1.0e30f;
 
+// Warp-wide reduction of 16 per-lane column values v[0..15] (sum or max): four halving
+// exchanges leave lane l with column col16(l) reduced over the lanes sharing bits 1..4
+// of l, a fifth exchange completes it.  16 shuffles instead of 16 x 5.
+__device__ __forceinline__ int col16(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int half = 8, m = 16; half >= 1; half >>= 1, m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = up ? v[j] : v[j + half];
+      const float keep = up ? v[j + half] : v[j];
+      const float got = __shfl_xor_sync(0xffffffffu, send, m);
+      v[j] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return kMax ? fmaxf(v[0], got) : v[0] + got;
+}
+
+// In-register transpose of W x W blocks among groups of W lanes (W = 4 or 8): lane i of a
+// group holds a[j] = element (i, j); afterwards it holds a[j] = element (j, i).
+template <int W>
+__device__ __forceinline__ void lane_transpose(float* a, int lane) {
+#pragma unroll
+  for (int m = W / 2; m >= 1; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      if ((j & m) == 0) {
+        const float send = up ? a[j] : a[j | m];
+        const float got = __shfl_xor_sync(0xffffffffu, send, m);
+        if (up)
+          a[j] = got;
+        else
+          a[j | m] = got;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <int NG, int STAGES>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
@@ -157,6 +207,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     return;
   }
 
+  // The schedule reads kv_indptr and then qo_indptr; fetch both arrays' first lines at
+  // once so that the second read does not wait for a second trip to memory.
+  if (threadIdx.x < 64) {
+    const int i = 32 * (threadIdx.x >> 1);
+    if (i <= prm.sp.B) prefetch_l1((threadIdx.x & 1) ? prm.sp.qo_indptr + i : prm.sp.kv_indptr + i);
+  }
   PieceIter iter;
   iter.init(prm.sp, blockIdx.x);
   {
@@ -271,18 +327,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           if (bar_red_or(1, 128, dmax > kTau)) {
             // rare: move these columns' reference to their tile maxima
+            {
+              float v[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              float v = xs[k];
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) red[q4 * 16 + k] = v;
+              for (int k = 0; k < 16; ++k) v[k] = xs[k];
+              const float wmax = reduce_scatter16<true>(v, lane);
+              if ((lane & 1) == 0) red[col16(lane) * 4 + q4] = wmax;
             }
             bar_sync(1, 128);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int n = 16 * ch + k;
-              const float tmax = fmaxf(fmaxf(red[k], red[16 + k]), fmaxf(red[32 + k], red[48 + k]));
+              const float4 r4 = *reinterpret_cast<const float4*>(red + 4 * k);
+              const float tmax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
               const float m_new = fmaxf(m_ref[n], tmax);
               const float alpha = ex2_approx(m_ref[n] - m_new);   // 0 from the initial reference
               l_acc[n] *= alpha;
@@ -347,11 +404,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           mbar_wait(mbase + kMiscPv + 8 * (it_g & 1), (it_g >> 1) & 1, abort_flag, prm.err);
           tc_fence_after();
 #pragma unroll
-          for (int n = 0; n < NG; ++n) {
-            float v = l_acc[n];
+          for (int ch = 0; ch < NG / 16; ++ch) {
+            float v[16];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) red[q4 * NG + n] = v;
+            for (int k = 0; k < 16; ++k) v[k] = l_acc[16 * ch + k];
+            const float wsum = reduce_scatter16<false>(v, lane);
+            if ((lane & 1) == 0) red[q4 * NG + 16 * ch + col16(lane)] = wsum;
           }
           bar_sync(1, 128);
           // one thread per row: normaliser, lse and output offset of that row
@@ -389,29 +447,60 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             s_off[n] = off;
           }
           bar_sync(1, 128);
-          // normalised output: thread = value column c within each 128-wide block
+          // normalised output.  TMEM lane = value column: a warp holds 32 adjacent columns
+          // of every row.  Lanes exchange values (in-register transposes) so that each
+          // writes 16 contiguous bytes of one row: 8 bf16 columns (rows i, i + 8 of the
+          // chunk for lane i of 8) or 4 fp32 columns (rows i, i + 4, i + 8, i + 12 for lane
+          // i of 4).  Scalar stores when o's layout does not allow 16-byte stores.
           const bool to_bf16 = direct && !prm.o_fp32;
+          const bool vec = !direct || prm.o_vec16;
           float* fdst = direct ? reinterpret_cast<float*>(prm.o) : prm.part_o;
           __nv_bfloat16* hdst = reinterpret_cast<__nv_bfloat16*>(prm.o);
 #pragma unroll 1
-          for (int bk = 0; bk < 4; ++bk) {
-            const int c = bk * 128 + prow;
+          for (int ch = 0; ch < NG / 16; ++ch) {
 #pragma unroll 1
-            for (int ch = 0; ch < NG / 16; ++ch) {
+            for (int bk = 0; bk < 4; ++bk) {
               float hi[16], lo[16];
               tmem_ld16(tl + LY::kOBase + bk * NPV + 16 * ch, hi);
               tmem_ld16(tl + LY::kOBase + bk * NPV + NG + 16 * ch, lo);
               tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int n = 16 * ch + k;
-                const int64_t off = s_off[n];
-                if (off >= 0) {
-                  const float val = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[n];
+              for (int k = 0; k < 16; ++k) hi[k] = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[16 * ch + k];
+              const int cw = bk * 128 + 32 * q4;   // first column of this warp
+              if (!vec) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const int64_t off = s_off[16 * ch + k];
+                  if (off < 0) continue;
                   if (to_bf16)
-                    hdst[off + c] = __float2bfloat16_rn(val);
+                    hdst[off + cw + lane] = __float2bfloat16_rn(hi[k]);
                   else
-                    fdst[off + c] = val;
+                    fdst[off + cw + lane] = hi[k];
+                }
+              } else if (to_bf16) {
+                lane_transpose<8>(hi, lane);
+                lane_transpose<8>(hi + 8, lane);
+                const int c0 = cw + 8 * (lane >> 3);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int64_t off = s_off[16 * ch + 8 * h + (lane & 7)];
+                  if (off >= 0) {
+                    const float* a = hi + 8 * h;
+                    *reinterpret_cast<uint4*>(hdst + off + c0) =
+                        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                   pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) lane_transpose<4>(hi + 4 * g, lane);
+                const int c0 = cw + 4 * (lane >> 2);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const int64_t off = s_off[16 * ch + 4 * g + (lane & 3)];
+                  if (off >= 0)
+                    *reinterpret_cast<float4*>(fdst + off + c0) =
+                        make_float4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
                 }
               }
             }

@@ -150,6 +150,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// Bring the 128-byte line holding `p` into this SM's L1 (a hint: nothing waits for it).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 // Arrive on `bar` once all cp.async issued so far by this thread have completed (the
 // arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

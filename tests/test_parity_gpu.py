@@ -61,6 +61,29 @@ def test_fp32_output(pm):
     _check(case, o_dtype=torch.float32)
 
 
+@pytest.mark.parametrize("dtype,width", [(torch.bfloat16, 516), (torch.bfloat16, 520),
+                                          (torch.float32, 514), (torch.float32, 516)])
+def test_output_row_strides(pm, dtype, width):
+    """o as a view of a wider buffer: head strides that do (520, 516 fp32) and do not (516
+    bf16, 514 fp32) allow 16-byte stores; both store paths must write exactly o's columns."""
+    case = gu.to_device(mla_inputs.make_custom([700, 300, 1], q_lens=[1, 2, 1], H=12, seed=9,
+                                               q_scale=1.0, kv_scale=1.0, name="strided"))
+    n_tok = case.q.shape[0]
+    base = torch.full((n_tok, 12, width), 7.0, dtype=dtype, device="cuda")
+    o = base[:, :, :512]
+    lse = torch.empty((n_tok, 12), dtype=torch.float32, device="cuda")
+    for splits in (0, 1):
+        ws = pm.make_workspace(case.B, 12, case.max_seqlen_q, splits, "cuda")
+        pm.mla_decode(case.q, case.kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                      case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
+                      case.kv_scale, num_kv_splits=splits, lse_out=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert pm.mla_check_error(ws) == 0
+        o_ref, lse_ref = gu.run_oracle(case)
+        gu.compare(o, lse, o_ref, lse_ref, what=f"strided {width} splits {splits}")
+        assert bool((base[:, :, 512:] == 7.0).all()), "write past the row's 512 columns"
+
+
 @pytest.mark.parametrize("H", [16, 24, 40, 96])
 def test_head_counts(pm, H):
     """16 -> one 16-row group, 24 -> 32-row group, 40 -> 48-row group, 96 -> two 48-row groups."""
