@@ -185,6 +185,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// q rows [qrow, qrow + NG) of the group into shared memory: one TMA tile load per
+// 128-byte latent block and one for the rope block, completing on `bar`.  Rows past the
+// unit's real rows belong to other requests (or are out of range and read zeros); their
+// columns are discarded.
+template <int NG>
+__device__ __forceinline__ void issue_q_load(uint32_t sQ, const CUtensorMap* lat,
+                                             const CUtensorMap* rope, int qrow, uint32_t bar) {
+  mbar_arrive_expect_tx(bar, NG * kD);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tma_load_2d(sQ + c * NG * 128, lat, c * 128, qrow, bar);
+  tma_load_2d(sQ + 4 * NG * 128, rope, 512, qrow, bar);
+}
+
 template <int NG, int STAGES>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
@@ -199,6 +212,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint32_t mbase = sbase + LY::kMiscOff;
   uint8_t* misc = smem + LY::kMiscOff;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc + kMiscTmem);
+  const uint32_t sQ = sbase + LY::kQOff;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + kMiscAbort);
   float* red = reinterpret_cast<float*>(misc + kMiscRed);
 
@@ -207,6 +221,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     return;
   }
 
+  if (threadIdx.x == 64) {   // descriptors of the q loads, fetched while the schedule is read
+    prefetch_tensormap(&tm_q_lat);
+    prefetch_tensormap(&tm_q_rope);
+  }
   // The schedule reads kv_indptr and then qo_indptr; fetch both arrays' first lines at
   // once so that the second read does not wait for a second trip to memory.
   if (threadIdx.x < 64) {
@@ -215,14 +233,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   PieceIter iter;
   iter.init(prm.sp, blockIdx.x);
+  int first_qrow;   // q row of the first piece's group (its q load starts in the set-up)
   {
-    PieceIter probe;
-    probe.init(prm.sp, blockIdx.x);
     Piece pc;
     int bad = 0;
-    if (!probe.next(pc, &bad)) {    // no work for this CTA (uniform across the block)
+    if (!iter.next(pc, &bad)) {    // no work for this CTA (uniform across the block)
       if (bad && threadIdx.x == 0) atomicOr(prm.err, kErrBadIndptr);
       return;
+    }
+    iter.hold(pc);                 // every role starts from this piece
+    first_qrow = pc.qo0 * prm.sp.H + pc.g * NG;
+    // the first tile's row ids: their fetch overlaps the set-up below
+    if (threadIdx.x < kTile / 32) {
+      const int64_t gi = pc.kv0 + pc.j0 + 32 * threadIdx.x;
+      if (gi >= 0 && gi < prm.kv_indices_len) prefetch_l1(prm.kv_indices + gi);
     }
   }
 
@@ -242,14 +266,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(mbase + kMiscDrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    issue_q_load<NG>(sQ, &tm_q_lat, &tm_q_rope, first_qrow, mbase + kMiscQFull);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(misc + kMiscTmem), LY::kTmemCols);
     tmem_relinquish();
-  }
-  if (threadIdx.x == 0) {
-    prefetch_tensormap(&tm_q_lat);
-    prefetch_tensormap(&tm_q_rope);
   }
   tc_fence_before();
   __syncthreads();
@@ -259,12 +280,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sQ = sbase + LY::kQOff;
   int bad = 0;
 
   if (warp >= kSoftmaxWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ===================================================== softmax + epilogue (4 warps)
+    // The softmax warps read their first piece again (from memory: off their critical path,
+    // they wait for the first tile's logits) and so keep no held piece in registers.
+    iter.init(prm.sp, blockIdx.x);
     const int q4 = warp & 3;                 // TMEM lane quadrant this warp may access
     const int prow = 32 * q4 + lane;         // position within the tile == TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
@@ -428,7 +451,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (n < pc.rows) {
               if (direct) {
                 const int rr = pc.g * NG + n;              // row within the request
-                const int64_t tok = static_cast<int64_t>(prm.sp.qo_indptr[pc.b]) + rr / H;
+                const int64_t tok = static_cast<int64_t>(pc.qo0) + rr / H;
                 const int64_t r = tok * H + rr % H;
                 if (r < prm.n_q_rows) {
                   off = tok * prm.o_stride_tok + (rr % H) * prm.o_stride_head;
@@ -527,25 +550,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       while (!aborted && iter.next(pc, &bad)) {
         const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
         if (warp == 0 && lane == 0) {
-          // q rows of this piece: one TMA tile load per 128-byte latent block + rope block.
-          // Rows past the unit's real rows belong to other requests (or are out of range and
-          // read zeros); their columns are discarded.
-          if (n_piece > 0 &&
-              !mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
+          // q rows of this piece, once the previous piece's QK has released the buffer
+          // (the first piece's load was issued during the set-up)
+          if (n_piece == 0) {
+            ++q_loads;
+          } else if (!mbar_wait(mbase + kMiscQEmpty, (n_piece - 1) & 1, abort_flag, prm.err)) {
             aborted = true;
           } else {
-            const int qrow = prm.sp.qo_indptr[pc.b] * prm.sp.H + pc.g * NG;
-            mbar_arrive_expect_tx(mbase + kMiscQFull, NG * kD);
-  #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(sQ + c * NG * 128, &tm_q_lat, c * 128, qrow, mbase + kMiscQFull);
-            tma_load_2d(sQ + 4 * NG * 128, &tm_q_rope, 512, qrow, mbase + kMiscQFull);
+            issue_q_load<NG>(sQ, &tm_q_lat, &tm_q_rope, pc.qo0 * prm.sp.H + pc.g * NG,
+                             mbase + kMiscQFull);
             ++q_loads;
           }
         }
         aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
         if (aborted) break;
-        const int64_t kvbase = prm.sp.kv_indptr[pc.b];
+        const int64_t kvbase = pc.kv0;
         // row id of row j of this warp in tile t (-1: past the piece or invalid)
         auto load_row = [&](int t, int j) -> int {
           if (j >= rows_w) return -1;

@@ -68,6 +68,8 @@ struct Piece {
   int rows;        // real query rows in this group (<= NG)
   int64_t slot;    // partial slot (ignored when direct)
   bool direct;     // this piece is the whole unit: write o / lse directly
+  int64_t kv0;     // kv_indptr[b]: position j of the request is kv_indices[kv0 + j]
+  int qo0;         // qo_indptr[b]: first query token of the request
 };
 
 // Effective CTA count of the auto policy for a line of W positions.
@@ -113,6 +115,8 @@ struct PieceIter {
   int Gp;
   int64_t x, x1;       // auto policy cursor
   int64_t p, p_end;    // fixed policy cursor
+  Piece held;          // returned again by the next call of next() when have_held
+  bool have_held;
 
   // Every member is assigned on every path: the iterator is only ever constructed with
   // init(), never copied.
@@ -130,6 +134,8 @@ struct PieceIter {
     Gp = 0;
     x = x1 = 0;
     p = p_end = 0;
+    have_held = false;
+    held = Piece{0, 0, 0, 0, 0, 0, 0, 0, false, 0, 0};
     if (sp.splits <= 0) {
       W = static_cast<int64_t>(sp.groups) * (sp.kv_indptr[sp.B] - sp.kv_indptr[0]);
       Gp = auto_ctas(W, sp.grid);
@@ -145,7 +151,19 @@ struct PieceIter {
     }
   }
 
+  // Make the next call of next() return pc again (the piece it returned last), so that a
+  // piece computed once up front is not recomputed from memory by every role.
+  PMLA_HD void hold(const Piece& pc) {
+    held = pc;
+    have_held = true;
+  }
+
   PMLA_HD bool next(Piece& pc, int* bad) {
+    if (have_held) {
+      have_held = false;
+      pc = held;
+      return true;
+    }
     while (true) {
       if (sp.splits <= 0) {
         if (x >= x1) return false;
@@ -190,7 +208,9 @@ struct PieceIter {
         pc.direct = (sp.splits == 1);
         p += sp.grid;
       }
-      pc.T = sp.qo_indptr[pc.b + 1] - sp.qo_indptr[pc.b];
+      pc.kv0 = sp.kv_indptr[pc.b];
+      pc.qo0 = sp.qo_indptr[pc.b];
+      pc.T = sp.qo_indptr[pc.b + 1] - pc.qo0;
       const int rows_req = pc.T * sp.H;
       int rows = rows_req - pc.g * sp.NG;
       if (rows > sp.NG) rows = sp.NG;
