@@ -49,6 +49,9 @@ WORKLOAD_TEXT = {
 }
 
 
+SOAK_S = 1.0   # shortest span of steps the clock record covers
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "paged_mla_latent_gb300", "csrc", "*"))):
@@ -81,7 +84,7 @@ def recorded_traffic(config: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while the GPU runs the steps."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -95,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -240,6 +243,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-l2-flush", action="store_true")
+    ap.add_argument("--clock-soak-s", type=float, default=SOAK_S,
+                    help="shortest span of steps the nvidia-smi clock record covers")
     ap.add_argument("--eager", action="store_true",
                     help="time eager calls instead of a CUDA-graph replay of the call")
     ap.add_argument("--ref-requests", type=int, default=2)
@@ -317,6 +322,20 @@ def main():
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
+        # nvidia-smi samples every 100 ms: when the K timed steps take less than a second,
+        # the same steps keep running (untimed) until a second has passed, so the clock
+        # record covers this load.
+        soak = 0
+        while time.perf_counter() - t_wall0 < args.clock_soak_s:
+            for i in range(64):
+                if not args.no_l2_flush:
+                    flush.fill_((i + 3) & 0xFF)
+                if graph is not None:
+                    graph.replay()
+                else:
+                    call()
+            soak += 64
+            torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     st = pm.mla_check_error(ws)
@@ -399,7 +418,10 @@ def main():
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
-            "clocks": clocks.summary(),
+            "clocks": dict(clocks.summary(),
+                           window=("the timed region" if soak == 0 else
+                                   f"the timed region and {soak} identical untimed steps "
+                                   f"right after it ({args.clock_soak_s:g} s in all)")),
             "wall_s_timed_region": t_wall,
             "timing": "CUDA graph replay of one call per step" if graph is not None else "eager calls",
             "host_us_per_eager_call": t_host * 1e6,
