@@ -140,6 +140,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, bytes_per_rank: int, ms: float) -> float:
+    """GB/s of the whole job: every rank processes its own batch of bytes_per_rank in ms."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -343,14 +357,11 @@ def main():
         raise RuntimeError(f"device error in the timed region: {pm.mla_status_string(st)}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = sum(step_ms) / len(step_ms)
-    if dist is not None:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dist, dev)
 
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
     algo = mla_inputs.algorithmic_bytes(case)
-    value = world * gathered / (mean_ms * 1e-3) / 1e9
+    value = whole_job_rate(world, gathered, mean_ms)
     peak, peak_kind = measured_peaks()
     achieved = algo / (mean_ms * 1e-3) / 1e9
 
@@ -383,8 +394,8 @@ def main():
             torch.cuda.synchronize(dev)
             if i >= 2:
                 e_ms.append((time.perf_counter() - t0) * 1e3)
-        e_mean = sum(e_ms) / len(e_ms)
-        e2e = {"value": world * gathered / (e_mean * 1e-3) / 1e9, "unit": UNIT,
+        e_mean = max_over_ranks(sum(e_ms) / len(e_ms), dist, dev)
+        e2e = {"value": whole_job_rate(world, gathered, e_mean), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_mean}
 
     cpu_base = None

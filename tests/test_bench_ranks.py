@@ -1,0 +1,79 @@
+"""The multi-rank path of bench.py on CPU: gloo process groups of two ranks.
+
+On a GPU node bench.py runs one independent replica per GPU (no data exchange); the job's
+time is the slowest rank's and its throughput the sum over ranks.  These tests exercise that
+host logic, and the reference arm's rank handling, without a GPU.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        slowest = bench.max_over_ranks(10.0 + 5.0 * rank, dist, "cpu")
+        rate = bench.whole_job_rate(world, 1_000_000_000, slowest)
+        out.put((rank, slowest, rate))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_rate_gloo():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(out.get(timeout=10) for _ in range(2))
+    # both ranks see the slower rank's 15 ms; two ranks x 1 GB in 15 ms = 133.3 GB/s
+    for rank, slowest, rate in got:
+        assert slowest == 15.0
+        assert rate == pytest.approx(2 * 1.0 / 0.015)
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
+    assert bench.whole_job_rate(1, 576_000, 1.0) == pytest.approx(0.576)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Under torchrun with two CPU ranks the oracle arm runs on rank 0 only: one JSON line,
+    every rank exits 0."""
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "1",
+           "--warmup", "0"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
