@@ -129,8 +129,10 @@ constexpr int kPGroup = kTile * 16;   // 2048
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // The reference max moves only when a logit exceeds it by more than kTau (log2 units),
-// so P stays <= 2^kTau = 256 < 448 (e4m3 max) and O is rescaled rarely.
-constexpr float kTau = 8.0f;
+// so O is rescaled rarely and p <= 2^kTau = 16.  The bound keeps both FP8 planes of P in
+// range: e4m3 rounds p to hi within p / 16, so the lo plane 256 (p - hi) stays below
+// 256 < 448 (the e4m3 maximum); a larger headroom would saturate lo for p > 28.
+constexpr float kTau = 4.0f;
 constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
 // Initial reference max: finite, so that p = 2^(x - ref) needs no special case (masked
 // logits are -inf and give 0) and the first tile always moves it (x - ref > kTau).

@@ -303,7 +303,7 @@ def test_context_shard_merge_small(pm):
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_running_max_rescale_every_tile(pm, splits):
     """Cache rows rise tile by tile so that, for heads 0-5, every 128-position tile's logits
-    exceed the previous tile's by ~10 nats (more than the 2^8 headroom of the reference
+    exceed the previous tile's by ~10 nats (more than the headroom of the reference
     max): the kernel must move its reference and rescale the accumulated output on every
     tile.  Heads 6-11 see a slow rise (no rescale).  Values carry random latent parts."""
     L = 15 * 128 + 37
@@ -318,6 +318,34 @@ def test_running_max_rescale_every_tile(pm, splits):
     q[0, :6, :] = f8(1.0)
     q[0, 6:, :] = f8(0.125)
     q[0, :, 300:512] = 0                                  # those columns do not enter the logits
+    case.kv = keys
+    case.q = q
+    _check(case, num_kv_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [0, 1])
+def test_logit_jump_within_reference_headroom(pm, splits):
+    """A position in a later tile whose logit is 5-7.5 log2 units above every earlier one
+    and whose values are large.  However the kernel treats the jump (moving its reference
+    max, or keeping it and giving the position a weight p = 2^5..2^7.5), the weight must
+    reach the tensor core with the hi/lo precision: a lo plane 256 (p - hi) that saturates
+    at the e4m3 maximum misweights such a position by a few percent.  No head's jump is
+    large enough to force a move on its own (a move for one head moves its whole
+    16-column chunk)."""
+    L = 6 * 128 + 11
+    spike = 700
+    case = mla_inputs.make_custom([L], H=12, seed=23, q_scale=1.0, kv_scale=1.0)
+    f8 = lambda x: torch.tensor([x]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    idx = case.kv_indices[:L].long()
+    keys = case.kv.clone()
+    keys[idx, 512:] = 0                                   # rope columns: logits 0 ...
+    keys[idx[spike], 512:] = f8(1.0)                      # ... except at the jump
+    keys[idx[spike], :512] = f8(320.0)                    # large values at the jump
+    q = case.q.clone()
+    q[0, :, :512] = 0                                     # logits from the rope part only
+    qvs = [0.75, 0.8125, 0.875, 0.9375, 1.0, 1.125, 1.125, 1.0, 0.9375, 0.875, 0.8125, 0.75]
+    for h, qv in enumerate(qvs):
+        q[0, h, 512:] = f8(qv)                            # jump = 6.66 * qv log2 units
     case.kv = keys
     case.q = q
     _check(case, num_kv_splits=splits)
