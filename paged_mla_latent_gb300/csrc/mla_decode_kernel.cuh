@@ -25,9 +25,10 @@
 //                     two P planes side by side).
 //   softmax warps   : (warps 8-11) read S^T from TMEM (one position per thread), scale, mask,
 //                     online softmax in the exp2 domain with a lazily moved reference
-//                     max, and write P as two FP8 planes: hi = e4m3(p) and
-//                     lo = e4m3(256 * (p - hi)), so P reaches the tensor core with
-//                     ~2^-8 relative precision while staying an FP8 x FP8 product.
+//                     max, and write P (scaled by 2^6 relative to that max) as two FP8
+//                     planes: hi = e4m3(p) and lo = e4m3(16 * (p - hi)), so P reaches
+//                     the tensor core with ~2^-8 relative precision for weights down to
+//                     2^-12 of the max while staying an FP8 x FP8 product.
 //                     At the end of a piece they normalise O and write o / lse (or a
 //                     normalised partial for the merge kernel).
 #pragma once
@@ -128,14 +129,23 @@ constexpr int kPGroup = kTile * 16;   // 2048
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// The reference max moves only when a logit exceeds it by more than kTau (log2 units),
-// so O is rescaled rarely and p <= 2^kTau = 16.  The bound keeps both FP8 planes of P in
-// range: e4m3 rounds p to hi within p / 16, so the lo plane 256 (p - hi) stays below
-// 256 < 448 (the e4m3 maximum); a larger headroom would saturate lo for p > 28.
-constexpr float kTau = 4.0f;
-constexpr float kLoScale = 256.0f;   // lo plane carries 256 * (p - hi)
+// P in FP8.  Each column keeps m = (reference max) - kPShift, and a logit x (log2 units)
+// becomes p = 2^(x - m): the column's probabilities scaled by 2^kPShift relative to the
+// reference.  The reference moves only when a logit exceeds it by more than kHeadroom, so
+// O is rescaled rarely and p <= 2^kMoveAt = 256 (< 448, the e4m3 maximum).  p reaches the
+// tensor core as two planes, hi = e4m3(p) and lo = e4m3(kLoScale (p - hi)): e4m3 rounds p
+// within p / 16, so lo <= p <= 256 also fits, and hi + lo / kLoScale carries ~2^-8
+// relative precision for every p >= 2^-6, i.e. for weights down to 2^-12 of the reference
+// (a sink far above a large uniform bulk keeps the bulk's mass).  The row sum l accumulates
+// the same scaled p, so o = (O_hi + O_lo / kLoScale) / l and lse = (m + log2 l) ln 2 need
+// no correction for the scale.
+constexpr float kPShift = 6.0f;
+constexpr float kHeadroom = 2.0f;
+constexpr float kMoveAt = kHeadroom + kPShift;
+constexpr float kLoScale = 16.0f;
+constexpr uint32_t kLoScaleF16x2 = 0x4C004C00u;   // kLoScale as two f16
 // Initial reference max: finite, so that p = 2^(x - ref) needs no special case (masked
-// logits are -inf and give 0) and the first tile always moves it (x - ref > kTau).
+// logits are -inf and give 0) and the first tile always moves it (x - m > kMoveAt).
 constexpr float kRefInit = -1.0e30f;
 
 // Warp-wide reduction of 16 per-lane column values v[0..15] (sum or max): four halving
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     uint32_t it_g = 0;
     Piece pc;
-    float m_ref[NG];
+    float m_ref[NG];   // reference max - kPShift, per column
     float l_acc[NG];
     while (iter.next(pc, &bad)) {
       const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             xs[k] = xform(xs[k], 16 * ch + k);
             dmax = fmaxf(dmax, xs[k] - m_ref[16 * ch + k]);
           }
-          if (bar_red_or(1, 128, dmax > kTau)) {
+          if (bar_red_or(1, 128, dmax > kMoveAt)) {
             // rare: move these columns' reference to their tile maxima
             {
               float v[16];
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               const int n = 16 * ch + k;
               const float4 r4 = *reinterpret_cast<const float4*>(red + 4 * k);
               const float tmax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
-              const float m_new = fmaxf(m_ref[n], tmax);
+              const float m_new = fmaxf(m_ref[n], tmax - kPShift);
               const float alpha = ex2_approx(m_ref[n] - m_new);   // 0 from the initial reference
               l_acc[n] *= alpha;
               m_ref[n] = m_new;
@@ -394,8 +404,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               tmem_wait_st();
             }
           }
-          // probabilities relative to the reference (<= 2^kTau), split into two FP8 planes:
-          // hi = e4m3(p), lo = e4m3(256 (p - hi)), the residual taken in f16x2
+          // scaled probabilities (<= 2^kMoveAt), split into two FP8 planes:
+          // hi = e4m3(p), lo = e4m3(kLoScale (p - hi)), the residual taken in f16x2
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
@@ -406,8 +416,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             l_acc[n + 1] += p1;
             const uint32_t p16 = f32x2_to_f16x2(p1, p0);          // low half: p0
             const uint32_t hi = f16x2_to_e4m3x2(p16);             // byte 0: p0, byte 1: p1
-            const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), 0x5C005C00u);
-            const uint32_t lo = f16x2_to_e4m3x2(r16);              // 256 (p - hi)
+            const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), kLoScaleF16x2);
+            const uint32_t lo = f16x2_to_e4m3x2(r16);              // kLoScale (p - hi)
             if ((k & 2) == 0) {
               hw[k >> 2] = hi;
               lw[k >> 2] = lo;

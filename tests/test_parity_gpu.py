@@ -349,3 +349,28 @@ def test_logit_jump_within_reference_headroom(pm, splits):
     case.kv = keys
     case.q = q
     _check(case, num_kv_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [0, 1])
+def test_sink_over_uniform_bulk(pm, splits):
+    """An attention sink at position 0 whose logit is ~11 log2 units above 2,000 identical
+    bulk positions: each bulk weight is ~2^-11 of the sink's, but together they carry about
+    half of the mass, and identical rows make any rounding of their weights systematic.  The
+    weights must keep the hi/lo precision even that far below the reference max."""
+    L = 2001
+    case = mla_inputs.make_custom([L], H=12, seed=29, q_scale=1.0, kv_scale=1.0)
+    f8 = lambda x: torch.tensor([x]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    idx = case.kv_indices[:L].long()
+    keys = case.kv.clone()
+    keys[idx, :] = f8(2.0)                                # bulk: identical rows, values 2
+    keys[idx, 512:] = 0                                   # bulk rope 0
+    keys[idx[0], :512] = 0                                # sink: values 0 ...
+    keys[idx[0], 512:] = f8(1.75)                         # ... rope 1.75
+    q = case.q.clone()
+    q[0, :, :512] = 0
+    qvs = [0.9375, 0.875, 1.0, 0.8125, 0.9375, 0.875, 1.0, 0.8125, 0.9375, 0.875, 1.0, 0.8125]
+    for h, qv in enumerate(qvs):
+        q[0, h, 512:] = f8(qv)                            # sink - bulk = 11.66 * qv log2 units
+    case.kv = keys
+    case.q = q
+    _check(case, num_kv_splits=splits)
