@@ -691,58 +691,106 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           mma_commit(mbase + kMiscSFull + 8 * (i & 1));
         };
-        // Issue loop.  QK of tile q needs its cache rows (full), the piece's q rows and a
-        // free S buffer (PV of tile q-2 issued); PV of tile p needs P (p_full).  Whichever
-        // is ready goes first, PV preferred: it releases a ring stage to the producers.
-        bool pv_first[2] = {false, false};
-        uint32_t q_next = 0, p_next = 0;   // next tile for QK / PV (CTA-wide numbering)
-        bool have_piece = false, q_ready = false;
-        int nt = 0, t_in = 0;
-        unsigned long long idle_since = 0;
-        while (true) {
-          while (!have_piece || t_in >= nt) {
-            if (!iter.next(pc, &bad)) {
-              have_piece = false;
-              break;
+        if constexpr (STAGES >= 3) {
+          // Issue order: QK(0), QK(1), PV(0), QK(2), PV(1), ... (CTA-wide tile numbers): QK
+          // runs one tile ahead of PV, so the tensor pipe computes the next logits while the
+          // softmax warps work, and QK(i+1) reuses the S buffer of tile i-1 only after PV(i-1)
+          // was issued, i.e. after its softmax finished.  Each step waits (bounded) for its
+          // own inputs: the stage's rows (and the piece's q rows) for QK, P for PV.
+          uint32_t i = 0;              // next tile to QK
+          bool pend = false;           // the PV of tile pend_j is still to be issued
+          uint32_t pend_j = 0;
+          bool pend_first = false;     // ... and that tile is its piece's first
+          bool ok = true;
+          auto pv_step = [&]() {
+            const uint32_t j = pend_j;
+            if (!mbar_wait(mbase + kMiscPFull + 8 * (j & 1), (j >> 1) & 1, abort_flag, prm.err)) {
+              ok = false;
+              return;
             }
-            have_piece = true;
-            nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
-            t_in = 0;
-            q_ready = false;
-          }
-          if (!have_piece && p_next == q_next) break;   // everything issued
-          bool progressed = false;
-          if (p_next < q_next && mbar_test(mbase + kMiscPFull + 8 * (p_next & 1), (p_next >> 1) & 1)) {
-            issue_pv(p_next, pv_first[p_next & 1]);
-            ++p_next;
-            progressed = true;
-          } else if (have_piece && q_next <= p_next + 1) {
-            if (t_in == 0 && !q_ready) q_ready = mbar_test(mbase + kMiscQFull, n_piece & 1);
-            const int stage = static_cast<int>(q_next % STAGES);
-            if ((t_in > 0 || q_ready) &&
-                mbar_test(mbase + kMiscFull + 8 * stage, (q_next / STAGES) & 1)) {
-              issue_qk(q_next);
-              pv_first[q_next & 1] = (t_in == 0);
-              if (t_in == nt - 1) {
-                mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q rows
-                ++n_piece;
+            issue_pv(j, pend_first);
+            pend = false;
+          };
+          while (ok && iter.next(pc, &bad)) {
+            const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+            for (int t = 0; t < nt && ok; ++t) {
+              if (t == 0 && !mbar_wait(mbase + kMiscQFull, n_piece & 1, abort_flag, prm.err)) {
+                ok = false;
+                break;
               }
-              ++q_next;
-              ++t_in;
-              progressed = true;
+              const int stage = static_cast<int>(i % STAGES);
+              if (!mbar_wait(mbase + kMiscFull + 8 * stage, (i / STAGES) & 1, abort_flag, prm.err)) {
+                ok = false;
+                break;
+              }
+              issue_qk(i);
+              if (t == nt - 1) mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q
+              if (pend) pv_step();
+              pend = true;
+              pend_j = i;
+              pend_first = (t == 0);
+              ++i;
             }
+            ++n_piece;
           }
-          if (progressed) {
-            idle_since = 0;
-          } else {
-            if (*abort_flag) break;
-            const unsigned long long now = globaltimer_ns();
-            if (idle_since == 0) {
-              idle_since = now;
-            } else if (now - idle_since > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicOr(prm.err, kErrTimeout);
-              break;
+          if (ok && pend) pv_step();
+        } else {
+          // With two stages, QK(i+1) needs the stage PV(i-1) is about to release: a fixed
+          // order would idle the tensor pipe on that reload, so issue whichever step is
+          // ready first.
+          // Issue loop.  QK of tile q needs its cache rows (full), the piece's q rows and a
+          // free S buffer (PV of tile q-2 issued); PV of tile p needs P (p_full).  Whichever
+          // is ready goes first, PV preferred: it releases a ring stage to the producers.
+          bool pv_first[2] = {false, false};
+          uint32_t q_next = 0, p_next = 0;   // next tile for QK / PV (CTA-wide numbering)
+          bool have_piece = false, q_ready = false;
+          int nt = 0, t_in = 0;
+          unsigned long long idle_since = 0;
+          while (true) {
+            while (!have_piece || t_in >= nt) {
+              if (!iter.next(pc, &bad)) {
+                have_piece = false;
+                break;
+              }
+              have_piece = true;
+              nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+              t_in = 0;
+              q_ready = false;
+            }
+            if (!have_piece && p_next == q_next) break;   // everything issued
+            bool progressed = false;
+            if (p_next < q_next && mbar_test(mbase + kMiscPFull + 8 * (p_next & 1), (p_next >> 1) & 1)) {
+              issue_pv(p_next, pv_first[p_next & 1]);
+              ++p_next;
+              progressed = true;
+            } else if (have_piece && q_next <= p_next + 1) {
+              if (t_in == 0 && !q_ready) q_ready = mbar_test(mbase + kMiscQFull, n_piece & 1);
+              const int stage = static_cast<int>(q_next % STAGES);
+              if ((t_in > 0 || q_ready) &&
+                  mbar_test(mbase + kMiscFull + 8 * stage, (q_next / STAGES) & 1)) {
+                issue_qk(q_next);
+                pv_first[q_next & 1] = (t_in == 0);
+                if (t_in == nt - 1) {
+                  mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q rows
+                  ++n_piece;
+                }
+                ++q_next;
+                ++t_in;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              idle_since = 0;
+            } else {
+              if (*abort_flag) break;
+              const unsigned long long now = globaltimer_ns();
+              if (idle_since == 0) {
+                idle_since = now;
+              } else if (now - idle_since > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(prm.err, kErrTimeout);
+                break;
+              }
             }
           }
         }
