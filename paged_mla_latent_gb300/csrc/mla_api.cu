@@ -173,7 +173,16 @@ struct Plan {
   int NG, groups, grid, splits;
   int64_t slots;
   size_t lse_off, o_off, bytes;
+  // Shared-prefix cascade (automatic policy, decode batches of <= 24 rows per request):
+  // prefix pass over groups of gsize requests with 48-row tiles, partials after the
+  // plain layout; cbytes = workspace for the plain layout plus those.
+  bool cascade_ok;
+  int gsize;
+  int64_t pslots;
+  size_t plse_off, po_off, cbytes;
 };
+constexpr size_t kSharedOff = 128;   // int32 in the header: the shared prefix length
+constexpr int kPrefixNG = 48;
 
 int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Plan* p) {
   if (B < 0 || H < 1 || H > kMaxHeads || max_seqlen_q < 1 || max_seqlen_q > kMaxSeqlenQ)
@@ -188,7 +197,134 @@ int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Pl
   p->lse_off = kHeaderBytes;
   p->o_off = align_up(p->lse_off + static_cast<size_t>(p->slots) * p->NG * sizeof(float), 256);
   p->bytes = p->o_off + static_cast<size_t>(p->slots) * p->NG * kDV * sizeof(float);
+  p->cascade_ok = false;
+  p->gsize = 1;
+  p->pslots = 0;
+  p->plse_off = p->po_off = p->bytes;
+  p->cbytes = p->bytes;
+  if (p->splits == 0 && rows <= kPrefixNG / 2 && B >= kPrefixNG / rows) {
+    // (at least one full group: for fewer requests the extra launches cost more than
+    // sharing the prefix saves)
+    p->cascade_ok = true;
+    p->gsize = kPrefixNG / rows;
+    const int VB = (B + p->gsize - 1) / p->gsize;
+    p->pslots = partial_slots(VB, 1, 0, p->grid);
+    p->plse_off = align_up(p->bytes, 256);
+    p->po_off = align_up(p->plse_off + static_cast<size_t>(p->pslots) * kPrefixNG * sizeof(float), 256);
+    p->cbytes = p->po_off + static_cast<size_t>(p->pslots) * kPrefixNG * kDV * sizeof(float);
+  }
   return MLA_OK;
+}
+
+}  // namespace
+
+// Workspace of the plain decode (whole) and of the shared-prefix cascade (cascade >=
+// whole); the cascade runs when the caller's workspace holds it.
+int pmla_workspace_sizes(int B, int H, int max_seqlen_q, int num_kv_splits, int sms,
+                         size_t* whole, size_t* cascade) {
+  if (sms <= 0) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if ((rc = device_sms(dev, &sms))) return rc;
+  }
+  Plan p;
+  const int rc = make_plan(B, H, max_seqlen_q, num_kv_splits, sms, &p);
+  if (rc) return rc;
+  *whole = p.bytes;
+  *cascade = p.cbytes;
+  return MLA_OK;
+}
+
+namespace {
+
+// Shared-prefix cascade: find the prefix P every request shares (device), run the
+// prefix pass (groups of plan.gsize requests, 48-row tiles) and the suffix pass (each
+// request's own positions) into partials, then merge the two per output row.  With no
+// shared prefix (P below kMinShared) the prefix pass has no work, the suffix pass is the
+// plain decode and the merge touches only the units that were split.
+int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr, int64_t q_rows,
+                   const mla_tensor_t* kv_indices, const CUtensorMap& q_lat,
+                   const CUtensorMap& q_rope, cudaStream_t stream) {
+  uint8_t* ws = reinterpret_cast<uint8_t*>(prm.err);
+  int32_t* shared = reinterpret_cast<int32_t*>(ws + kSharedOff);
+  if (cudaMemsetAsync(shared, 0x7F, sizeof(int32_t), stream) != cudaSuccess) return MLA_ERR_CUDA;
+  SharedPrefixParams sp;
+  sp.kv_indptr = prm.sp.kv_indptr;
+  sp.qo_indptr = prm.sp.qo_indptr;
+  sp.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
+  sp.kv_indices_len = prm.kv_indices_len;
+  sp.B = prm.sp.B;
+  sp.shared = shared;
+  mla_shared_prefix_kernel<<<plan.grid * 2, 256, 0, stream>>>(sp);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+  CUtensorMap p_lat, p_rope;
+  int rc;
+  if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  if ((rc = make_map(&p_rope, q_ptr, q_rows, kD, 64, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
+  DecodeParams pp = prm;
+  pp.sp.mode = kSchedPrefix;
+  pp.sp.NG = kPrefixNG;
+  pp.sp.groups = 1;
+  pp.sp.gsize = plan.gsize;
+  pp.sp.shared = shared;
+  pp.part_lse = reinterpret_cast<float*>(ws + plan.plse_off);
+  pp.part_o = reinterpret_cast<float*>(ws + plan.po_off);
+  pp.n_slots = plan.pslots;
+  if ((rc = launch_decode_ng48(p_lat, p_rope, pp, plan.grid, stream))) return rc;
+
+  DecodeParams ps = prm;
+  ps.sp.mode = kSchedSuffix;
+  ps.sp.gsize = plan.gsize;
+  ps.sp.shared = shared;
+  switch (plan.NG) {
+    case 16: rc = launch_decode_ng16(q_lat, q_rope, ps, plan.grid, stream); break;
+    default: rc = launch_decode_ng32(q_lat, q_rope, ps, plan.grid, stream); break;
+  }
+  if (rc) return rc;
+
+  CascadeMergeParams mp;
+  mp.ss = ps.sp;
+  mp.sp = pp.sp;
+  mp.s_o = ps.part_o;
+  mp.s_lse = ps.part_lse;
+  mp.p_o = pp.part_o;
+  mp.p_lse = pp.part_lse;
+  mp.s_slots = ps.n_slots;
+  mp.p_slots = pp.n_slots;
+  mp.o = prm.o;
+  mp.o_fp32 = prm.o_fp32;
+  mp.o_stride_tok = prm.o_stride_tok;
+  mp.o_stride_head = prm.o_stride_head;
+  mp.lse_out = prm.lse_out;
+  mp.n_q_rows = q_rows;
+  mp.err = prm.err;
+  const int64_t units = static_cast<int64_t>(prm.sp.B) * plan.groups;
+  const int VB = (prm.sp.B + plan.gsize - 1) / plan.gsize;
+  // partials per row: the CTAs of one prefix group plus those of one suffix
+  const int lanes = merge_lanes_for(plan.grid / VB + plan.grid / (units > 0 ? units : 1) + 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), lanes / 2);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  switch (lanes) {
+    case 64: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<64>, mp); break;
+    case 32: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<32>, mp); break;
+    case 16: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<16>, mp); break;
+    case 8: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<8>, mp); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<4>, mp); break;
+    default: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<2>, mp); break;
+  }
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -223,7 +359,7 @@ int mla_get_workspace_size(int32_t batch_size, int32_t num_heads, int32_t max_se
   Plan p;
   int rc = make_plan(batch_size, num_heads, max_seqlen_q, num_kv_splits, sms, &p);
   if (rc) return rc;
-  *bytes_out = p.bytes;
+  *bytes_out = p.cbytes;
   return MLA_OK;
 }
 
@@ -267,6 +403,9 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.sp.groups = plan.groups;
   prm.sp.splits = plan.splits;
   prm.sp.grid = plan.grid;
+  prm.sp.mode = kSchedWhole;
+  prm.sp.gsize = 1;
+  prm.sp.shared = nullptr;
   prm.kv = static_cast<const uint8_t*>(kv_buffer->ptr);
   prm.kv_pitch = cs.kv_pitch;
   prm.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
@@ -290,6 +429,9 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.part_o = reinterpret_cast<float*>(ws + plan.o_off);
   prm.n_slots = plan.slots;
   prm.err = reinterpret_cast<int*>(ws);
+
+  if (plan.cascade_ok && workspace_bytes >= plan.cbytes)
+    return launch_cascade(plan, prm, q->ptr, q_rows, kv_indices, q_lat, q_rope, stream);
 
   switch (plan.NG) {
     case 16: rc = launch_decode_ng16(q_lat, q_rope, prm, plan.grid, stream); break;
@@ -329,7 +471,9 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
     case 64: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<64>, mp); break;
     case 32: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<32>, mp); break;
     case 16: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<16>, mp); break;
-    default: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<8>, mp); break;
+    case 8: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<8>, mp); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<4>, mp); break;
+    default: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<2>, mp); break;
   }
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -382,7 +526,9 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
     case 64: mla_csr_merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(prm); break;
     case 32: mla_csr_merge_kernel<32><<<grid, kMergeThreads, 0, stream>>>(prm); break;
     case 16: mla_csr_merge_kernel<16><<<grid, kMergeThreads, 0, stream>>>(prm); break;
-    default: mla_csr_merge_kernel<8><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    case 8: mla_csr_merge_kernel<8><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    case 4: mla_csr_merge_kernel<4><<<grid, kMergeThreads, 0, stream>>>(prm); break;
+    default: mla_csr_merge_kernel<2><<<grid, kMergeThreads, 0, stream>>>(prm); break;
   }
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -8,8 +8,8 @@
 
 namespace pmla {
 
-template <int NG, int STAGES>
-int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+template <int NG, int STAGES, int MODE>
+int launch_decode_mode(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream) {
   using LY = DecodeLayout<NG, STAGES>;
   static std::mutex mu;
@@ -19,16 +19,27 @@ int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(mla_decode_kernel<NG, STAGES>,
+      if (cudaFuncSetAttribute(mla_decode_kernel<NG, STAGES, MODE>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                LY::kSmemBytes) != cudaSuccess)
         return MLA_ERR_CUDA;
       attr_set[dev] = true;
     }
   }
-  mla_decode_kernel<NG, STAGES><<<grid, kDecodeThreads, LY::kSmemBytes, stream>>>(q_lat, q_rope,
-                                                                                   prm);
+  mla_decode_kernel<NG, STAGES, MODE><<<grid, kDecodeThreads, LY::kSmemBytes, stream>>>(
+      q_lat, q_rope, prm);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// The plain decode, or the cascade half (CASCADE) this row-group size runs.
+template <int NG, int STAGES, int CASCADE>
+int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+                       const DecodeParams& prm, int grid, cudaStream_t stream) {
+  if (prm.sp.mode == kSchedWhole)
+    return launch_decode_mode<NG, STAGES, kSchedWhole>(q_lat, q_rope, prm, grid, stream);
+  if (prm.sp.mode == CASCADE)
+    return launch_decode_mode<NG, STAGES, CASCADE>(q_lat, q_rope, prm, grid, stream);
+  return MLA_ERR_UNSUPPORTED;
 }
 
 }  // namespace pmla

@@ -210,7 +210,9 @@ __device__ __forceinline__ void issue_q_load(uint32_t sQ, const CUtensorMap* lat
   tma_load_2d(sQ + 4 * NG * 128, rope, 512, qrow, bar);
 }
 
-template <int NG, int STAGES>
+// MODE: the schedule (kSchedWhole for a plain decode, kSchedPrefix / kSchedSuffix for the
+// two halves of the shared-prefix cascade), fixed at compile time.
+template <int NG, int STAGES, int MODE>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
                       const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams prm) {
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int i = 32 * (threadIdx.x >> 1);
     if (i <= prm.sp.B) prefetch_l1((threadIdx.x & 1) ? prm.sp.qo_indptr + i : prm.sp.kv_indptr + i);
   }
-  PieceIter iter;
+  PieceIterT<MODE> iter;
   iter.init(prm.sp, blockIdx.x);
   int first_qrow;   // q row of the first piece's group (its q load starts in the set-up)
   {
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         m_ref[n] = kRefInit;
         l_acc[n] = 0.f;
       }
-      const int causal_from = pc.L - pc.T;   // positions beyond this need the causal test
+      const int causal_from = pc.cfrom;   // positions beyond this need the causal test
       // draft t of this group's row n sees positions <= L - T + t
       if (prow < NG) s_lim[prow] = causal_from + (pc.g * NG + prow) / H;
       bar_sync(1, 128);

@@ -25,10 +25,13 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeUnroll = 4;          // partials in flight per thread
 
-// Partial lanes for an average of `per_row` partials per merged row: 8, 16, 32 or 64.
+// Partial lanes for an average of `per_row` partials per merged row: 2 .. 64 (2: one
+// block holds a whole 512-column row).
 inline int merge_lanes_for(int64_t per_row) {
-  return per_row >= 96 ? 64 : per_row >= 40 ? 32 : per_row >= 16 ? 16 : 8;
+  return per_row >= 96 ? 64 : per_row >= 40 ? 32 : per_row >= 16 ? 16 : per_row >= 8 ? 8
+       : per_row >= 4 ? 4 : 2;
 }
+constexpr int kMergeBlocksPerSm = 3;   // launch bound: registers for 3 resident blocks
 
 struct MergeOut {
   void* o;
@@ -65,10 +68,13 @@ __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const Me
                                      int col0) {
   constexpr int Q = kMergeThreads / P;    // column quads per block
   constexpr int kCols = 4 * Q;
-  static_assert(Q <= 32 && Q * P == kMergeThreads, "bad merge shape");
-  __shared__ float s_m[kMergeWarps][Q];
-  __shared__ float s_w[kMergeWarps][Q];
-  __shared__ float4 s_acc[kMergeWarps][Q];
+  // Rows of partial states left after the in-warp combine: one per warp when a warp holds
+  // several partial lanes of the same columns (Q < 32), else one per partial lane.
+  constexpr int R = Q < 32 ? kMergeWarps : P;
+  static_assert(Q * P == kMergeThreads && kCols <= kDV, "bad merge shape");
+  __shared__ float s_m[R][Q];
+  __shared__ float s_w[R][Q];
+  __shared__ float4 s_acc[R][Q];
   const int c = threadIdx.x % Q;
   const int p = threadIdx.x / Q;
   MergeState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
@@ -85,48 +91,54 @@ __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const Me
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) merge_combine(st, l[u], 1.f, v[u]);
   }
-  // lanes q, q + Q, q + 2Q, ... of a warp hold the same columns
-#pragma unroll
-  for (int off = Q; off < 32; off <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, st.m, off);
-    const float w2 = __shfl_xor_sync(0xffffffffu, st.w, off);
-    float4 a2;
-    a2.x = __shfl_xor_sync(0xffffffffu, st.a.x, off);
-    a2.y = __shfl_xor_sync(0xffffffffu, st.a.y, off);
-    a2.z = __shfl_xor_sync(0xffffffffu, st.a.z, off);
-    a2.w = __shfl_xor_sync(0xffffffffu, st.a.w, off);
-    merge_combine(st, m2, w2, a2);
-  }
-  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (lane < Q) {
-    s_m[warp][lane] = st.m;
-    s_w[warp][lane] = st.w;
-    s_acc[warp][lane] = st.a;
+  if constexpr (Q < 32) {
+    // lanes q, q + Q, q + 2Q, ... of a warp hold the same columns
+#pragma unroll
+    for (int off = Q; off < 32; off <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, st.m, off);
+      const float w2 = __shfl_xor_sync(0xffffffffu, st.w, off);
+      float4 a2;
+      a2.x = __shfl_xor_sync(0xffffffffu, st.a.x, off);
+      a2.y = __shfl_xor_sync(0xffffffffu, st.a.y, off);
+      a2.z = __shfl_xor_sync(0xffffffffu, st.a.z, off);
+      a2.w = __shfl_xor_sync(0xffffffffu, st.a.w, off);
+      merge_combine(st, m2, w2, a2);
+    }
+    if (lane < Q) {
+      const int w = threadIdx.x >> 5;
+      s_m[w][lane] = st.m;
+      s_w[w][lane] = st.w;
+      s_acc[w][lane] = st.a;
+    }
+  } else {
+    s_m[p][c] = st.m;
+    s_w[p][c] = st.w;
+    s_acc[p][c] = st.a;
   }
   __syncthreads();
-  if (threadIdx.x < kCols) {
-    const int cq = threadIdx.x >> 2;
+  for (int col = threadIdx.x; col < kCols; col += kMergeThreads) {
+    const int cq = col >> 2;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w][cq]);
+    for (int w = 0; w < R; ++w) M = fmaxf(M, s_m[w][cq]);
     float tot = 0.f, val = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kMergeWarps; ++w) {
+      for (int w = 0; w < R; ++w) {
         if (s_m[w][cq] == -INFINITY) continue;
         const float f = __expf(s_m[w][cq] - M);
         tot += s_w[w][cq] * f;
-        val += reinterpret_cast<const float*>(&s_acc[w][cq])[threadIdx.x & 3] * f;
+        val += reinterpret_cast<const float*>(&s_acc[w][cq])[col & 3] * f;
       }
       val /= tot;
     }
-    const int64_t off = out.o_off + col0 + threadIdx.x;
+    const int64_t off = out.o_off + col0 + col;
     if (out.o_fp32)
       reinterpret_cast<float*>(out.o)[off] = val;
     else
       reinterpret_cast<__nv_bfloat16*>(out.o)[off] = __float2bfloat16_rn(val);
-    if (threadIdx.x == 0 && out.lse != nullptr && col0 == 0)
+    if (col == 0 && out.lse != nullptr && col0 == 0)
       *out.lse = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
   }
 }
@@ -154,7 +166,7 @@ struct SplitMergeParams {
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
 template <int P>
-__global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const SplitMergeParams prm) {
+__global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_merge_kernel(const SplitMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
   const int64_t u = blockIdx.x / NG;
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const Sp
   int64_t first = 0;
   int count = 0;
   if (L > 0) {
-    if (!unit_partials(sp, b, g, &first, &count)) return;   // written directly by its CTA
+    if (!unit_partials<kSchedWhole>(sp, b, g, &first, &count)) return;   // written directly by its CTA
     if (first < 0 || first + count > prm.n_slots) {
       if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
       return;
@@ -201,6 +213,141 @@ __global__ void __launch_bounds__(kMergeThreads) mla_split_merge_kernel(const Sp
   merge_partials_block<P>(count, o_of, lse_of, out, col0);
 }
 
+// ---------------------------------------------------------------- shared-prefix cascade
+
+struct SharedPrefixParams {
+  const int32_t* kv_indptr;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indices;
+  int64_t kv_indices_len;
+  int B;
+  int* shared;     // holds a large value on entry; receives P
+};
+
+// P = the number of leading positions whose cache row ids are the same for every request
+// (compared with request 0), capped so that every query of every request sees all of them
+// (query t of a request with T queries and L positions sees positions <= L - T + t).
+// Each warp compares 32 positions of one request at a time, over a contiguous range of
+// (request, 32-position chunk) pairs, and stops on a request at its first difference.
+__global__ void __launch_bounds__(256) mla_shared_prefix_kernel(const SharedPrefixParams prm) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t b = gtid; b < prm.B; b += nthreads) {
+    const int L = prm.kv_indptr[b + 1] - prm.kv_indptr[b];
+    const int T = prm.qo_indptr[b + 1] - prm.qo_indptr[b];
+    const int lim = L - T + 1;
+    atomicMin(prm.shared, lim > 0 ? lim : 0);
+  }
+  if (prm.B < 2) return;
+  const int64_t base0 = prm.kv_indptr[0];
+  const int L0 = prm.kv_indptr[1] - prm.kv_indptr[0];
+  if (L0 <= 0) return;
+  const int64_t nch = (L0 + 31) / 32;
+  const int64_t total = static_cast<int64_t>(prm.B - 1) * nch;
+  const int64_t warp = gtid >> 5;
+  const int64_t nwarps = nthreads >> 5;
+  const int64_t c0 = total * warp / nwarps;
+  const int64_t c1 = total * (warp + 1) / nwarps;
+  int64_t done_b = -1;   // request already found to differ
+  for (int64_t c = c0; c < c1; ++c) {
+    const int64_t b = 1 + c / nch;
+    if (b == done_b) continue;
+    const int j = static_cast<int>((c % nch) * 32) + lane;
+    const int64_t bb = prm.kv_indptr[b];
+    const int Lb = prm.kv_indptr[b + 1] - static_cast<int>(bb);
+    bool diff = false;
+    if (j < L0 && j < Lb) {
+      const int64_t i0 = base0 + j, i1 = bb + j;
+      diff = (i0 < 0 || i1 < 0 || i0 >= prm.kv_indices_len || i1 >= prm.kv_indices_len) ||
+             prm.kv_indices[i0] != prm.kv_indices[i1];
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, diff);
+    if (m != 0) {
+      if (lane == 0) atomicMin(prm.shared, j + __ffs(m) - 1);
+      done_b = b;
+    }
+  }
+}
+
+struct CascadeMergeParams {
+  SchedParams ss;          // suffix pass (rows per group = ss.NG)
+  SchedParams sp;          // prefix pass (one group of sp.NG rows per virtual request)
+  const float* s_o;        // (slots, ss.NG, 512)
+  const float* s_lse;
+  const float* p_o;        // (slots, sp.NG, 512)
+  const float* p_lse;
+  int64_t s_slots, p_slots;
+  void* o;
+  int o_fp32;
+  int64_t o_stride_tok, o_stride_head;
+  float* lse_out;
+  int64_t n_q_rows;
+  int* err;
+};
+
+// grid = (B * groups * NG, P / 2), block = 256.  Output row n of unit (b, g) of the suffix
+// schedule merges the prefix partials of its group (row (qo_b - qo_group) H + g NG + n of
+// that group's rows) with the partials of its own suffix.  When no prefix is shared the
+// suffix pass ran as a plain decode: units it wrote directly are skipped.
+template <int P>
+__global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
+  const SchedParams& ss = prm.ss;
+  const int NGs = ss.NG;
+  const int64_t u = blockIdx.x / NGs;
+  const int n = static_cast<int>(blockIdx.x - u * NGs);
+  const int b = static_cast<int>(u / ss.groups);
+  const int g = static_cast<int>(u - static_cast<int64_t>(b) * ss.groups);
+  const int col0 = blockIdx.y * (4 * kMergeThreads / P);
+  const int qo0 = ss.qo_indptr[b];
+  const int T = ss.qo_indptr[b + 1] - qo0;
+  const int rr = g * NGs + n;                   // row within the request (token-major)
+  if (rr >= T * ss.H || n >= NGs) return;
+  const int64_t r = static_cast<int64_t>(qo0) * ss.H + rr;
+  if (r < 0 || r >= prm.n_q_rows) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeRow);
+    return;
+  }
+  const int64_t shared = sched_shared<kSchedSuffix>(ss);
+  int64_t sf = 0, pf = 0;
+  int sc = 0, pc = 0;
+  const bool has_s = unit_partials<kSchedSuffix>(ss, b, g, &sf, &sc);
+  const int L = ss.kv_indptr[b + 1] - ss.kv_indptr[b];
+  if (!has_s) {
+    sc = 0;
+    if (shared == 0 && L > 0) return;           // written directly by the decode kernel
+  }
+  const int v = b / prm.sp.gsize;
+  const int np = (qo0 - ss.qo_indptr[v * prm.sp.gsize]) * ss.H + rr;
+  if (shared > 0 && unit_partials<kSchedPrefix>(prm.sp, v, 0, &pf, &pc)) {
+    if (np >= prm.sp.NG || pf < 0 || pf + pc > prm.p_slots) {
+      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
+      return;
+    }
+  } else {
+    pc = 0;
+  }
+  if (sc > 0 && (sf < 0 || sf + sc > prm.s_slots)) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
+    return;
+  }
+  grid_dependency_wait();   // partials come from the decode kernels
+  MergeOut out;
+  out.o = prm.o;
+  out.o_fp32 = prm.o_fp32;
+  out.o_off = (r / ss.H) * prm.o_stride_tok + (r % ss.H) * prm.o_stride_head;
+  out.lse = prm.lse_out ? prm.lse_out + r : nullptr;
+  const int pNG = prm.sp.NG;
+  auto o_of = [&](int k) -> const float* {
+    return k < pc ? prm.p_o + ((pf + k) * pNG + np) * kDV
+                  : prm.s_o + ((sf + (k - pc)) * NGs + n) * kDV;
+  };
+  auto lse_of = [&](int k) -> float {
+    return k < pc ? prm.p_lse[(pf + k) * pNG + np] : prm.s_lse[(sf + (k - pc)) * NGs + n];
+  };
+  merge_partials_block<P>(pc + sc, o_of, lse_of, out, col0);
+}
+
 struct CsrMergeParams {
   const float* o_parts;     // (P, H, 512), last dim contiguous
   int64_t op_stride_p, op_stride_h;
@@ -219,7 +366,7 @@ struct CsrMergeParams {
 
 // grid = (n_out * H, P / 2), block = 256.  Public merge with an explicit reduce map.
 template <int P>
-__global__ void __launch_bounds__(kMergeThreads) mla_csr_merge_kernel(const CsrMergeParams prm) {
+__global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_csr_merge_kernel(const CsrMergeParams prm) {
   const int64_t rr = blockIdx.x / prm.H;
   const int h = static_cast<int>(blockIdx.x - rr * prm.H);
   const int col0 = blockIdx.y * (4 * kMergeThreads / P);

@@ -50,27 +50,102 @@ PMLA_HD inline int groups_for(int rows_per_request, int ng) {
   return (rows_per_request + ng - 1) / ng;
 }
 
+// What a schedule covers.  kSchedWhole: every request's positions, as described above.
+// The two other modes split a batch whose requests share their first P cache positions
+// (the prefix-cache pattern of the captured concurrency-16/24 workloads:
+// "[Kimi-K3 MLA TP8] MLA performance" §1 "Environment" and §5.4):
+//  * kSchedPrefix: "virtual requests" v, each a group of gsize consecutive requests, attend
+//    positions [0, P) together.  Their query rows are consecutive in q (request-major), so
+//    a group is one MMA N-tile and each shared cache row is read once per group instead of
+//    once per request.  No causal masking: every query of the group sees the whole prefix.
+//  * kSchedSuffix: each request attends its own positions [P, L_b).
+// Both always write partials; the cascade merge combines the two per output row.  P is a
+// device value (found by a kernel from kv_indices, see mla_merge_kernel.cuh); values
+// below kMinShared count as 0.
+enum : int { kSchedWhole = 0, kSchedPrefix = 1, kSchedSuffix = 2 };
+constexpr int kMinShared = 1024;
+// The schedule functions take the mode as a template argument: a compile-time mode gives
+// the decode kernel only its own code path (the plain decode carries none of the cascade's
+// arithmetic); kSchedAny reads it from SchedParams::mode (merge kernels, host tests).
+constexpr int kSchedAny = -1;
+
 struct SchedParams {
   const int32_t* kv_indptr;
   const int32_t* qo_indptr;
   int B;
   int H;
   int NG;
-  int groups;      // row groups per request
+  int groups;      // row groups per (virtual) request
   int splits;      // <= 0 auto, else fixed pieces per unit
   int grid;        // CTAs launched
+  int mode;        // kSchedWhole / kSchedPrefix / kSchedSuffix
+  int gsize;       // kSchedPrefix: requests per virtual request
+  const int32_t* shared;   // kSchedPrefix / kSchedSuffix: the shared prefix length P
 };
 
 struct Piece {
-  int b, g;        // request, row group
-  int j0, j1;      // positions [j0, j1) of the request
-  int L, T;        // request kv_len and q_len
+  int b, g;        // (virtual) request, row group
+  int j0, j1;      // positions [j0, j1) of the (virtual) request
+  int L, T;        // its kv_len and query tokens
+  int cfrom;       // causal masking applies to positions > cfrom + (token index)
   int rows;        // real query rows in this group (<= NG)
   int64_t slot;    // partial slot (ignored when direct)
   bool direct;     // this piece is the whole unit: write o / lse directly
-  int64_t kv0;     // kv_indptr[b]: position j of the request is kv_indices[kv0 + j]
-  int qo0;         // qo_indptr[b]: first query token of the request
+  int64_t kv0;     // position j of the piece's request is kv_indices[kv0 + j]
+  int qo0;         // first query token of the (virtual) request
 };
+
+template <int MODE>
+PMLA_HD inline int sched_mode(const SchedParams& sp) {
+  return MODE == kSchedAny ? sp.mode : MODE;
+}
+
+// The shared prefix length a schedule uses (0 in whole mode or below kMinShared).
+template <int MODE = kSchedAny>
+PMLA_HD inline int64_t sched_shared(const SchedParams& sp) {
+  if (sched_mode<MODE>(sp) == kSchedWhole || sp.shared == nullptr) return 0;
+  const int64_t P = *sp.shared;
+  return P >= kMinShared ? P : 0;
+}
+
+// Number of (virtual) requests of a schedule.
+template <int MODE = kSchedAny>
+PMLA_HD inline int sched_requests(const SchedParams& sp) {
+  return sched_mode<MODE>(sp) == kSchedPrefix ? (sp.B + sp.gsize - 1) / sp.gsize : sp.B;
+}
+
+// Positions of all (virtual) requests before v, and of v itself.
+template <int MODE = kSchedAny>
+PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
+  const int mode = sched_mode<MODE>(sp);
+  if (mode == kSchedPrefix) return static_cast<int64_t>(v) * P;
+  return static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0] -
+         (mode == kSchedSuffix ? static_cast<int64_t>(v) * P : 0);
+}
+template <int MODE = kSchedAny>
+PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
+  const int mode = sched_mode<MODE>(sp);
+  if (mode == kSchedPrefix) return static_cast<int>(P);
+  return sp.kv_indptr[v + 1] - sp.kv_indptr[v] - (mode == kSchedSuffix ? static_cast<int>(P) : 0);
+}
+// First index-array entry and query tokens [qo0, qo1) of (virtual) request v.
+template <int MODE = kSchedAny>
+PMLA_HD inline int64_t sched_kv0(const SchedParams& sp, int64_t P, int v) {
+  const int mode = sched_mode<MODE>(sp);
+  if (mode == kSchedPrefix) return sp.kv_indptr[v * sp.gsize];
+  return static_cast<int64_t>(sp.kv_indptr[v]) + (mode == kSchedSuffix ? P : 0);
+}
+template <int MODE = kSchedAny>
+PMLA_HD inline void sched_tokens(const SchedParams& sp, int v, int* qo0, int* qo1) {
+  if (sched_mode<MODE>(sp) == kSchedPrefix) {
+    const int last = (v + 1) * sp.gsize < sp.B ? (v + 1) * sp.gsize : sp.B;
+    *qo0 = sp.qo_indptr[v * sp.gsize];
+    *qo1 = sp.qo_indptr[last];
+  } else {
+    *qo0 = sp.qo_indptr[v];
+    *qo1 = sp.qo_indptr[v + 1];
+  }
+}
 
 // Effective CTA count of the auto policy for a line of W positions.
 PMLA_HD inline int auto_ctas(int64_t W, int grid) {
@@ -85,13 +160,17 @@ PMLA_HD inline int auto_cta_of(int64_t x, int64_t W, int Gp) {
   return static_cast<int>(((x + 1) * Gp - 1) / W);
 }
 
-// Largest b in [0, B) with groups * (kv_indptr[b] - kv_indptr[0]) <= x.
-PMLA_HD inline int find_request(const int32_t* kvp, int B, int groups, int64_t x) {
-  const int32_t kv0 = kvp[0];
-  int lo = 0, hi = B - 1;
+// Largest v in [0, VB) with groups * cum(v) <= x.
+template <int MODE = kSchedAny>
+PMLA_HD inline int find_request(const SchedParams& sp, int64_t P, int VB, int64_t x) {
+  if (sched_mode<MODE>(sp) == kSchedPrefix) {
+    const int64_t v = x / (static_cast<int64_t>(sp.groups) * P);
+    return static_cast<int>(v < VB ? v : VB - 1);
+  }
+  int lo = 0, hi = VB - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(groups) * (kvp[mid] - kv0) <= x)
+    if (static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, mid) <= x)
       lo = mid;
     else
       hi = mid - 1;
@@ -108,9 +187,12 @@ PMLA_HD inline void piece_bounds(int L, int splits, int k, int* j0, int* j1) {
 // Iterator over one CTA's pieces.  Every role of a CTA constructs it with the same
 // arguments and so sees the same sequence.  Pieces without work (no real rows, no
 // positions) are skipped.  On inconsistent indptr data it stops and sets *bad.
-struct PieceIter {
+template <int MODE = kSchedAny>
+struct PieceIterT {
   SchedParams sp;
   int cta;
+  int VB;
+  int64_t P;
   int64_t W;
   int Gp;
   int64_t x, x1;       // auto policy cursor
@@ -121,23 +203,19 @@ struct PieceIter {
   // Every member is assigned on every path: the iterator is only ever constructed with
   // init(), never copied.
   PMLA_HD void init(const SchedParams& s, int cta_id) {
-    sp.kv_indptr = s.kv_indptr;
-    sp.qo_indptr = s.qo_indptr;
-    sp.B = s.B;
-    sp.H = s.H;
-    sp.NG = s.NG;
-    sp.groups = s.groups;
-    sp.splits = s.splits;
-    sp.grid = s.grid;
+    sp = s;
     cta = cta_id;
+    P = sched_shared<MODE>(s);
+    VB = sched_requests<MODE>(s);
     W = 0;
     Gp = 0;
     x = x1 = 0;
     p = p_end = 0;
     have_held = false;
-    held = Piece{0, 0, 0, 0, 0, 0, 0, 0, false, 0, 0};
+    held = Piece{0, 0, 0, 0, 0, 0, 0, 0, 0, false, 0, 0};
+    if (sched_mode<MODE>(s) == kSchedPrefix && P == 0) return;   // nothing shared: no work
     if (sp.splits <= 0) {
-      W = static_cast<int64_t>(sp.groups) * (sp.kv_indptr[sp.B] - sp.kv_indptr[0]);
+      W = static_cast<int64_t>(sp.groups) * (VB > 0 ? sched_cum<MODE>(sp, P, VB) : 0);
       Gp = auto_ctas(W, sp.grid);
       if (W <= 0 || cta >= Gp) {
         x = x1 = 0;
@@ -147,7 +225,7 @@ struct PieceIter {
       }
     } else {
       p = cta;
-      p_end = static_cast<int64_t>(sp.B) * sp.groups * sp.splits;
+      p_end = static_cast<int64_t>(VB) * sp.groups * sp.splits;
     }
   }
 
@@ -167,9 +245,9 @@ struct PieceIter {
     while (true) {
       if (sp.splits <= 0) {
         if (x >= x1) return false;
-        const int b = find_request(sp.kv_indptr, sp.B, sp.groups, x);
-        const int64_t base = static_cast<int64_t>(sp.groups) * (sp.kv_indptr[b] - sp.kv_indptr[0]);
-        const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+        const int v = find_request<MODE>(sp, P, VB, x);
+        const int64_t base = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, v);
+        const int L = sched_len<MODE>(sp, P, v);
         const int64_t off = x - base;
         if (L <= 0 || off < 0 || off >= static_cast<int64_t>(L) * sp.groups) {
           *bad = 1;
@@ -181,26 +259,26 @@ struct PieceIter {
         const int64_t room = x1 - x;
         const int j1 = (L - j0 <= room) ? L : j0 + static_cast<int>(room);
         x += j1 - j0;
-        pc.b = b;
+        pc.b = v;
         pc.g = g;
         pc.j0 = j0;
         pc.j1 = j1;
         pc.L = L;
-        pc.slot = static_cast<int64_t>(cta) + static_cast<int64_t>(b) * sp.groups + g;
+        pc.slot = static_cast<int64_t>(cta) + static_cast<int64_t>(v) * sp.groups + g;
         pc.direct = (j0 == 0 && j1 == L);
       } else {
         if (p >= p_end) return false;
         const int64_t u = p / sp.splits;
         const int k = static_cast<int>(p - u * sp.splits);
-        const int b = static_cast<int>(u / sp.groups);
-        const int g = static_cast<int>(u - static_cast<int64_t>(b) * sp.groups);
-        const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+        const int v = static_cast<int>(u / sp.groups);
+        const int g = static_cast<int>(u - static_cast<int64_t>(v) * sp.groups);
+        const int L = sched_len<MODE>(sp, P, v);
         if (L < 0) {
           *bad = 1;
           p = p_end;
           return false;
         }
-        pc.b = b;
+        pc.b = v;
         pc.g = g;
         piece_bounds(L, sp.splits, k, &pc.j0, &pc.j1);
         pc.L = L;
@@ -208,9 +286,13 @@ struct PieceIter {
         pc.direct = (sp.splits == 1);
         p += sp.grid;
       }
-      pc.kv0 = sp.kv_indptr[pc.b];
-      pc.qo0 = sp.qo_indptr[pc.b];
-      pc.T = sp.qo_indptr[pc.b + 1] - pc.qo0;
+      // a cascade half never holds the whole answer of a request (P > 0)
+      if (sched_mode<MODE>(sp) != kSchedWhole && P > 0) pc.direct = false;
+      pc.kv0 = sched_kv0<MODE>(sp, P, pc.b);
+      int qo1 = 0;
+      sched_tokens<MODE>(sp, pc.b, &pc.qo0, &qo1);
+      pc.T = qo1 - pc.qo0;
+      pc.cfrom = sched_mode<MODE>(sp) == kSchedPrefix ? pc.L : pc.L - pc.T;
       const int rows_req = pc.T * sp.H;
       int rows = rows_req - pc.g * sp.NG;
       if (rows > sp.NG) rows = sp.NG;
@@ -219,36 +301,46 @@ struct PieceIter {
     }
   }
 };
+// Runtime-mode iterator (host simulation).
+using PieceIter = PieceIterT<kSchedAny>;
 
-// Number of partial slots a call needs (host and device agree on this bound).
-PMLA_HD inline int64_t partial_slots(int B, int groups, int splits, int grid) {
-  const int64_t units = static_cast<int64_t>(B) * groups;
+// Number of partial slots a call needs for (virtual) requests VB (host and device agree
+// on this bound).
+PMLA_HD inline int64_t partial_slots(int VB, int groups, int splits, int grid) {
+  const int64_t units = static_cast<int64_t>(VB) * groups;
   if (splits <= 0) return units + grid;
   if (splits == 1) return 0;
   return units * splits;
 }
 
-// Partials of unit (b, g) as the decode kernel wrote them: slots first .. first+count-1
+// Partials of unit (v, g) as the decode kernel wrote them: slots first .. first+count-1
 // (fixed policy: some may be empty pieces, see piece_bounds).  Returns false when the
 // unit needs no merge: it ran whole on one CTA (written directly) or has no positions.
-PMLA_HD inline bool unit_partials(const SchedParams& sp, int b, int g, int64_t* first,
+// In the cascade modes (with a shared prefix) every unit's pieces are partials.
+template <int MODE = kSchedAny>
+PMLA_HD inline bool unit_partials(const SchedParams& sp, int v, int g, int64_t* first,
                                   int* count) {
-  const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+  const int64_t P = sched_shared<MODE>(sp);
+  const int mode = sched_mode<MODE>(sp);
+  if (mode == kSchedPrefix && P == 0) return false;
+  const int VB = sched_requests<MODE>(sp);
+  const int L = sched_len<MODE>(sp, P, v);
   if (L <= 0) return false;
-  const int64_t u = static_cast<int64_t>(b) * sp.groups + g;
+  const bool all_partial = mode != kSchedWhole && P > 0;
+  const int64_t u = static_cast<int64_t>(v) * sp.groups + g;
   if (sp.splits <= 0) {
-    const int64_t W = static_cast<int64_t>(sp.groups) * (sp.kv_indptr[sp.B] - sp.kv_indptr[0]);
+    const int64_t W = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, VB);
     const int Gp = auto_ctas(W, sp.grid);
-    const int64_t xs = static_cast<int64_t>(sp.groups) * (sp.kv_indptr[b] - sp.kv_indptr[0]) +
+    const int64_t xs = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, v) +
                        static_cast<int64_t>(g) * L;
     const int i0 = auto_cta_of(xs, W, Gp);
     const int i1 = auto_cta_of(xs + L - 1, W, Gp);
-    if (i0 == i1) return false;
+    if (i0 == i1 && !all_partial) return false;
     *first = static_cast<int64_t>(i0) + u;   // CTA i writes unit u's piece to slot i + u
     *count = i1 - i0 + 1;
     return true;
   }
-  if (sp.splits == 1) return false;
+  if (sp.splits == 1 && !all_partial) return false;
   *first = u * sp.splits;
   *count = sp.splits;
   return true;

@@ -39,6 +39,37 @@ int sched_unit_partials(const int32_t* kv_indptr, const int32_t* qo_indptr, int 
   return pmla::unit_partials(sp, b, g, first, count) ? 1 : 0;
 }
 
+// Same for a cascade half: mode 1 = prefix (virtual requests of gsize requests), 2 =
+// suffix; shared = the shared prefix length the device would have found.
+int64_t sched_pieces_mode(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H, int NG,
+                          int groups, int splits, int grid, int mode, int gsize, int shared,
+                          int64_t* out, int64_t max_out) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, &shared};
+  int64_t n = 0;
+  for (int cta = 0; cta < grid; ++cta) {
+    pmla::PieceIter it;
+    it.init(sp, cta);
+    pmla::Piece pc;
+    int bad = 0;
+    while (it.next(pc, &bad)) {
+      if (n >= max_out) return -1;
+      int64_t* o = out + 10 * n;
+      o[0] = cta; o[1] = pc.b; o[2] = pc.g; o[3] = pc.j0; o[4] = pc.j1; o[5] = pc.rows;
+      o[6] = pc.slot; o[7] = pc.direct ? 1 : 0; o[8] = pc.kv0; o[9] = pc.cfrom;
+      ++n;
+    }
+    if (bad) return -2;
+  }
+  return n;
+}
+
+int sched_unit_partials_mode(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H,
+                             int NG, int groups, int splits, int grid, int mode, int gsize,
+                             int shared, int v, int g, int64_t* first, int* count) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, &shared};
+  return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
+}
+
 int64_t sched_partial_slots(int B, int groups, int splits, int grid) {
   return pmla::partial_slots(B, groups, splits, grid);
 }

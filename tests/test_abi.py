@@ -58,11 +58,24 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_plan(lib):
-    # auto policy: (B*groups + SMs) partial slots of NG rows x (512 + 1) floats + header
+    # auto policy: (B*groups + SMs) partial slots of NG rows x (512 + 1) floats + header,
+    # and for decode batches (<= 24 rows per request) the shared-prefix cascade's prefix
+    # pass: (ceil(B / groups of 4) + SMs) slots of 48 rows
     sz = lib.mla_get_workspace_size(16, 12, 1, 0, 152)
     ng, slots = 16, 16 + 152
-    assert sz >= 256 + slots * ng * 513 * 4
-    assert sz < 256 + 256 + slots * ng * 513 * 4 + 256
+    pslots = 4 + 152
+    plain = 256 + slots * ng * 513 * 4
+    prefix = pslots * 48 * 513 * 4
+    assert plain + prefix <= sz < plain + prefix + 4 * 256
+    # fewer requests than one group of 4: no cascade
+    sz3 = lib.mla_get_workspace_size(3, 12, 1, 0, 152)
+    assert sz3 < 256 + (3 + 152) * 16 * 513 * 4 + 3 * 256
+    # one request: no cascade
+    sz1 = lib.mla_get_workspace_size(1, 12, 1, 0, 152)
+    assert 256 + 153 * 16 * 513 * 4 <= sz1 < 256 + 153 * 16 * 513 * 4 + 3 * 256
+    # q_len 4 x 12 heads = 48 rows: no room for two requests per group, no cascade
+    sz4 = lib.mla_get_workspace_size(64, 12, 4, 0, 152)
+    assert sz4 < 256 + (64 + 152) * 48 * 513 * 4 + 3 * 256
     # 96 heads -> two groups of 48 rows
     sz96 = lib.mla_get_workspace_size(1, 96, 1, 0, 152)
     assert sz96 >= (2 + 152) * 48 * 513 * 4
