@@ -256,7 +256,7 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   sp.kv_indices_len = prm.kv_indices_len;
   sp.B = prm.sp.B;
   sp.shared = shared;
-  mla_shared_prefix_kernel<<<plan.grid * 2, 256, 0, stream>>>(sp);
+  mla_shared_prefix_kernel<<<plan.grid * 4, 256, 0, stream>>>(sp);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
   CUtensorMap p_lat, p_rope;

@@ -227,8 +227,12 @@ struct SharedPrefixParams {
 // P = the number of leading positions whose cache row ids are the same for every request
 // (compared with request 0), capped so that every query of every request sees all of them
 // (query t of a request with T queries and L positions sees positions <= L - T + t).
-// Each warp compares 32 positions of one request at a time, over a contiguous range of
-// (request, 32-position chunk) pairs, and stops on a request at its first difference.
+// Work item = 256 positions of one request: each lane loads 8 of them (32 apart, so every
+// load instruction of the warp is coalesced) with all 16 loads in flight at once; the
+// warp then reports the first difference.  Items past the current P are skipped.
+constexpr int kPrefixCmpPerLane = 8;
+constexpr int kPrefixItem = 32 * kPrefixCmpPerLane;
+
 __global__ void __launch_bounds__(256) mla_shared_prefix_kernel(const SharedPrefixParams prm) {
   const int lane = threadIdx.x & 31;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -243,30 +247,34 @@ __global__ void __launch_bounds__(256) mla_shared_prefix_kernel(const SharedPref
   const int64_t base0 = prm.kv_indptr[0];
   const int L0 = prm.kv_indptr[1] - prm.kv_indptr[0];
   if (L0 <= 0) return;
-  const int64_t nch = (L0 + 31) / 32;
-  const int64_t total = static_cast<int64_t>(prm.B - 1) * nch;
-  const int64_t warp = gtid >> 5;
+  const int64_t nitems = (L0 + kPrefixItem - 1) / kPrefixItem;
+  const int64_t total = static_cast<int64_t>(prm.B - 1) * nitems;
   const int64_t nwarps = nthreads >> 5;
-  const int64_t c0 = total * warp / nwarps;
-  const int64_t c1 = total * (warp + 1) / nwarps;
-  int64_t done_b = -1;   // request already found to differ
-  for (int64_t c = c0; c < c1; ++c) {
-    const int64_t b = 1 + c / nch;
-    if (b == done_b) continue;
-    const int j = static_cast<int>((c % nch) * 32) + lane;
+  for (int64_t it = gtid >> 5; it < total; it += nwarps) {
+    const int64_t b = 1 + it / nitems;
+    const int j0 = static_cast<int>((it % nitems) * kPrefixItem);
+    const int cur = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(prm.shared), 0);
+    if (j0 >= cur) continue;   // a difference (or the cap) lies before this item
     const int64_t bb = prm.kv_indptr[b];
     const int Lb = prm.kv_indptr[b + 1] - static_cast<int>(bb);
-    bool diff = false;
-    if (j < L0 && j < Lb) {
+    const int n = L0 < Lb ? L0 : Lb;
+    int a[kPrefixCmpPerLane], c[kPrefixCmpPerLane];
+#pragma unroll
+    for (int u = 0; u < kPrefixCmpPerLane; ++u) {
+      const int j = j0 + 32 * u + lane;
       const int64_t i0 = base0 + j, i1 = bb + j;
-      diff = (i0 < 0 || i1 < 0 || i0 >= prm.kv_indices_len || i1 >= prm.kv_indices_len) ||
-             prm.kv_indices[i0] != prm.kv_indices[i1];
+      const bool ok = j < n && i0 >= 0 && i1 >= 0 && i0 < prm.kv_indices_len &&
+                      i1 < prm.kv_indices_len;
+      a[u] = ok ? __ldg(prm.kv_indices + i0) : 0;
+      c[u] = ok ? __ldg(prm.kv_indices + i1) : (j < n ? 1 : 0);   // out of range: differs
     }
-    const unsigned m = __ballot_sync(0xffffffffu, diff);
-    if (m != 0) {
-      if (lane == 0) atomicMin(prm.shared, j + __ffs(m) - 1);
-      done_b = b;
-    }
+    int first = 0x7FFFFFFF;
+#pragma unroll
+    for (int u = kPrefixCmpPerLane - 1; u >= 0; --u)
+      if (a[u] != c[u]) first = j0 + 32 * u + lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+    if (lane == 0 && first != 0x7FFFFFFF) atomicMin(prm.shared, first);
   }
 }
 
