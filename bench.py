@@ -252,6 +252,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--num-kv-splits", type=int, default=0)
+    ap.add_argument("--entry", default="auto", choices=["auto", "plain", "shared_prefix"],
+                    help="auto: mla_decode_shared_prefix for workloads whose requests share a "
+                         "prefix by construction (c16, c24), else mla_decode")
     ap.add_argument("--q-scale", type=float, default=mla_inputs.DEFAULT_Q_SCALE)
     ap.add_argument("--kv-scale", type=float, default=mla_inputs.DEFAULT_KV_SCALE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -280,15 +283,26 @@ def main():
     n_tok, H = case.q.shape[0], case.q.shape[1]
     o = torch.empty((n_tok, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
-    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev)
+    shared = int(case.meta.get("shared_prefix", 0))
+    entry = args.entry
+    if entry == "auto":
+        entry = "shared_prefix" if shared > 0 and args.num_kv_splits <= 0 else "plain"
+    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev,
+                           shared_prefix=(entry == "shared_prefix"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def call(q=case.q, qo=case.qo_indptr, kvp=case.kv_indptr, idx=case.kv_indices,
-             last=case.kv_last_page_lens, out=o, l=lse):
-        pm.mla_decode(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q, case.sm_scale,
-                      case.q_scale, case.kv_scale, num_kv_splits=args.num_kv_splits,
-                      lse_out=l, workspace=ws)   # on the current stream (capturable)
+             last=case.kv_last_page_lens, out=o, l=lse, which=None):
+        # on the current stream (capturable)
+        if (which or entry) == "shared_prefix":
+            pm.mla_decode_shared_prefix(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q,
+                                        case.sm_scale, case.q_scale, case.kv_scale, shared,
+                                        lse_out=l, workspace=ws)
+        else:
+            pm.mla_decode(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q, case.sm_scale,
+                          case.q_scale, case.kv_scale, num_kv_splits=args.num_kv_splits,
+                          lse_out=l, workspace=ws)
 
     for i in range(args.warmup):
         if not args.no_l2_flush:
@@ -359,6 +373,38 @@ def main():
     mean_ms = sum(step_ms) / len(step_ms)
     mean_ms = max_over_ranks(mean_ms, dist, dev)
 
+    # Workloads with a shared prefix: the plain mla_decode on the same inputs, timed the same
+    # way, reported beside the shared-prefix call.
+    plain = None
+    if entry == "shared_prefix":
+        g2 = None
+        if not args.eager:
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                call(which="plain")
+        torch.cuda.synchronize(dev)
+        for i in range(max(args.warmup, 3)):
+            if not args.no_l2_flush:
+                flush.fill_(i & 0xFF)
+            g2.replay() if g2 is not None else call(which="plain")
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            if not args.no_l2_flush:
+                flush.fill_((i + 11) & 0xFF)
+            ev[i][0].record(stream)
+            g2.replay() if g2 is not None else call(which="plain")
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        p_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, dist, dev)
+        plain = {"entry": "mla_decode", "us_per_call": p_ms * 1e3,
+                 "value": whole_job_rate(world, mla_inputs.gathered_kv_bytes(case.kv_lens), p_ms),
+                 "unit": UNIT}
+        st = pm.mla_check_error(ws)
+        if st != 0:
+            raise RuntimeError(f"device error in the plain timing: {pm.mla_status_string(st)}")
+
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
     algo = mla_inputs.algorithmic_bytes(case)
     value = whole_job_rate(world, gathered, mean_ms)
@@ -419,16 +465,23 @@ def main():
                        "q_len": case.max_seqlen_q, "positions": case.total_kv,
                        "gathered_kv_bytes": gathered, "algorithmic_bytes": algo,
                        "num_kv_splits": args.num_kv_splits,
+                       "entry": ("mla_decode_shared_prefix (shared prefix of %d positions, "
+                                 "known to the caller)" % shared) if entry == "shared_prefix"
+                                else "mla_decode",
                        "l2": "flushed before every step (512 MB write, outside the timed region)"
                              if not args.no_l2_flush else "not flushed",
                        "parallelism": f"{world} independent replicas (one batch per GPU)"},
-            "roofline": {"bound": "hbm", "kernel": "mla_decode call (decode + merge kernels)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("mla_decode_shared_prefix call (prefix + suffix decode, merge)"
+                                    if entry == "shared_prefix" else
+                                    "mla_decode call (decode + merge kernels)"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": recorded_traffic(args.config)},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (4 if entry == "shared_prefix" else 2) * args.steps,
+            "plain_call": plain,
             "clocks": dict(clocks.summary(),
                            window=("the timed region" if soak == 0 else
                                    f"the timed region and {soak} identical untimed steps "

@@ -131,6 +131,44 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
                void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * Workspace for mla_decode_shared_prefix with these sizes (automatic split-KV); >= the
+ * plain decode's.  Arguments as for mla_get_workspace_size.
+ */
+int mla_get_shared_prefix_workspace_size(int32_t batch_size, int32_t num_heads,
+                                         int32_t max_seqlen_q, int32_t num_sms,
+                                         size_t* bytes_out);
+
+/*
+ * mla_decode for a batch whose requests share their first cache positions: the prefix-
+ * cache pattern of the captured concurrency-16/24 decode steps ("[Kimi-K3 MLA TP8] MLA
+ * performance" §1 "Environment", §5.4 "Possible cross-request KV reuse").  Same
+ * arguments and results as mla_decode with num_kv_splits = 0, except:
+ *   shared_prefix_len  P >= 0: for every request b, kv_indices[kv_indptr[b] + j] is the
+ *                      same row for all j < P, and every query sees all P positions
+ *                      (P <= kv_len_b - q_len_b + 1).  The caller knows this from its
+ *                      prefix cache; it is not searched for.  A request breaking the
+ *                      second condition is flagged (MLA_ERR_BAD_INPUT through
+ *                      mla_check_error); breaking the first gives wrong results.
+ *   workspace          at least mla_get_shared_prefix_workspace_size(...) bytes for the
+ *                      shared-prefix path; with less (but at least
+ *                      mla_get_workspace_size(B, H, max_seqlen_q, 0, ...)) it runs the
+ *                      plain decode.
+ * The shared positions are attended in groups of requests (48 query rows per tile, i.e.
+ * 4 requests at 12 heads and q_len 1), so each shared row is read once per group instead
+ * of once per request; each request's own positions run separately and the two halves
+ * are merged by their log-sum-exp.  Batches with fewer requests than one group, more
+ * than 24 query rows per request, or P < 1024 run the plain decode.
+ */
+int mla_decode_shared_prefix(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
+                             const mla_tensor_t* o, const mla_tensor_t* qo_indptr,
+                             const mla_tensor_t* kv_indptr, const mla_tensor_t* kv_indices,
+                             const mla_tensor_t* kv_last_page_lens, int32_t max_seqlen_q,
+                             float sm_scale, const mla_tensor_t* q_scale,
+                             const mla_tensor_t* kv_scale, int32_t shared_prefix_len,
+                             const mla_tensor_t* lse_out, void* workspace,
+                             size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * Softmax-weighted merge of partial results ("Scaling Kimi K3 on AMD Instinct MI355X",
  * §1: each partial answer carries its normalisation, so shards merge exactly):
  *   for output row r < n_out and head h, over the partial rows
@@ -166,8 +204,10 @@ int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
                  void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
- * Synchronises `stream`, returns the first device-side error recorded in the
- * workspace's error words since the last check (MLA_OK if none) and clears them.
+ * Synchronises `stream`, returns the device-side errors recorded in the workspace's error
+ * words since the last check (MLA_OK if none) and clears them: MLA_ERR_TIMEOUT before
+ * MLA_ERR_BAD_INDEX (an index or indptr out of range), MLA_ERR_UNSUPPORTED (shared memory
+ * misaligned) and MLA_ERR_BAD_INPUT (a shared prefix longer than a request's queries see).
  */
 int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream);
 

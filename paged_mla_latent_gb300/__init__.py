@@ -22,8 +22,9 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MlaError", "mla_decode", "mla_decode_noalloc", "mla_merge_partials", "mla_validate", "mla_check_error",
-    "mla_get_workspace_size", "mla_status_string", "make_workspace", "library_path",
+    "MlaError", "mla_decode", "mla_decode_shared_prefix", "mla_decode_noalloc", "mla_merge_partials",
+    "mla_validate", "mla_check_error", "mla_get_workspace_size", "mla_get_shared_prefix_workspace_size",
+    "mla_status_string", "make_workspace", "library_path",
 ]
 
 MLA_DTYPE_FP8_E4M3FN = 1
@@ -60,6 +61,11 @@ def _load() -> ctypes.CDLL:
     lib.mla_get_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     lib.mla_decode.restype = ctypes.c_int
     lib.mla_decode.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, c_sz, vp]
+    lib.mla_get_shared_prefix_workspace_size.restype = ctypes.c_int
+    lib.mla_get_shared_prefix_workspace_size.argtypes = [c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
+    lib.mla_decode_shared_prefix.restype = ctypes.c_int
+    lib.mla_decode_shared_prefix.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P,
+                                             vp, c_sz, vp]
     lib.mla_decode_noalloc.restype = ctypes.c_int
     lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, vp]
     lib.mla_merge_partials.restype = ctypes.c_int
@@ -137,12 +143,25 @@ def mla_get_workspace_size(batch_size: int, num_heads: int, max_seqlen_q: int = 
     return int(out.value)
 
 
+def mla_get_shared_prefix_workspace_size(batch_size: int, num_heads: int, max_seqlen_q: int = 1,
+                                         num_sms: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.mla_get_shared_prefix_workspace_size(batch_size, num_heads, max_seqlen_q, num_sms,
+                                                     ctypes.byref(out)),
+           "mla_get_shared_prefix_workspace_size")
+    return int(out.value)
+
+
 def make_workspace(batch_size: int, num_heads: int, max_seqlen_q: int = 1,
-                   num_kv_splits: int = 0, device=None) -> torch.Tensor:
-    """A zero-initialised device workspace large enough for such calls."""
+                   num_kv_splits: int = 0, device=None, shared_prefix: bool = False) -> torch.Tensor:
+    """A zero-initialised device workspace large enough for such calls (shared_prefix:
+    for mla_decode_shared_prefix)."""
     device = torch.device(device or "cuda")
     with torch.cuda.device(device):
-        n = mla_get_workspace_size(batch_size, num_heads, max_seqlen_q, num_kv_splits)
+        if shared_prefix:
+            n = mla_get_shared_prefix_workspace_size(batch_size, num_heads, max_seqlen_q)
+        else:
+            n = mla_get_workspace_size(batch_size, num_heads, max_seqlen_q, num_kv_splits)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -163,6 +182,26 @@ def mla_decode(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_l
                          int(num_kv_splits), _ref(dlse), ctypes.c_void_p(workspace.data_ptr()),
                          workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     _check(rc, "mla_decode")
+    return workspace
+
+
+def mla_decode_shared_prefix(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
+                             kv_last_page_lens, max_seqlen_q, sm_scale, q_scale, kv_scale,
+                             shared_prefix_len, lse_out=None, workspace=None, stream=None):
+    """Decode a batch whose requests share their first shared_prefix_len cache positions
+    (see include/paged_mla.h).  Returns the workspace used."""
+    if workspace is None:
+        workspace = make_workspace(len(kv_indptr) - 1, q.shape[1], max_seqlen_q, 0, q.device,
+                                   shared_prefix=True)
+    descs = [_desc(t) for t in (q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
+                                kv_last_page_lens, q_scale, kv_scale, lse_out)]
+    dq, dkv, do, dqo, dkvp, didx, dlast, dqs, dks, dlse = descs
+    rc = _lib.mla_decode_shared_prefix(
+        _ref(dq), _ref(dkv), _ref(do), _ref(dqo), _ref(dkvp), _ref(didx), _ref(dlast),
+        int(max_seqlen_q), float(sm_scale), _ref(dqs), _ref(dks), int(shared_prefix_len),
+        _ref(dlse), ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    _check(rc, "mla_decode_shared_prefix")
     return workspace
 
 

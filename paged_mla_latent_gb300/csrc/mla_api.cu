@@ -181,7 +181,6 @@ struct Plan {
   int64_t pslots;
   size_t plse_off, po_off, cbytes;
 };
-constexpr size_t kSharedOff = 128;   // int32 in the header: the shared prefix length
 constexpr int kPrefixNG = 48;
 
 int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Plan* p) {
@@ -218,47 +217,15 @@ int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Pl
 
 }  // namespace
 
-// Workspace of the plain decode (whole) and of the shared-prefix cascade (cascade >=
-// whole); the cascade runs when the caller's workspace holds it.
-int pmla_workspace_sizes(int B, int H, int max_seqlen_q, int num_kv_splits, int sms,
-                         size_t* whole, size_t* cascade) {
-  if (sms <= 0) {
-    int dev = 0;
-    int rc = current_device(&dev);
-    if (rc) return rc;
-    if ((rc = device_sms(dev, &sms))) return rc;
-  }
-  Plan p;
-  const int rc = make_plan(B, H, max_seqlen_q, num_kv_splits, sms, &p);
-  if (rc) return rc;
-  *whole = p.bytes;
-  *cascade = p.cbytes;
-  return MLA_OK;
-}
-
 namespace {
 
-// Shared-prefix cascade: find the prefix P every request shares (device), run the
-// prefix pass (groups of plan.gsize requests, 48-row tiles) and the suffix pass (each
-// request's own positions) into partials, then merge the two per output row.  With no
-// shared prefix (P below kMinShared) the prefix pass has no work, the suffix pass is the
-// plain decode and the merge touches only the units that were split.
+// Shared-prefix cascade: the prefix pass (groups of plan.gsize requests over the first
+// `shared` positions, 48-row tiles) and the suffix pass (each request's own positions)
+// write partials, and the cascade merge combines the two per output row.
 int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr, int64_t q_rows,
-                   const mla_tensor_t* kv_indices, const CUtensorMap& q_lat,
-                   const CUtensorMap& q_rope, cudaStream_t stream) {
+                   int32_t shared, const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+                   cudaStream_t stream) {
   uint8_t* ws = reinterpret_cast<uint8_t*>(prm.err);
-  int32_t* shared = reinterpret_cast<int32_t*>(ws + kSharedOff);
-  if (cudaMemsetAsync(shared, 0x7F, sizeof(int32_t), stream) != cudaSuccess) return MLA_ERR_CUDA;
-  SharedPrefixParams sp;
-  sp.kv_indptr = prm.sp.kv_indptr;
-  sp.qo_indptr = prm.sp.qo_indptr;
-  sp.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
-  sp.kv_indices_len = prm.kv_indices_len;
-  sp.B = prm.sp.B;
-  sp.shared = shared;
-  mla_shared_prefix_kernel<<<plan.grid * 4, 256, 0, stream>>>(sp);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-
   CUtensorMap p_lat, p_rope;
   int rc;
   if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
@@ -327,48 +294,16 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* mla_status_string(int status) {
-  switch (status) {
-    case MLA_OK: return "MLA_OK";
-    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
-    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
-    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
-    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
-    case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX";
-    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
-    case MLA_ERR_BAD_INPUT: return "MLA_ERR_BAD_INPUT";
-    default: return "MLA_ERR_UNKNOWN";
-  }
-}
-
-int mla_get_workspace_size(int32_t batch_size, int32_t num_heads, int32_t max_seqlen_q,
-                           int32_t num_kv_splits, int32_t num_sms, size_t* bytes_out) {
-  if (!bytes_out) return MLA_ERR_INVALID_ARG;
-  int sms = num_sms;
-  if (sms <= 0) {
-    int dev = 0;
-    int rc = current_device(&dev);
-    if (rc) return rc;
-    rc = device_sms(dev, &sms);
-    if (rc) return rc;
-  }
-  Plan p;
-  int rc = make_plan(batch_size, num_heads, max_seqlen_q, num_kv_splits, sms, &p);
-  if (rc) return rc;
-  *bytes_out = p.cbytes;
-  return MLA_OK;
-}
-
-int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
-               const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
-               const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
-               int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
-               const mla_tensor_t* kv_scale, int32_t num_kv_splits, const mla_tensor_t* lse_out,
-               void* workspace, size_t workspace_bytes, mla_stream_t stream_) {
+// mla_decode and mla_decode_shared_prefix: shared_len = the leading positions every
+// request shares (0: none / unknown).  The cascade runs when the batch qualifies, the
+// prefix is at least kMinShared long and the workspace holds the cascade's partials.
+int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
+                const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
+                const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
+                int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
+                const mla_tensor_t* kv_scale, int32_t num_kv_splits, int32_t shared_len,
+                const mla_tensor_t* lse_out, void* workspace, size_t workspace_bytes,
+                mla_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   CallShape cs;
   int rc = check_inputs(q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens, &cs);
@@ -379,6 +314,7 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY)
     return MLA_ERR_INVALID_ARG;
   if (max_seqlen_q < 1 || max_seqlen_q > kMaxSeqlenQ) return MLA_ERR_INVALID_ARG;
+  if (shared_len < 0) return MLA_ERR_INVALID_ARG;
   if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   if (cs.B == 0 || cs.n_tok == 0) return MLA_OK;   // nothing to attend
 
@@ -405,7 +341,7 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.sp.grid = plan.grid;
   prm.sp.mode = kSchedWhole;
   prm.sp.gsize = 1;
-  prm.sp.shared = nullptr;
+  prm.sp.shared = 0;
   prm.kv = static_cast<const uint8_t*>(kv_buffer->ptr);
   prm.kv_pitch = cs.kv_pitch;
   prm.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
@@ -430,8 +366,8 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   prm.n_slots = plan.slots;
   prm.err = reinterpret_cast<int*>(ws);
 
-  if (plan.cascade_ok && workspace_bytes >= plan.cbytes)
-    return launch_cascade(plan, prm, q->ptr, q_rows, kv_indices, q_lat, q_rope, stream);
+  if (plan.cascade_ok && shared_len >= kMinShared && workspace_bytes >= plan.cbytes)
+    return launch_cascade(plan, prm, q->ptr, q_rows, shared_len, q_lat, q_rope, stream);
 
   switch (plan.NG) {
     case 16: rc = launch_decode_ng16(q_lat, q_rope, prm, plan.grid, stream); break;
@@ -478,6 +414,86 @@ int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_t
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_BAD_INPUT: return "MLA_ERR_BAD_INPUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_get_workspace_size(int32_t batch_size, int32_t num_heads, int32_t max_seqlen_q,
+                           int32_t num_kv_splits, int32_t num_sms, size_t* bytes_out) {
+  if (!bytes_out) return MLA_ERR_INVALID_ARG;
+  int sms = num_sms;
+  if (sms <= 0) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    rc = device_sms(dev, &sms);
+    if (rc) return rc;
+  }
+  Plan p;
+  int rc = make_plan(batch_size, num_heads, max_seqlen_q, num_kv_splits, sms, &p);
+  if (rc) return rc;
+  *bytes_out = p.bytes;
+  return MLA_OK;
+}
+
+int mla_get_shared_prefix_workspace_size(int32_t batch_size, int32_t num_heads,
+                                         int32_t max_seqlen_q, int32_t num_sms,
+                                         size_t* bytes_out) {
+  if (!bytes_out) return MLA_ERR_INVALID_ARG;
+  int sms = num_sms;
+  if (sms <= 0) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    rc = device_sms(dev, &sms);
+    if (rc) return rc;
+  }
+  Plan p;
+  int rc = make_plan(batch_size, num_heads, max_seqlen_q, 0, sms, &p);
+  if (rc) return rc;
+  *bytes_out = p.cbytes;
+  return MLA_OK;
+}
+
+int mla_decode(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
+               const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
+               const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
+               int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
+               const mla_tensor_t* kv_scale, int32_t num_kv_splits, const mla_tensor_t* lse_out,
+               void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  return decode_impl(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                     max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits, 0, lse_out,
+                     workspace, workspace_bytes, stream);
+}
+
+int mla_decode_shared_prefix(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
+                             const mla_tensor_t* o, const mla_tensor_t* qo_indptr,
+                             const mla_tensor_t* kv_indptr, const mla_tensor_t* kv_indices,
+                             const mla_tensor_t* kv_last_page_lens, int32_t max_seqlen_q,
+                             float sm_scale, const mla_tensor_t* q_scale,
+                             const mla_tensor_t* kv_scale, int32_t shared_prefix_len,
+                             const mla_tensor_t* lse_out, void* workspace,
+                             size_t workspace_bytes, mla_stream_t stream) {
+  return decode_impl(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                     max_seqlen_q, sm_scale, q_scale, kv_scale, 0, shared_prefix_len, lse_out,
+                     workspace, workspace_bytes, stream);
+}
+
 
 int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_parts,
                        const mla_tensor_t* reduce_indptr, const mla_tensor_t* reduce_idx,
@@ -581,6 +597,7 @@ int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream
   if (host & kErrTimeout) return MLA_ERR_TIMEOUT;
   if (host & kErrAnyIndex) return MLA_ERR_BAD_INDEX;
   if (host & kErrMisaligned) return MLA_ERR_UNSUPPORTED;
+  if (host & kErrBadInput) return MLA_ERR_BAD_INPUT;
   return MLA_ERR_CUDA;
 }
 

@@ -215,69 +215,6 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
 
 // ---------------------------------------------------------------- shared-prefix cascade
 
-struct SharedPrefixParams {
-  const int32_t* kv_indptr;
-  const int32_t* qo_indptr;
-  const int32_t* kv_indices;
-  int64_t kv_indices_len;
-  int B;
-  int* shared;     // holds a large value on entry; receives P
-};
-
-// P = the number of leading positions whose cache row ids are the same for every request
-// (compared with request 0), capped so that every query of every request sees all of them
-// (query t of a request with T queries and L positions sees positions <= L - T + t).
-// Work item = 256 positions of one request: each lane loads 8 of them (32 apart, so every
-// load instruction of the warp is coalesced) with all 16 loads in flight at once; the
-// warp then reports the first difference.  Items past the current P are skipped.
-constexpr int kPrefixCmpPerLane = 8;
-constexpr int kPrefixItem = 32 * kPrefixCmpPerLane;
-
-__global__ void __launch_bounds__(256) mla_shared_prefix_kernel(const SharedPrefixParams prm) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t b = gtid; b < prm.B; b += nthreads) {
-    const int L = prm.kv_indptr[b + 1] - prm.kv_indptr[b];
-    const int T = prm.qo_indptr[b + 1] - prm.qo_indptr[b];
-    const int lim = L - T + 1;
-    atomicMin(prm.shared, lim > 0 ? lim : 0);
-  }
-  if (prm.B < 2) return;
-  const int64_t base0 = prm.kv_indptr[0];
-  const int L0 = prm.kv_indptr[1] - prm.kv_indptr[0];
-  if (L0 <= 0) return;
-  const int64_t nitems = (L0 + kPrefixItem - 1) / kPrefixItem;
-  const int64_t total = static_cast<int64_t>(prm.B - 1) * nitems;
-  const int64_t nwarps = nthreads >> 5;
-  for (int64_t it = gtid >> 5; it < total; it += nwarps) {
-    const int64_t b = 1 + it / nitems;
-    const int j0 = static_cast<int>((it % nitems) * kPrefixItem);
-    const int cur = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(prm.shared), 0);
-    if (j0 >= cur) continue;   // a difference (or the cap) lies before this item
-    const int64_t bb = prm.kv_indptr[b];
-    const int Lb = prm.kv_indptr[b + 1] - static_cast<int>(bb);
-    const int n = L0 < Lb ? L0 : Lb;
-    int a[kPrefixCmpPerLane], c[kPrefixCmpPerLane];
-#pragma unroll
-    for (int u = 0; u < kPrefixCmpPerLane; ++u) {
-      const int j = j0 + 32 * u + lane;
-      const int64_t i0 = base0 + j, i1 = bb + j;
-      const bool ok = j < n && i0 >= 0 && i1 >= 0 && i0 < prm.kv_indices_len &&
-                      i1 < prm.kv_indices_len;
-      a[u] = ok ? __ldg(prm.kv_indices + i0) : 0;
-      c[u] = ok ? __ldg(prm.kv_indices + i1) : (j < n ? 1 : 0);   // out of range: differs
-    }
-    int first = 0x7FFFFFFF;
-#pragma unroll
-    for (int u = kPrefixCmpPerLane - 1; u >= 0; --u)
-      if (a[u] != c[u]) first = j0 + 32 * u + lane;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
-    if (lane == 0 && first != 0x7FFFFFFF) atomicMin(prm.shared, first);
-  }
-}
-
 struct CascadeMergeParams {
   SchedParams ss;          // suffix pass (rows per group = ss.NG)
   SchedParams sp;          // prefix pass (one group of sp.NG rows per virtual request)
@@ -296,8 +233,7 @@ struct CascadeMergeParams {
 
 // grid = (B * groups * NG, P / 2), block = 256.  Output row n of unit (b, g) of the suffix
 // schedule merges the prefix partials of its group (row (qo_b - qo_group) H + g NG + n of
-// that group's rows) with the partials of its own suffix.  When no prefix is shared the
-// suffix pass ran as a plain decode: units it wrote directly are skipped.
+// that group's rows) with the partials of its own suffix.
 template <int P>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
   const SchedParams& ss = prm.ss;
@@ -321,6 +257,8 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
   int sc = 0, pc = 0;
   const bool has_s = unit_partials<kSchedSuffix>(ss, b, g, &sf, &sc);
   const int L = ss.kv_indptr[b + 1] - ss.kv_indptr[b];
+  if (shared > 0 && L - shared < T - 1 && threadIdx.x == 0 && blockIdx.y == 0)
+    atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
   if (!has_s) {
     sc = 0;
     if (shared == 0 && L > 0) return;           // written directly by the decode kernel

@@ -15,10 +15,6 @@
 
 #include "../../include/paged_mla.h"
 
-// Workspace of the plain decode and of the shared-prefix cascade (mla_api.cu).
-int pmla_workspace_sizes(int B, int H, int max_seqlen_q, int num_kv_splits, int sms,
-                         size_t* whole, size_t* cascade);
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -61,12 +57,11 @@ extern "C" int mla_decode_noalloc(const mla_tensor_t* q, const mla_tensor_t* kv_
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!q || !qo_indptr || q->ndim != 3 || qo_indptr->ndim != 1 || qo_indptr->shape[0] < 1)
     return MLA_ERR_INVALID_ARG;
-  // Scratch this call needs, on the current device, against the fixed array (the plain
-  // decode must fit; the shared-prefix cascade runs only if its larger layout also fits).
-  size_t need = 0, cascade = 0;
-  int rc = pmla_workspace_sizes(static_cast<int>(qo_indptr->shape[0] - 1),
-                                static_cast<int>(q->shape[1]), max_seqlen_q, num_kv_splits, 0,
-                                &need, &cascade);
+  // Scratch this call needs, on the current device, against the fixed array.
+  size_t need = 0;
+  int rc = mla_get_workspace_size(static_cast<int32_t>(qo_indptr->shape[0] - 1),
+                                  static_cast<int32_t>(q->shape[1]), max_seqlen_q, num_kv_splits,
+                                  0, &need);
   if (rc != MLA_OK) return rc;
   if (need > static_cast<size_t>(MLA_NOALLOC_SCRATCH_BYTES)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;

@@ -59,9 +59,9 @@ PMLA_HD inline int groups_for(int rows_per_request, int ng) {
 //    a group is one MMA N-tile and each shared cache row is read once per group instead of
 //    once per request.  No causal masking: every query of the group sees the whole prefix.
 //  * kSchedSuffix: each request attends its own positions [P, L_b).
-// Both always write partials; the cascade merge combines the two per output row.  P is a
-// device value (found by a kernel from kv_indices, see mla_merge_kernel.cuh); values
-// below kMinShared count as 0.
+// Both always write partials; the cascade merge combines the two per output row.  P comes
+// from the caller, who knows its prefix cache (mla_decode_shared_prefix); prefixes
+// shorter than kMinShared are not split off.
 enum : int { kSchedWhole = 0, kSchedPrefix = 1, kSchedSuffix = 2 };
 constexpr int kMinShared = 1024;
 // The schedule functions take the mode as a template argument: a compile-time mode gives
@@ -80,7 +80,7 @@ struct SchedParams {
   int grid;        // CTAs launched
   int mode;        // kSchedWhole / kSchedPrefix / kSchedSuffix
   int gsize;       // kSchedPrefix: requests per virtual request
-  const int32_t* shared;   // kSchedPrefix / kSchedSuffix: the shared prefix length P
+  int shared;      // kSchedPrefix / kSchedSuffix: the shared prefix length P
 };
 
 struct Piece {
@@ -103,8 +103,8 @@ PMLA_HD inline int sched_mode(const SchedParams& sp) {
 // The shared prefix length a schedule uses (0 in whole mode or below kMinShared).
 template <int MODE = kSchedAny>
 PMLA_HD inline int64_t sched_shared(const SchedParams& sp) {
-  if (sched_mode<MODE>(sp) == kSchedWhole || sp.shared == nullptr) return 0;
-  const int64_t P = *sp.shared;
+  if (sched_mode<MODE>(sp) == kSchedWhole) return 0;
+  const int64_t P = sp.shared;
   return P >= kMinShared ? P : 0;
 }
 

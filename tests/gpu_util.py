@@ -22,18 +22,26 @@ def to_device(case, device="cuda"):
 
 
 def run_gpu(case, num_kv_splits=0, o_dtype=torch.bfloat16, with_lse=True, workspace=None,
-            kv_view=None, q_override=None):
+            kv_view=None, q_override=None, shared_prefix=None):
+    """shared_prefix: None -> mla_decode; an int P -> mla_decode_shared_prefix(P)."""
     import paged_mla_latent_gb300 as pm
     q = case.q if q_override is None else q_override
     n_tok, H = q.shape[0], q.shape[1]
     o = torch.full((n_tok, H, 512), float("nan"), dtype=o_dtype, device=q.device)
     lse = torch.full((n_tok, H), float("nan"), dtype=torch.float32, device=q.device) if with_lse else None
     if workspace is None:
-        workspace = pm.make_workspace(case.B, H, case.max_seqlen_q, num_kv_splits, q.device)
+        workspace = pm.make_workspace(case.B, H, case.max_seqlen_q, num_kv_splits, q.device,
+                                      shared_prefix=shared_prefix is not None)
     kv = case.kv if kv_view is None else kv_view
-    pm.mla_decode(q, kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
-                  case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
-                  case.kv_scale, num_kv_splits=num_kv_splits, lse_out=lse, workspace=workspace)
+    if shared_prefix is None:
+        pm.mla_decode(q, kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                      case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
+                      case.kv_scale, num_kv_splits=num_kv_splits, lse_out=lse, workspace=workspace)
+    else:
+        pm.mla_decode_shared_prefix(q, kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                                    case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale,
+                                    case.q_scale, case.kv_scale, shared_prefix, lse_out=lse,
+                                    workspace=workspace)
     torch.cuda.synchronize()
     status = pm.mla_check_error(workspace)
     return o, lse, status

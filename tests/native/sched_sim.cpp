@@ -44,7 +44,7 @@ int sched_unit_partials(const int32_t* kv_indptr, const int32_t* qo_indptr, int 
 int64_t sched_pieces_mode(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H, int NG,
                           int groups, int splits, int grid, int mode, int gsize, int shared,
                           int64_t* out, int64_t max_out) {
-  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, &shared};
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared};
   int64_t n = 0;
   for (int cta = 0; cta < grid; ++cta) {
     pmla::PieceIter it;
@@ -66,7 +66,7 @@ int64_t sched_pieces_mode(const int32_t* kv_indptr, const int32_t* qo_indptr, in
 int sched_unit_partials_mode(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H,
                              int NG, int groups, int splits, int grid, int mode, int gsize,
                              int shared, int v, int g, int64_t* first, int* count) {
-  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, &shared};
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared};
   return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
 }
 

@@ -58,24 +58,11 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_plan(lib):
-    # auto policy: (B*groups + SMs) partial slots of NG rows x (512 + 1) floats + header,
-    # and for decode batches (<= 24 rows per request) the shared-prefix cascade's prefix
-    # pass: (ceil(B / groups of 4) + SMs) slots of 48 rows
+    # auto policy: (B*groups + SMs) partial slots of NG rows x (512 + 1) floats + header
     sz = lib.mla_get_workspace_size(16, 12, 1, 0, 152)
     ng, slots = 16, 16 + 152
-    pslots = 4 + 152
     plain = 256 + slots * ng * 513 * 4
-    prefix = pslots * 48 * 513 * 4
-    assert plain + prefix <= sz < plain + prefix + 4 * 256
-    # fewer requests than one group of 4: no cascade
-    sz3 = lib.mla_get_workspace_size(3, 12, 1, 0, 152)
-    assert sz3 < 256 + (3 + 152) * 16 * 513 * 4 + 3 * 256
-    # one request: no cascade
-    sz1 = lib.mla_get_workspace_size(1, 12, 1, 0, 152)
-    assert 256 + 153 * 16 * 513 * 4 <= sz1 < 256 + 153 * 16 * 513 * 4 + 3 * 256
-    # q_len 4 x 12 heads = 48 rows: no room for two requests per group, no cascade
-    sz4 = lib.mla_get_workspace_size(64, 12, 4, 0, 152)
-    assert sz4 < 256 + (64 + 152) * 48 * 513 * 4 + 3 * 256
+    assert plain <= sz < plain + 2 * 256
     # 96 heads -> two groups of 48 rows
     sz96 = lib.mla_get_workspace_size(1, 96, 1, 0, 152)
     assert sz96 >= (2 + 152) * 48 * 513 * 4
@@ -85,6 +72,18 @@ def test_workspace_size_plan(lib):
         lib.mla_get_workspace_size(16, 12, 0, 0, 152)     # max_seqlen_q < 1
     with pytest.raises(lib.MlaError):
         lib.mla_get_workspace_size(16, 0, 1, 0, 152)      # no heads
+
+
+def test_shared_prefix_workspace_size(lib):
+    # plain partials + the prefix pass's: (ceil(B / 4) + SMs) slots of 48 rows
+    sz = lib.mla_get_shared_prefix_workspace_size(16, 12, 1, 152)
+    plain = lib.mla_get_workspace_size(16, 12, 1, 0, 152)
+    prefix = (4 + 152) * 48 * 513 * 4
+    assert plain + prefix <= sz < plain + prefix + 3 * 256
+    # batches that never take the shared-prefix path need only the plain workspace
+    for B, H, T in [(3, 12, 1), (1, 12, 1), (64, 12, 4), (16, 96, 1)]:
+        assert (lib.mla_get_shared_prefix_workspace_size(B, H, T, 152) ==
+                lib.mla_get_workspace_size(B, H, T, 0, 152))
 
 
 def _t(ptr, dtype, shape, stride=None):
@@ -150,6 +149,25 @@ def _call(a):
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, over, expect):
     assert _call(_args(**over)) == expect
+
+
+def _call_sp(a, prefix):
+    import paged_mla_latent_gb300 as pm
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    return pm._lib.mla_decode_shared_prefix(
+        r(a["q"]), r(a["kv"]), r(a["o"]), r(a["qo"]), r(a["kvp"]), r(a["idx"]), r(a["last"]),
+        a["mq"], a["sm"], r(a["qs"]), r(a["ks"]), prefix, r(a["lse"]), ctypes.c_void_p(a["ws"]),
+        a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,prefix,expect", [
+    (dict(), -1, 1),                                  # negative shared prefix
+    (dict(q=None), 2048, 1),
+    (dict(o=_t((1 << 40) + (2 << 20), 2, [2, 12, 256])), 2048, 1),
+    (dict(ws=(1 << 40) + 8), 2048, 1),
+])
+def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib, over, prefix, expect):
+    assert _call_sp(_args(**over), prefix) == expect
 
 
 def test_merge_rejects_bad_arguments_on_host(lib):

@@ -19,14 +19,21 @@ def pm():
     return m
 
 
-def _run(pm, case):
+def _run(pm, case, shared_prefix=None):
     n_tok, H = case.q.shape[0], case.q.shape[1]
     o = torch.full((n_tok, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((n_tok, H), float("nan"), dtype=torch.float32, device="cuda")
-    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, 0, "cuda")
-    pm.mla_decode(case.q, case.kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
-                  case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
-                  case.kv_scale, lse_out=lse, workspace=ws)
+    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, 0, "cuda",
+                           shared_prefix=shared_prefix is not None)
+    if shared_prefix is None:
+        pm.mla_decode(case.q, case.kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                      case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
+                      case.kv_scale, lse_out=lse, workspace=ws)
+    else:
+        pm.mla_decode_shared_prefix(case.q, case.kv, o, case.qo_indptr, case.kv_indptr,
+                                    case.kv_indices, case.kv_last_page_lens, case.max_seqlen_q,
+                                    case.sm_scale, case.q_scale, case.kv_scale, shared_prefix,
+                                    lse_out=lse, workspace=ws)
     torch.cuda.synchronize()
     assert pm.mla_check_error(ws) == 0
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
@@ -45,9 +52,10 @@ def _check_samples(case, o, lse, samples):
 
 @pytest.mark.parametrize("name", ["c16", "c24"])
 @pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
-def test_shared_prefix_workloads_sampled(pm, name, scales):
+@pytest.mark.parametrize("entry", ["plain", "shared_prefix"])
+def test_shared_prefix_workloads_sampled(pm, name, scales, entry):
     case = mla_inputs.make_case(name, seed=0, device="cuda", q_scale=scales[0], kv_scale=scales[1])
-    o, lse = _run(pm, case)
+    o, lse = _run(pm, case, case.meta["shared_prefix"] if entry == "shared_prefix" else None)
     B = case.B
     _check_samples(case, o, lse, [(0, 0, 0), (0, 0, 11), (B // 2, 0, 5), (B - 1, 0, 7)])
 

@@ -111,56 +111,50 @@ def test_shared_prefix(pm):
     _check(case)
 
 
-def _shared_found(ws):
-    """The shared prefix length the cascade's detection left in the workspace header."""
-    return int(ws[128:132].view(torch.int32).item())
-
-
-@pytest.mark.parametrize("kv_lens,q_lens,prefix,expect", [
-    ([3000, 3100, 2900, 3050, 3200], [1] * 5, 2048, 2048),         # 2 groups (4 + 1)
-    ([2500] * 9, [1] * 9, 2500, 2500),                             # whole requests shared
-    ([2600, 2100, 3300, 2100, 2800, 2200], [1] * 6, 2100, 2100),   # some suffixes empty
-    ([4000, 4500, 3900], [2, 2, 2], 3000, 3000),                   # 2 queries each, causal tail
-    ([3000, 3000, 3000, 3000], [1, 2, 1, 1], 2999, 2999),          # prefix up to the causal cap
-    ([1500, 1700, 1600, 1800], [1] * 4, 900, 900),                 # too short to split off
+@pytest.mark.parametrize("kv_lens,q_lens,prefix", [
+    ([3000, 3100, 2900, 3050, 3200], [1] * 5, 2048),         # 2 groups (4 + 1)
+    ([2500] * 9, [1] * 9, 2500),                             # whole requests shared
+    ([2600, 2100, 3300, 2100, 2800, 2200], [1] * 6, 2100),   # some suffixes empty
+    ([4000, 4500, 3900, 4100], [2] * 4, 3000),               # 2 queries each, causal tail
+    ([3000, 3000, 3000, 3000], [1, 2, 1, 1], 2999),          # prefix up to the causal cap
+    ([1500, 1700, 1600, 1800], [1] * 4, 900),                # too short: plain decode
+    ([2000, 2100, 2200], [1] * 3, 1500),                     # under one group: plain decode
 ])
 @pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
-def test_shared_prefix_cascade(pm, kv_lens, q_lens, prefix, expect, scales):
-    """Requests sharing their first cache rows go through the cascade (prefix pass over
-    groups of requests, suffix pass per request, merge); the result must equal the oracle,
-    and the detected prefix must be exactly the shared rows (capped so every query sees
-    them all)."""
+def test_shared_prefix_cascade(pm, kv_lens, q_lens, prefix, scales):
+    """mla_decode_shared_prefix: the shared rows are attended in groups of requests (prefix
+    pass), each request's own rows separately (suffix pass), and the halves merged; the
+    result must equal the oracle.  Unattended rows are poisoned."""
     case = gu.to_device(mla_inputs.make_custom(kv_lens, q_lens=q_lens, H=12, seed=31,
                                                shared_prefix=prefix, q_scale=scales[0],
                                                kv_scale=scales[1], poison=True,
                                                index_buffer=sum(kv_lens) + 64, name="cascade"))
-    ws = pm.make_workspace(case.B, 12, case.max_seqlen_q, 0, "cuda")
-    o, lse, status = gu.run_gpu(case, workspace=ws)
+    o, lse, status = gu.run_gpu(case, shared_prefix=prefix)
     assert status == 0, f"device error {status}"
-    cap = min(L - T + 1 for L, T in zip(kv_lens, q_lens))
-    assert _shared_found(ws) == min(expect, cap)
     o_ref, lse_ref = gu.run_oracle(case)
     gu.compare(o, lse, o_ref, lse_ref, what="cascade")
 
 
-def test_cascade_needs_the_larger_workspace(pm):
-    """A workspace that holds only the plain decode's partials still gives the right answer:
-    the cascade is skipped (its prefix length is never written)."""
+def test_shared_prefix_with_the_plain_workspace(pm):
+    """With only the plain decode's workspace the call runs the plain decode: same answer."""
     case = gu.to_device(mla_inputs.make_custom([3000] * 5, H=12, seed=32, shared_prefix=2500,
                                                q_scale=1.0, kv_scale=1.0))
-    full = pm.mla_get_workspace_size(case.B, 12, 1, 0)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    slots = case.B * 1 + sms                  # 16-row groups, one per request, automatic split
-    align = lambda x: (x + 255) // 256 * 256
-    plain = align(256 + slots * 16 * 4) + slots * 16 * 512 * 4
-    assert plain < full
+    plain = pm.mla_get_workspace_size(case.B, 12, 1, 0)
+    assert plain < pm.mla_get_shared_prefix_workspace_size(case.B, 12, 1)
     ws = torch.zeros(plain, dtype=torch.uint8, device="cuda")
-    o, lse, status = gu.run_gpu(case, workspace=ws)
+    o, lse, status = gu.run_gpu(case, workspace=ws, shared_prefix=2500)
     assert status == 0
-    assert _shared_found(ws) == 0
     o_ref, lse_ref = gu.run_oracle(case)
     gu.compare(o, lse, o_ref, lse_ref, what="plain path")
 
+
+def test_shared_prefix_beyond_a_query_is_flagged(pm):
+    """A claimed prefix that the second draft of a request could not see in full (P > kv_len
+    - q_len + 1) is reported as bad input; the kernels finish normally."""
+    case = gu.to_device(mla_inputs.make_custom([3000, 3000, 3000, 3000], q_lens=[1, 2, 1, 1],
+                                               H=12, seed=33, shared_prefix=3000))
+    o, lse, status = gu.run_gpu(case, shared_prefix=3000)
+    assert status == 7   # MLA_ERR_BAD_INPUT
 
 
 def test_poisoned_rows_and_index_tail(pm):
