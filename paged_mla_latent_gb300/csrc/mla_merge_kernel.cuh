@@ -25,11 +25,14 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeUnroll = 4;          // partials in flight per thread
 
-// Partial lanes for an average of `per_row` partials per merged row: 2 .. 64 (2: one
-// block holds a whole 512-column row).
+// Partial lanes for an average of `per_row` partials per merged row: the smallest power
+// of two (2 .. 64) that leaves each lane at most one round of kMergeUnroll loads, so that
+// few blocks (each paying its set-up latency) cover the rows.  2: a block holds a whole
+// 512-column row.
 inline int merge_lanes_for(int64_t per_row) {
-  return per_row >= 96 ? 64 : per_row >= 40 ? 32 : per_row >= 16 ? 16 : per_row >= 8 ? 8
-       : per_row >= 4 ? 4 : 2;
+  int lanes = 2;
+  while (lanes < 64 && lanes * kMergeUnroll < per_row) lanes *= 2;
+  return lanes;
 }
 constexpr int kMergeBlocksPerSm = 3;   // launch bound: registers for 3 resident blocks
 
