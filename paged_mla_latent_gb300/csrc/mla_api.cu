@@ -219,6 +219,47 @@ int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Pl
 
 namespace {
 
+// Launch a merge kernel instantiation for (lanes, unroll) with programmatic dependent launch:
+// the merge grid is scheduled while the decode grid runs and waits on the device
+// (griddepcontrol.wait) for the partials.
+template <int P, int U>
+struct SplitMergeK {
+  static void* fn() { return reinterpret_cast<void*>(mla_split_merge_kernel<P, U>); }
+};
+template <int P, int U>
+struct CascadeMergeK {
+  static void* fn() { return reinterpret_cast<void*>(mla_cascade_merge_kernel<P, U>); }
+};
+
+template <template <int, int> class K>
+void* merge_fn(const MergeShape& ms) {
+  const bool u8 = ms.unroll == 8;
+  switch (ms.lanes) {
+    case 64: return u8 ? K<64, 8>::fn() : K<64, 4>::fn();
+    case 32: return u8 ? K<32, 8>::fn() : K<32, 4>::fn();
+    case 16: return u8 ? K<16, 8>::fn() : K<16, 4>::fn();
+    case 8: return u8 ? K<8, 8>::fn() : K<8, 4>::fn();
+    case 4: return u8 ? K<4, 8>::fn() : K<4, 4>::fn();
+    default: return u8 ? K<2, 8>::fn() : K<2, 4>::fn();
+  }
+}
+
+template <template <int, int> class K, class Params>
+cudaError_t launch_merge(const MergeShape& ms, int64_t n_rows, const Params& mp, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_rows), ms.lanes / 2);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<Params*>(&mp)};
+  return cudaLaunchKernelExC(&cfg, merge_fn<K>(ms), args);
+}
+
 // Shared-prefix cascade: the prefix pass (groups of plan.gsize requests over the first
 // `shared` positions, 48-row tiles) and the suffix pass (each request's own positions)
 // write partials, and the cascade merge combines the two per output row.
@@ -270,26 +311,9 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   const int64_t units = static_cast<int64_t>(prm.sp.B) * plan.groups;
   const int VB = (prm.sp.B + plan.gsize - 1) / plan.gsize;
   // partials per row: the CTAs of one prefix group plus those of one suffix
-  const int lanes = merge_lanes_for(plan.grid / VB + plan.grid / (units > 0 ? units : 1) + 4);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), lanes / 2);
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  switch (lanes) {
-    case 64: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<64>, mp); break;
-    case 32: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<32>, mp); break;
-    case 16: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<16>, mp); break;
-    case 8: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<8>, mp); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<4>, mp); break;
-    default: e = cudaLaunchKernelEx(&cfg, mla_cascade_merge_kernel<2>, mp); break;
-  }
+  const MergeShape ms = merge_shape_for(plan.grid / VB + plan.grid / (units > 0 ? units : 1) + 4,
+                                        units * plan.NG, plan.grid);
+  const cudaError_t e = launch_merge<CascadeMergeK>(ms, units * plan.NG, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -389,28 +413,9 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
   const int64_t units = static_cast<int64_t>(cs.B) * plan.groups;
-  const int lanes = merge_lanes_for(units > 0 ? plan.slots / units : 1);
-  // Programmatic dependent launch: the merge grid is scheduled while the decode grid
-  // runs and waits on the device (griddepcontrol.wait) for the partials.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * plan.NG), lanes / 2);
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  switch (lanes) {
-    case 64: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<64>, mp); break;
-    case 32: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<32>, mp); break;
-    case 16: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<16>, mp); break;
-    case 8: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<8>, mp); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<4>, mp); break;
-    default: e = cudaLaunchKernelEx(&cfg, mla_split_merge_kernel<2>, mp); break;
-  }
+  const MergeShape ms = merge_shape_for(units > 0 ? plan.slots / units : 1, units * plan.NG,
+                                        plan.grid);
+  const cudaError_t e = launch_merge<SplitMergeK>(ms, units * plan.NG, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -536,7 +541,7 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
   prm.o_stride_h = o->stride[1];
   prm.lse_out = lse_out ? static_cast<float*>(lse_out->ptr) : nullptr;
   prm.err = error_word;
-  const int lanes = merge_lanes_for(m / n_out);
+  const int lanes = merge_lanes_for(m / n_out, 4);
   dim3 grid(static_cast<unsigned>(n_out * H), lanes / 2);
   switch (lanes) {
     case 64: mla_csr_merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(prm); break;

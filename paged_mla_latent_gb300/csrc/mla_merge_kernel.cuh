@@ -22,19 +22,31 @@
 namespace pmla {
 
 constexpr int kMergeThreads = 256;
+constexpr int kMergeBlocksPerSm = 3;   // launch bound: registers for 3 resident blocks
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeUnroll = 4;          // partials in flight per thread
 
-// Partial lanes for an average of `per_row` partials per merged row: the smallest power
-// of two (2 .. 64) that leaves each lane at most one round of kMergeUnroll loads, so that
-// few blocks (each paying its set-up latency) cover the rows.  2: a block holds a whole
-// 512-column row.
-inline int merge_lanes_for(int64_t per_row) {
+// Merge launch shape for n_rows merged rows of ~per_row partials each: P partial lanes
+// (2 .. 64; a block covers 1024 / P columns, 2 = a whole 512-column row) with U loads in
+// flight per lane.  P is the smallest power of two leaving each lane one round of U loads.
+// A grid within two waves of resident blocks keeps U = 4 (more, lighter blocks); a larger
+// one takes U = 8 when that halves the lanes (half the blocks, each paying its set-up
+// latency once).
+struct MergeShape {
+  int lanes, unroll;
+};
+inline int merge_lanes_for(int64_t per_row, int unroll) {
   int lanes = 2;
-  while (lanes < 64 && lanes * kMergeUnroll < per_row) lanes *= 2;
+  while (lanes < 64 && lanes * unroll < per_row) lanes *= 2;
   return lanes;
 }
-constexpr int kMergeBlocksPerSm = 3;   // launch bound: registers for 3 resident blocks
+inline MergeShape merge_shape_for(int64_t per_row, int64_t n_rows, int sms) {
+  const int l4 = merge_lanes_for(per_row, 4);
+  const int l8 = merge_lanes_for(per_row, 8);
+  if (l8 == l4 || n_rows * (l4 / 2) <= 2 * static_cast<int64_t>(sms) * kMergeBlocksPerSm)
+    return {l4, 4};
+  return {l8, 8};
+}
+
 
 struct MergeOut {
   void* o;
@@ -66,7 +78,7 @@ __device__ __forceinline__ void merge_combine(MergeState& x, float m2, float w2,
 // lse_of(k) and o_of(k) give partial k's log-sum-exp and the start of its 512 normalised
 // values.  Lanes of one warp that share a column quad combine by shuffles, the eight warps
 // through shared memory.
-template <int P, class OOf, class LseOf>
+template <int P, int U, class OOf, class LseOf>
 __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const MergeOut& out,
                                      int col0) {
   constexpr int Q = kMergeThreads / P;    // column quads per block
@@ -81,18 +93,18 @@ __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const Me
   const int c = threadIdx.x % Q;
   const int p = threadIdx.x / Q;
   MergeState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-  for (int k0 = p; k0 < count; k0 += kMergeUnroll * P) {
-    float l[kMergeUnroll];
-    float4 v[kMergeUnroll];
+  for (int k0 = p; k0 < count; k0 += U * P) {
+    float l[U];
+    float4 v[U];
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int k = k0 + u * P;
       l[u] = (k < count) ? lse_of(k) : -INFINITY;
       v[u] = (k < count) ? *reinterpret_cast<const float4*>(o_of(k) + col0 + 4 * c)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) merge_combine(st, l[u], 1.f, v[u]);
+    for (int u = 0; u < U; ++u) merge_combine(st, l[u], 1.f, v[u]);
   }
   const int lane = threadIdx.x & 31;
   if constexpr (Q < 32) {
@@ -168,7 +180,7 @@ struct SplitMergeParams {
 // grid = (units * NG, P / 2), block = 256.  Merges the units the scheduler split and writes
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
-template <int P>
+template <int P, int U>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_merge_kernel(const SplitMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
@@ -213,7 +225,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
     }
     return prm.part_lse[(first + k) * NG + n];
   };
-  merge_partials_block<P>(count, o_of, lse_of, out, col0);
+  merge_partials_block<P, U>(count, o_of, lse_of, out, col0);
 }
 
 // ---------------------------------------------------------------- shared-prefix cascade
@@ -237,7 +249,7 @@ struct CascadeMergeParams {
 // grid = (B * groups * NG, P / 2), block = 256.  Output row n of unit (b, g) of the suffix
 // schedule merges the prefix partials of its group (row (qo_b - qo_group) H + g NG + n of
 // that group's rows) with the partials of its own suffix.
-template <int P>
+template <int P, int U>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
   const SchedParams& ss = prm.ss;
   const int NGs = ss.NG;
@@ -294,7 +306,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
   auto lse_of = [&](int k) -> float {
     return k < pc ? prm.p_lse[(pf + k) * pNG + np] : prm.s_lse[(sf + (k - pc)) * NGs + n];
   };
-  merge_partials_block<P>(pc + sc, o_of, lse_of, out, col0);
+  merge_partials_block<P, U>(pc + sc, o_of, lse_of, out, col0);
 }
 
 struct CsrMergeParams {
@@ -344,7 +356,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_csr_merg
     }
     return prm.lse_parts[s * prm.lp_stride_p + h * prm.lp_stride_h];
   };
-  merge_partials_block<P>(count, o_of, lse_of, out, col0);
+  merge_partials_block<P, 4>(count, o_of, lse_of, out, col0);
 }
 
 struct ValidateParams {
