@@ -173,9 +173,9 @@ struct Plan {
   int NG, groups, grid, splits;
   int64_t slots;
   size_t lse_off, o_off, bytes;
-  // Shared-prefix cascade (automatic policy, decode batches of <= 24 rows per request):
-  // prefix pass over groups of gsize requests with 48-row tiles, partials after the
-  // plain layout; cbytes = workspace for the plain layout plus those.
+  // Shared-prefix cascade (decode batches of <= 24 rows per request, at least one group):
+  // 48-row tiles over gsize-request prefix units and per-request units, pslots partial
+  // slots at plse_off / po_off (same header); cbytes = the larger of both layouts.
   bool cascade_ok;
   int gsize;
   int64_t pslots;
@@ -206,11 +206,12 @@ int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Pl
     // sharing the prefix saves)
     p->cascade_ok = true;
     p->gsize = kPrefixNG / rows;
-    const int VB = (B + p->gsize - 1) / p->gsize;
-    p->pslots = partial_slots(VB, 1, 0, p->grid);
-    p->plse_off = align_up(p->bytes, 256);
+    const int VP = (B + p->gsize - 1) / p->gsize;
+    p->pslots = partial_slots(VP + B, 1, 0, p->grid);
+    p->plse_off = kHeaderBytes;
     p->po_off = align_up(p->plse_off + static_cast<size_t>(p->pslots) * kPrefixNG * sizeof(float), 256);
-    p->cbytes = p->po_off + static_cast<size_t>(p->pslots) * kPrefixNG * kDV * sizeof(float);
+    const size_t end = p->po_off + static_cast<size_t>(p->pslots) * kPrefixNG * kDV * sizeof(float);
+    p->cbytes = end > p->bytes ? end : p->bytes;
   }
   return MLA_OK;
 }
@@ -260,19 +261,18 @@ cudaError_t launch_merge(const MergeShape& ms, int64_t n_rows, const Params& mp,
   return cudaLaunchKernelExC(&cfg, merge_fn<K>(ms), args);
 }
 
-// Shared-prefix cascade: the prefix pass (groups of plan.gsize requests over the first
-// `shared` positions, 48-row tiles) and the suffix pass (each request's own positions)
-// write partials, and the cascade merge combines the two per output row.
+// Shared-prefix cascade: one launch of the 48-row kernel over the prefix units (groups of
+// plan.gsize requests attending the first `shared` positions) and the requests' own
+// units, then the cascade merge of each row's two parts.
 int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr, int64_t q_rows,
-                   int32_t shared, const CUtensorMap& q_lat, const CUtensorMap& q_rope,
-                   cudaStream_t stream) {
+                   int32_t shared, int max_rows, cudaStream_t stream) {
   uint8_t* ws = reinterpret_cast<uint8_t*>(prm.err);
-  CUtensorMap p_lat, p_rope;
   int rc;
+  CUtensorMap p_lat, p_rope;
   if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
   if ((rc = make_map(&p_rope, q_ptr, q_rows, kD, 64, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
   DecodeParams pp = prm;
-  pp.sp.mode = kSchedPrefix;
+  pp.sp.mode = kSchedCascade;
   pp.sp.NG = kPrefixNG;
   pp.sp.groups = 1;
   pp.sp.gsize = plan.gsize;
@@ -282,25 +282,12 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   pp.n_slots = plan.pslots;
   if ((rc = launch_decode_ng48(p_lat, p_rope, pp, plan.grid, stream))) return rc;
 
-  DecodeParams ps = prm;
-  ps.sp.mode = kSchedSuffix;
-  ps.sp.gsize = plan.gsize;
-  ps.sp.shared = shared;
-  switch (plan.NG) {
-    case 16: rc = launch_decode_ng16(q_lat, q_rope, ps, plan.grid, stream); break;
-    default: rc = launch_decode_ng32(q_lat, q_rope, ps, plan.grid, stream); break;
-  }
-  if (rc) return rc;
-
   CascadeMergeParams mp;
-  mp.ss = ps.sp;
   mp.sp = pp.sp;
-  mp.s_o = ps.part_o;
-  mp.s_lse = ps.part_lse;
-  mp.p_o = pp.part_o;
-  mp.p_lse = pp.part_lse;
-  mp.s_slots = ps.n_slots;
-  mp.p_slots = pp.n_slots;
+  mp.part_o = pp.part_o;
+  mp.part_lse = pp.part_lse;
+  mp.n_slots = pp.n_slots;
+  mp.rows_per_req = max_rows;
   mp.o = prm.o;
   mp.o_fp32 = prm.o_fp32;
   mp.o_stride_tok = prm.o_stride_tok;
@@ -308,12 +295,12 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   mp.lse_out = prm.lse_out;
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
-  const int64_t units = static_cast<int64_t>(prm.sp.B) * plan.groups;
-  const int VB = (prm.sp.B + plan.gsize - 1) / plan.gsize;
-  // partials per row: the CTAs of one prefix group plus those of one suffix
-  const MergeShape ms = merge_shape_for(plan.grid / VB + plan.grid / (units > 0 ? units : 1) + 4,
-                                        units * plan.NG, plan.grid);
-  const cudaError_t e = launch_merge<CascadeMergeK>(ms, units * plan.NG, mp, stream);
+  const int B = prm.sp.B;
+  const int VP = (B + plan.gsize - 1) / plan.gsize;
+  const int64_t n_rows = static_cast<int64_t>(B) * max_rows;
+  // partials per row: the CTAs one prefix unit spans plus those of the request's own unit
+  const MergeShape ms = merge_shape_for(plan.grid / VP + plan.grid / B + 4, n_rows, plan.grid);
+  const cudaError_t e = launch_merge<CascadeMergeK>(ms, n_rows, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -391,7 +378,8 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   prm.err = reinterpret_cast<int*>(ws);
 
   if (plan.cascade_ok && shared_len >= kMinShared && workspace_bytes >= plan.cbytes)
-    return launch_cascade(plan, prm, q->ptr, q_rows, shared_len, q_lat, q_rope, stream);
+    return launch_cascade(plan, prm, q->ptr, q_rows, shared_len,
+                          static_cast<int>(cs.H * max_seqlen_q), stream);
 
   switch (plan.NG) {
     case 16: rc = launch_decode_ng16(q_lat, q_rope, prm, plan.grid, stream); break;

@@ -31,13 +31,13 @@ int launch_decode_mode(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-// The plain decode, or the cascade half (CASCADE) this row-group size runs.
+// The plain decode, or (CASCADE = kSchedCascade) the shared-prefix cascade.
 template <int NG, int STAGES, int CASCADE>
 int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream) {
   if (prm.sp.mode == kSchedWhole)
     return launch_decode_mode<NG, STAGES, kSchedWhole>(q_lat, q_rope, prm, grid, stream);
-  if (prm.sp.mode == CASCADE)
+  if (CASCADE != kSchedWhole && prm.sp.mode == CASCADE)
     return launch_decode_mode<NG, STAGES, CASCADE>(q_lat, q_rope, prm, grid, stream);
   return MLA_ERR_UNSUPPORTED;
 }

@@ -210,8 +210,8 @@ __device__ __forceinline__ void issue_q_load(uint32_t sQ, const CUtensorMap* lat
   tma_load_2d(sQ + 4 * NG * 128, rope, 512, qrow, bar);
 }
 
-// MODE: the schedule (kSchedWhole for a plain decode, kSchedPrefix / kSchedSuffix for the
-// two halves of the shared-prefix cascade), fixed at compile time.
+// MODE: the schedule (kSchedWhole for a plain decode, kSchedCascade for the shared-prefix
+// cascade), fixed at compile time.
 template <int NG, int STAGES, int MODE>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
@@ -353,6 +353,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // Columns are independent heads: each 16-column chunk is finished in one pass.
 #pragma unroll
         for (int ch = 0; ch < kCh; ++ch) {
+          // chunks past the unit's real rows (a 12-row unit in a 48-row tile) are skipped:
+          // their P columns only feed O columns that are never written out
+          if (ch > 0 && 16 * ch >= pc.rows) break;
           float xs[16];
           tmem_ld16(s_tm + 16 * ch, xs);
           tmem_wait_ld();
@@ -495,6 +498,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           __nv_bfloat16* hdst = reinterpret_cast<__nv_bfloat16*>(prm.o);
 #pragma unroll 1
           for (int ch = 0; ch < NG / 16; ++ch) {
+            if (ch > 0 && 16 * ch >= pc.rows) break;   // no real rows left
 #pragma unroll 1
             for (int bk = 0; bk < 4; ++bk) {
               float hi[16], lo[16];

@@ -231,13 +231,11 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
 // ---------------------------------------------------------------- shared-prefix cascade
 
 struct CascadeMergeParams {
-  SchedParams ss;          // suffix pass (rows per group = ss.NG)
-  SchedParams sp;          // prefix pass (one group of sp.NG rows per virtual request)
-  const float* s_o;        // (slots, ss.NG, 512)
-  const float* s_lse;
-  const float* p_o;        // (slots, sp.NG, 512)
-  const float* p_lse;
-  int64_t s_slots, p_slots;
+  SchedParams sp;          // the cascade schedule (sp.NG rows per slot, one group per unit)
+  const float* part_o;     // (slots, sp.NG, 512)
+  const float* part_lse;   // (slots, sp.NG)
+  int64_t n_slots;
+  int rows_per_req;        // grid.x = B * rows_per_req (= max_seqlen_q * H)
   void* o;
   int o_fp32;
   int64_t o_stride_tok, o_stride_head;
@@ -246,65 +244,52 @@ struct CascadeMergeParams {
   int* err;
 };
 
-// grid = (B * groups * NG, P / 2), block = 256.  Output row n of unit (b, g) of the suffix
-// schedule merges the prefix partials of its group (row (qo_b - qo_group) H + g NG + n of
-// that group's rows) with the partials of its own suffix.
+// grid = (B * rows_per_req, P / 2), block = 256.  Row rr of request b merges the partials
+// of its group's prefix unit (at row (qo_b - qo_group) H + rr of the group's rows) with
+// those of its own unit (row rr).
 template <int P, int U>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
-  const SchedParams& ss = prm.ss;
-  const int NGs = ss.NG;
-  const int64_t u = blockIdx.x / NGs;
-  const int n = static_cast<int>(blockIdx.x - u * NGs);
-  const int b = static_cast<int>(u / ss.groups);
-  const int g = static_cast<int>(u - static_cast<int64_t>(b) * ss.groups);
+  const SchedParams& sp = prm.sp;
+  const int NG = sp.NG;
+  const int b = static_cast<int>(blockIdx.x / prm.rows_per_req);
+  const int rr = static_cast<int>(blockIdx.x - static_cast<int64_t>(b) * prm.rows_per_req);
   const int col0 = blockIdx.y * (4 * kMergeThreads / P);
-  const int qo0 = ss.qo_indptr[b];
-  const int T = ss.qo_indptr[b + 1] - qo0;
-  const int rr = g * NGs + n;                   // row within the request (token-major)
-  if (rr >= T * ss.H || n >= NGs) return;
-  const int64_t r = static_cast<int64_t>(qo0) * ss.H + rr;
+  const int qo0 = sp.qo_indptr[b];
+  const int T = sp.qo_indptr[b + 1] - qo0;
+  if (rr >= T * sp.H) return;
+  const int64_t r = static_cast<int64_t>(qo0) * sp.H + rr;
   if (r < 0 || r >= prm.n_q_rows) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeRow);
     return;
   }
-  const int64_t shared = sched_shared<kSchedSuffix>(ss);
-  int64_t sf = 0, pf = 0;
-  int sc = 0, pc = 0;
-  const bool has_s = unit_partials<kSchedSuffix>(ss, b, g, &sf, &sc);
-  const int L = ss.kv_indptr[b + 1] - ss.kv_indptr[b];
-  if (shared > 0 && L - shared < T - 1 && threadIdx.x == 0 && blockIdx.y == 0)
+  const int64_t shared = sched_shared<kSchedCascade>(sp);
+  const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+  if (L - shared < T - 1 && threadIdx.x == 0 && blockIdx.y == 0)
     atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
-  if (!has_s) {
-    sc = 0;
-    if (shared == 0 && L > 0) return;           // written directly by the decode kernel
-  }
-  const int v = b / prm.sp.gsize;
-  const int np = (qo0 - ss.qo_indptr[v * prm.sp.gsize]) * ss.H + rr;
-  if (shared > 0 && unit_partials<kSchedPrefix>(prm.sp, v, 0, &pf, &pc)) {
-    if (np >= prm.sp.NG || pf < 0 || pf + pc > prm.p_slots) {
-      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
-      return;
-    }
-  } else {
-    pc = 0;
-  }
-  if (sc > 0 && (sf < 0 || sf + sc > prm.s_slots)) {
+  const int VP = sched_prefix_units(sp);
+  const int v = b / sp.gsize;
+  const int np = (qo0 - sp.qo_indptr[v * sp.gsize]) * sp.H + rr;
+  int64_t pf = 0, sf = 0;
+  int pc = 0, sc = 0;
+  if (!unit_partials<kSchedCascade>(sp, v, 0, &pf, &pc)) pc = 0;
+  if (!unit_partials<kSchedCascade>(sp, VP + b, 0, &sf, &sc)) sc = 0;
+  if (np >= NG || rr >= NG || (pc > 0 && (pf < 0 || pf + pc > prm.n_slots)) ||
+      (sc > 0 && (sf < 0 || sf + sc > prm.n_slots))) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
     return;
   }
-  grid_dependency_wait();   // partials come from the decode kernels
+  grid_dependency_wait();   // partials come from the decode kernel
   MergeOut out;
   out.o = prm.o;
   out.o_fp32 = prm.o_fp32;
-  out.o_off = (r / ss.H) * prm.o_stride_tok + (r % ss.H) * prm.o_stride_head;
+  out.o_off = (r / sp.H) * prm.o_stride_tok + (r % sp.H) * prm.o_stride_head;
   out.lse = prm.lse_out ? prm.lse_out + r : nullptr;
-  const int pNG = prm.sp.NG;
   auto o_of = [&](int k) -> const float* {
-    return k < pc ? prm.p_o + ((pf + k) * pNG + np) * kDV
-                  : prm.s_o + ((sf + (k - pc)) * NGs + n) * kDV;
+    return k < pc ? prm.part_o + ((pf + k) * NG + np) * kDV
+                  : prm.part_o + ((sf + (k - pc)) * NG + rr) * kDV;
   };
   auto lse_of = [&](int k) -> float {
-    return k < pc ? prm.p_lse[(pf + k) * pNG + np] : prm.s_lse[(sf + (k - pc)) * NGs + n];
+    return k < pc ? prm.part_lse[(pf + k) * NG + np] : prm.part_lse[(sf + (k - pc)) * NG + rr];
   };
   merge_partials_block<P, U>(pc + sc, o_of, lse_of, out, col0);
 }

@@ -51,18 +51,18 @@ PMLA_HD inline int groups_for(int rows_per_request, int ng) {
 }
 
 // What a schedule covers.  kSchedWhole: every request's positions, as described above.
-// The two other modes split a batch whose requests share their first P cache positions
-// (the prefix-cache pattern of the captured concurrency-16/24 workloads:
-// "[Kimi-K3 MLA TP8] MLA performance" §1 "Environment" and §5.4):
-//  * kSchedPrefix: "virtual requests" v, each a group of gsize consecutive requests, attend
+// kSchedCascade serves a batch whose requests share their first P cache positions (the
+// prefix-cache pattern of the captured concurrency-16/24 workloads: "[Kimi-K3 MLA TP8]
+// MLA performance" §1 "Environment" and §5.4).  Its line holds two kinds of units:
+//  * v < VP: prefix units.  Unit v is a group of gsize consecutive requests attending
 //    positions [0, P) together.  Their query rows are consecutive in q (request-major), so
 //    a group is one MMA N-tile and each shared cache row is read once per group instead of
 //    once per request.  No causal masking: every query of the group sees the whole prefix.
-//  * kSchedSuffix: each request attends its own positions [P, L_b).
-// Both always write partials; the cascade merge combines the two per output row.  P comes
-// from the caller, who knows its prefix cache (mla_decode_shared_prefix); prefixes
-// shorter than kMinShared are not split off.
-enum : int { kSchedWhole = 0, kSchedPrefix = 1, kSchedSuffix = 2 };
+//  * v = VP + b: request b attending its own positions [P, L_b).
+// Every unit writes partials; the cascade merge combines each row's prefix and own parts.
+// P comes from the caller, who knows its prefix cache (mla_decode_shared_prefix);
+// prefixes shorter than kMinShared are not split off.
+enum : int { kSchedWhole = 0, kSchedCascade = 1 };
 constexpr int kMinShared = 1024;
 // The schedule functions take the mode as a template argument: a compile-time mode gives
 // the decode kernel only its own code path (the plain decode carries none of the cascade's
@@ -78,9 +78,9 @@ struct SchedParams {
   int groups;      // row groups per (virtual) request
   int splits;      // <= 0 auto, else fixed pieces per unit
   int grid;        // CTAs launched
-  int mode;        // kSchedWhole / kSchedPrefix / kSchedSuffix
-  int gsize;       // kSchedPrefix: requests per virtual request
-  int shared;      // kSchedPrefix / kSchedSuffix: the shared prefix length P
+  int mode;        // kSchedWhole / kSchedCascade
+  int gsize;       // kSchedCascade: requests per prefix unit
+  int shared;      // kSchedCascade: the shared prefix length P
 };
 
 struct Piece {
@@ -108,43 +108,68 @@ PMLA_HD inline int64_t sched_shared(const SchedParams& sp) {
   return P >= kMinShared ? P : 0;
 }
 
-// Number of (virtual) requests of a schedule.
-template <int MODE = kSchedAny>
-PMLA_HD inline int sched_requests(const SchedParams& sp) {
-  return sched_mode<MODE>(sp) == kSchedPrefix ? (sp.B + sp.gsize - 1) / sp.gsize : sp.B;
+// Prefix units of a cascade schedule.
+PMLA_HD inline int sched_prefix_units(const SchedParams& sp) {
+  return (sp.B + sp.gsize - 1) / sp.gsize;
 }
 
-// Positions of all (virtual) requests before v, and of v itself.
+// Number of units on the line (per row group).
+template <int MODE = kSchedAny>
+PMLA_HD inline int sched_requests(const SchedParams& sp) {
+  return sched_mode<MODE>(sp) == kSchedCascade ? sched_prefix_units(sp) + sp.B : sp.B;
+}
+
+// Positions of all units before v on the line, and of v itself.
 template <int MODE = kSchedAny>
 PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
-  const int mode = sched_mode<MODE>(sp);
-  if (mode == kSchedPrefix) return static_cast<int64_t>(v) * P;
-  return static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0] -
-         (mode == kSchedSuffix ? static_cast<int64_t>(v) * P : 0);
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    if (v <= VP) return static_cast<int64_t>(v) * P;
+    const int b = v - VP;
+    return static_cast<int64_t>(VP) * P + sp.kv_indptr[b] - sp.kv_indptr[0] -
+           static_cast<int64_t>(b) * P;
+  }
+  return static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0];
 }
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
-  const int mode = sched_mode<MODE>(sp);
-  if (mode == kSchedPrefix) return static_cast<int>(P);
-  return sp.kv_indptr[v + 1] - sp.kv_indptr[v] - (mode == kSchedSuffix ? static_cast<int>(P) : 0);
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    if (v < VP) return static_cast<int>(P);
+    return sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP] - static_cast<int>(P);
+  }
+  return sp.kv_indptr[v + 1] - sp.kv_indptr[v];
 }
-// First index-array entry and query tokens [qo0, qo1) of (virtual) request v.
+// First index-array entry, query tokens [qo0, qo1) and causal base of unit v.
 template <int MODE = kSchedAny>
 PMLA_HD inline int64_t sched_kv0(const SchedParams& sp, int64_t P, int v) {
-  const int mode = sched_mode<MODE>(sp);
-  if (mode == kSchedPrefix) return sp.kv_indptr[v * sp.gsize];
-  return static_cast<int64_t>(sp.kv_indptr[v]) + (mode == kSchedSuffix ? P : 0);
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    if (v < VP) return sp.kv_indptr[v * sp.gsize];
+    return static_cast<int64_t>(sp.kv_indptr[v - VP]) + P;
+  }
+  return sp.kv_indptr[v];
 }
 template <int MODE = kSchedAny>
 PMLA_HD inline void sched_tokens(const SchedParams& sp, int v, int* qo0, int* qo1) {
-  if (sched_mode<MODE>(sp) == kSchedPrefix) {
-    const int last = (v + 1) * sp.gsize < sp.B ? (v + 1) * sp.gsize : sp.B;
-    *qo0 = sp.qo_indptr[v * sp.gsize];
-    *qo1 = sp.qo_indptr[last];
-  } else {
-    *qo0 = sp.qo_indptr[v];
-    *qo1 = sp.qo_indptr[v + 1];
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    if (v < VP) {
+      const int last = (v + 1) * sp.gsize < sp.B ? (v + 1) * sp.gsize : sp.B;
+      *qo0 = sp.qo_indptr[v * sp.gsize];
+      *qo1 = sp.qo_indptr[last];
+      return;
+    }
+    v -= VP;
   }
+  *qo0 = sp.qo_indptr[v];
+  *qo1 = sp.qo_indptr[v + 1];
+}
+// Positions beyond cfrom + (token index) need the causal test; prefix units have none.
+template <int MODE = kSchedAny>
+PMLA_HD inline int sched_cfrom(const SchedParams& sp, int v, int L, int T) {
+  if (sched_mode<MODE>(sp) == kSchedCascade && v < sched_prefix_units(sp)) return L;
+  return L - T;
 }
 
 // Effective CTA count of the auto policy for a line of W positions.
@@ -163,11 +188,13 @@ PMLA_HD inline int auto_cta_of(int64_t x, int64_t W, int Gp) {
 // Largest v in [0, VB) with groups * cum(v) <= x.
 template <int MODE = kSchedAny>
 PMLA_HD inline int find_request(const SchedParams& sp, int64_t P, int VB, int64_t x) {
-  if (sched_mode<MODE>(sp) == kSchedPrefix) {
-    const int64_t v = x / (static_cast<int64_t>(sp.groups) * P);
-    return static_cast<int>(v < VB ? v : VB - 1);
-  }
   int lo = 0, hi = VB - 1;
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    const int64_t prefix_end = static_cast<int64_t>(sp.groups) * VP * P;
+    if (x < prefix_end) return static_cast<int>(x / (static_cast<int64_t>(sp.groups) * P));
+    lo = VP;
+  }
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
     if (static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, mid) <= x)
@@ -213,7 +240,6 @@ struct PieceIterT {
     p = p_end = 0;
     have_held = false;
     held = Piece{0, 0, 0, 0, 0, 0, 0, 0, 0, false, 0, 0};
-    if (sched_mode<MODE>(s) == kSchedPrefix && P == 0) return;   // nothing shared: no work
     if (sp.splits <= 0) {
       W = static_cast<int64_t>(sp.groups) * (VB > 0 ? sched_cum<MODE>(sp, P, VB) : 0);
       Gp = auto_ctas(W, sp.grid);
@@ -292,7 +318,7 @@ struct PieceIterT {
       int qo1 = 0;
       sched_tokens<MODE>(sp, pc.b, &pc.qo0, &qo1);
       pc.T = qo1 - pc.qo0;
-      pc.cfrom = sched_mode<MODE>(sp) == kSchedPrefix ? pc.L : pc.L - pc.T;
+      pc.cfrom = sched_cfrom<MODE>(sp, pc.b, pc.L, pc.T);
       const int rows_req = pc.T * sp.H;
       int rows = rows_req - pc.g * sp.NG;
       if (rows > sp.NG) rows = sp.NG;
@@ -322,7 +348,6 @@ PMLA_HD inline bool unit_partials(const SchedParams& sp, int v, int g, int64_t* 
                                   int* count) {
   const int64_t P = sched_shared<MODE>(sp);
   const int mode = sched_mode<MODE>(sp);
-  if (mode == kSchedPrefix && P == 0) return false;
   const int VB = sched_requests<MODE>(sp);
   const int L = sched_len<MODE>(sp, P, v);
   if (L <= 0) return false;

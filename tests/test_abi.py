@@ -75,11 +75,11 @@ def test_workspace_size_plan(lib):
 
 
 def test_shared_prefix_workspace_size(lib):
-    # plain partials + the prefix pass's: (ceil(B / 4) + SMs) slots of 48 rows
+    # the cascade's 48-row slots: ceil(B / 4) prefix units + B own units + SMs
     sz = lib.mla_get_shared_prefix_workspace_size(16, 12, 1, 152)
-    plain = lib.mla_get_workspace_size(16, 12, 1, 0, 152)
-    prefix = (4 + 152) * 48 * 513 * 4
-    assert plain + prefix <= sz < plain + prefix + 3 * 256
+    cascade = 256 + (4 + 16 + 152) * 48 * 513 * 4
+    assert cascade <= sz < cascade + 2 * 256
+    assert sz > lib.mla_get_workspace_size(16, 12, 1, 0, 152)
     # batches that never take the shared-prefix path need only the plain workspace
     for B, H, T in [(3, 12, 1), (1, 12, 1), (64, 12, 4), (16, 96, 1)]:
         assert (lib.mla_get_shared_prefix_workspace_size(B, H, T, 152) ==

@@ -192,87 +192,58 @@ def cascade_partials(sim, kvp, qop, B, H, NG, groups, grid, mode, gsize, shared,
 
 
 def check_cascade(sim, kv_lens, q_lens, H, grid, shared):
-    """Prefix pass (groups of gsize requests over [0, P)) + suffix pass (each request over
-    [P, L)) attend every (request, query row, position) exactly once, with unique partial
-    slots, the index base of each piece at the right entry, causal limits only in the
-    suffix, and the merge's slot ranges matching what the passes wrote."""
+    """The cascade line (prefix units: groups of gsize requests over [0, P); own units:
+    each request over [P, L)) attends every (request, query row, position) exactly once,
+    with unique partial slots, each piece's index base at the right entry, causal limits
+    only on own units, and the merge's slot ranges matching what the decode wrote."""
     B = len(kv_lens)
     kvp = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
     qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     rows = max(q_lens) * H
-    NG = pick_ng(rows)
-    groups = (rows + NG - 1) // NG
     gsize = 48 // rows
-    P = shared if shared >= MIN_SHARED else 0
-    VB = (B + gsize - 1) // gsize
-    pre = cascade_pieces(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared)
-    suf = cascade_pieces(sim, kvp, qop, B, H, NG, groups, grid, 2, gsize, shared)
-    n_pslots = sim.sched_partial_slots(VB, 1, 0, grid)
-    n_sslots = sim.sched_partial_slots(B, groups, 0, grid)
-    if P == 0:
-        assert len(pre) == 0
-    # prefix: exact cover of [0, P) per virtual request, all partials
+    P = shared
+    VP = (B + gsize - 1) // gsize
+    pieces = cascade_pieces(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared)
+    n_slots = sim.sched_partial_slots(VP + B, 1, 0, grid)
     cover = {}
-    for cta, v, g, j0, j1, prow, slot, direct, kv0, cfrom in pre:
-        assert g == 0 and not direct and 0 <= slot < n_pslots
-        first_b = v * gsize
-        last_b = min(first_b + gsize, B)
-        assert kv0 == kvp[first_b] and cfrom == P
-        assert prow == (qop[last_b] - qop[first_b]) * H
+    for cta, v, g, j0, j1, prow, slot, direct, kv0, cfrom in pieces:
+        assert g == 0 and not direct and 0 <= slot < n_slots
+        if v < VP:
+            first_b, last_b = v * gsize, min(v * gsize + gsize, B)
+            assert kv0 == kvp[first_b] and cfrom == P and j1 <= P
+            assert prow == (qop[last_b] - qop[first_b]) * H
+        else:
+            b = v - VP
+            Ls = kv_lens[b] - P
+            assert kv0 == kvp[b] + P and cfrom == Ls - q_lens[b] and j1 <= Ls
+            assert prow == q_lens[b] * H
         cover.setdefault(v, []).append((j0, j1, slot))
-    slots = [p[6] for p in pre]
-    assert len(slots) == len(set(slots))
-    for v in range(VB if P else 0):
-        ps = sorted(cover[v])
+    slots = [p[6] for p in pieces]
+    assert len(slots) == len(set(slots)), "partial slot written twice"
+    for v in range(VP + B):
+        L = P if v < VP else kv_lens[v - VP] - P
+        ps = sorted(cover.get(v, []))
         pos = 0
         for j0, j1, _ in ps:
-            assert j0 == pos
+            assert j0 == pos, f"gap/overlap in unit {v}"
             pos = j1
-        assert pos == P
-        need, first, count = cascade_partials(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared, v, 0)
-        assert need == 1 and {p[2] for p in ps} == set(range(first, first + count))
-    # suffix: exact cover of [P, L) per unit
-    by_unit = {}
-    for cta, b, g, j0, j1, prow, slot, direct, kv0, cfrom in suf:
-        Ls = kv_lens[b] - P
-        assert 0 <= j0 < j1 <= Ls and kv0 == kvp[b] + P and cfrom == Ls - q_lens[b]
-        assert prow == min(NG, q_lens[b] * H - g * NG)
-        if P:
-            assert not direct
-        by_unit.setdefault((b, g), []).append((j0, j1, slot, direct))
-    sslots = [p[6] for p in suf if not p[7]]
-    assert len(sslots) == len(set(sslots)) and all(0 <= s < n_sslots for s in sslots)
-    for b in range(B):
-        for g in range(groups):
-            if q_lens[b] * H - g * NG <= 0:
-                continue
-            ps = sorted(by_unit.get((b, g), []))
-            Ls = kv_lens[b] - P
-            pos = 0
-            for j0, j1, *_ in ps:
-                assert j0 == pos
-                pos = j1
-            assert pos == max(Ls, 0)
-            need, first, count = cascade_partials(sim, kvp, qop, B, H, NG, groups, grid, 2, gsize,
-                                                  shared, b, g)
-            if Ls <= 0:
-                assert need == 0
-            elif len(ps) == 1 and ps[0][3]:
-                assert need == 0 and P == 0
-            else:
-                assert need == 1 and {p[2] for p in ps} == set(range(first, first + count))
+        assert pos == max(L, 0)
+        need, first, count = cascade_partials(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared,
+                                              v, 0)
+        if L <= 0:
+            assert need == 0
+        else:
+            assert need == 1 and {p[2] for p in ps} == set(range(first, first + count))
 
 
 CASCADE_CASES = [
-    # (kv_lens, q_lens, H, shared prefix length the device would find)
+    # (kv_lens, q_lens, H, shared prefix length the caller declares; >= 1024)
     ([68000] * 16, [1] * 16, 12, 63911),
     ([68000 + 37 * i for i in range(24)], [1] * 24, 12, 63911),
-    ([5000, 5000, 7000], [1, 1, 1], 12, 4000),           # 3 requests: one group of 3
-    ([3000] * 5, [1] * 5, 12, 3000),                      # whole requests shared: empty suffixes
+    ([5000, 5000, 7000, 6000, 5500], [1] * 5, 12, 4000),  # two groups (4 + 1)
+    ([3000] * 5, [1] * 5, 12, 3000),                      # whole requests shared: no own units
     ([3000, 2500, 4000, 2200, 2600], [1] * 5, 12, 2200),  # one request ends with the prefix
     ([9000] * 4, [2] * 4, 12, 8999),                      # two queries per request
-    ([2000] * 6, [1] * 6, 12, 100),                       # short prefix: not split off
-    ([2000] * 6, [1] * 6, 12, 0),
     ([12000] * 7, [1] * 7, 8, 5000),                      # 8 heads: groups of 6 requests
 ]
 
