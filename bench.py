@@ -70,14 +70,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(config: str):
-    """dram bytes per decode call from a committed ncu summary, if it matches this kernel."""
+def recorded_traffic(config: str, entry: str):
+    """dram bytes per decode launch from a committed ncu summary, if it matches this kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(config)
+    e = d.get(config if entry == "plain" else f"{config}+{entry}")
     if not e or e.get("kernel_source_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_call")
@@ -406,7 +406,7 @@ def main():
             raise RuntimeError(f"device error in the plain timing: {pm.mla_status_string(st)}")
 
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
-    algo = mla_inputs.algorithmic_bytes(case)
+    algo = mla_inputs.algorithmic_bytes(case, shared if entry == "shared_prefix" else 0)
     value = whole_job_rate(world, gathered, mean_ms)
     peak, peak_kind = measured_peaks()
     achieved = algo / (mean_ms * 1e-3) / 1e9
@@ -472,15 +472,22 @@ def main():
                              if not args.no_l2_flush else "not flushed",
                        "parallelism": f"{world} independent replicas (one batch per GPU)"},
             "roofline": {"bound": "hbm",
-                         "kernel": ("mla_decode_shared_prefix call (prefix + suffix decode, merge)"
+                         "kernel": ("mla_decode_shared_prefix call (one cascade decode launch: prefix "
+                                    "units then per-request units, then the cascade merge)"
                                     if entry == "shared_prefix" else
                                     "mla_decode call (decode + merge kernels)"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                         "traffic": recorded_traffic(args.config)},
+                         "traffic": recorded_traffic(args.config, entry),
+                         "bytes_counted": ("each distinct cache row once (the shared prefix's rows "
+                                           "once for the whole batch), 580 B per row with its "
+                                           "index, plus q, o and lse"
+                                           if entry == "shared_prefix" else
+                                           "580 B per attended position (row + index), plus q, "
+                                           "o and lse")},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
-            "gpu_launches": (4 if entry == "shared_prefix" else 2) * args.steps,
+            "gpu_launches": 2 * args.steps,
             "plain_call": plain,
             "clocks": dict(clocks.summary(),
                            window=("the timed region" if soak == 0 else

@@ -257,10 +257,15 @@ def gathered_kv_bytes(kv_lens) -> int:
     return D * int(sum(kv_lens))
 
 
-def algorithmic_bytes(case: Case) -> int:
-    """Cache rows + 4-byte indices + q in + o out (bf16) + lse out (fp32)."""
+def algorithmic_bytes(case: Case, shared_prefix: int = 0) -> int:
+    """Cache rows + 4-byte indices + q in + o out (bf16) + lse out (fp32).
+
+    With ``shared_prefix`` = P > 0 the first P positions of every request name the same
+    rows, so a call that is told so needs each of those rows (and its index) once.
+    """
     n_rows = int(sum(case.q_lens)) * case.H
-    return (580 * case.total_kv + n_rows * D + n_rows * DV * 2 + n_rows * 4)
+    positions = case.total_kv - (case.B - 1) * shared_prefix if shared_prefix > 0 else case.total_kv
+    return (580 * positions + n_rows * D + n_rows * DV * 2 + n_rows * 4)
 
 
 def useful_flops(kv_lens, q_lens, H: int) -> int:

@@ -241,14 +241,15 @@ void* merge_fn(const MergeShape& ms) {
     case 16: return u8 ? K<16, 8>::fn() : K<16, 4>::fn();
     case 8: return u8 ? K<8, 8>::fn() : K<8, 4>::fn();
     case 4: return u8 ? K<4, 8>::fn() : K<4, 4>::fn();
-    default: return u8 ? K<2, 8>::fn() : K<2, 4>::fn();
+    case 2: return u8 ? K<2, 8>::fn() : K<2, 4>::fn();
+    default: return K<1, 2>::fn();
   }
 }
 
 template <template <int, int> class K, class Params>
 cudaError_t launch_merge(const MergeShape& ms, int64_t n_rows, const Params& mp, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_rows), ms.lanes / 2);
+  cfg.gridDim = dim3(static_cast<unsigned>(merge_blocks_x(ms, n_rows)), ms.lanes > 1 ? ms.lanes / 2 : 1);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -296,10 +297,12 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
   const int B = prm.sp.B;
+  mp.n_merge_rows = static_cast<int64_t>(B) * max_rows;
   const int VP = (B + plan.gsize - 1) / plan.gsize;
   const int64_t n_rows = static_cast<int64_t>(B) * max_rows;
   // partials per row: the CTAs one prefix unit spans plus those of the request's own unit
-  const MergeShape ms = merge_shape_for(plan.grid / VP + plan.grid / B + 4, n_rows, plan.grid);
+  // (the shape counts the rows that do work: q_rows <= n_rows)
+  const MergeShape ms = merge_shape_for(plan.grid / VP + plan.grid / B + 4, q_rows, plan.grid);
   const cudaError_t e = launch_merge<CascadeMergeK>(ms, n_rows, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -401,8 +404,9 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   mp.n_q_rows = q_rows;
   mp.err = prm.err;
   const int64_t units = static_cast<int64_t>(cs.B) * plan.groups;
-  const MergeShape ms = merge_shape_for(units > 0 ? plan.slots / units : 1, units * plan.NG,
-                                        plan.grid);
+  mp.n_merge_rows = units * plan.NG;
+  // (rows past a group's real rows return at once: the shape counts the q_rows that work)
+  const MergeShape ms = merge_shape_for(units > 0 ? plan.slots / units : 1, q_rows, plan.grid);
   const cudaError_t e = launch_merge<SplitMergeK>(ms, units * plan.NG, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

@@ -25,12 +25,16 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeBlocksPerSm = 3;   // launch bound: registers for 3 resident blocks
 constexpr int kMergeWarps = kMergeThreads / 32;
 
-// Merge launch shape for n_rows merged rows of ~per_row partials each: P partial lanes
-// (2 .. 64; a block covers 1024 / P columns, 2 = a whole 512-column row) with U loads in
-// flight per lane.  P is the smallest power of two leaving each lane one round of U loads.
-// A grid within two waves of resident blocks keeps U = 4 (more, lighter blocks); a larger
-// one takes U = 8 when that halves the lanes (half the blocks, each paying its set-up
-// latency once).
+// Merge launch shape for n_rows merged rows of ~per_row partials each.
+//   lanes >= 2: one row per block, P = lanes partial lanes (a block covers 1024 / P
+//               columns, 2 = a whole 512-column row) with U = unroll loads in flight;
+//   lanes == 1: one row per warp (eight per block), each lane folding all of the row's
+//               partials for its 16 columns.
+// Every merge block pays a fixed latency (row lookup, the wait for the decode grid, one
+// round of loads, the combine), so the shape aims at one wave of resident blocks: P is the
+// smallest power of two giving each lane one round of U = 4 loads, halved while the grid
+// exceeds a wave (U = 8 where a lane then has more than four loads); rows too many for one
+// block each, with few partials, take a warp each.
 struct MergeShape {
   int lanes, unroll;
 };
@@ -40,11 +44,16 @@ inline int merge_lanes_for(int64_t per_row, int unroll) {
   return lanes;
 }
 inline MergeShape merge_shape_for(int64_t per_row, int64_t n_rows, int sms) {
-  const int l4 = merge_lanes_for(per_row, 4);
-  const int l8 = merge_lanes_for(per_row, 8);
-  if (l8 == l4 || n_rows * (l4 / 2) <= 2 * static_cast<int64_t>(sms) * kMergeBlocksPerSm)
-    return {l4, 4};
-  return {l8, 8};
+  // n_rows: the merged rows that do work (padding rows of a row group return at once)
+  const int64_t wave = static_cast<int64_t>(sms) * kMergeBlocksPerSm;
+  if (n_rows > wave && per_row <= 16) return {1, 2};
+  int lanes = merge_lanes_for(per_row, 4);
+  while (lanes > 2 && n_rows * (lanes / 2) > wave) lanes /= 2;
+  return {lanes, lanes * 4 >= per_row ? 4 : 8};
+}
+// Blocks along x for n_rows merged rows.
+inline int64_t merge_blocks_x(const MergeShape& ms, int64_t n_rows) {
+  return ms.lanes == 1 ? (n_rows + kMergeWarps - 1) / kMergeWarps : n_rows;
 }
 
 
@@ -158,6 +167,76 @@ __device__ void merge_partials_block(int count, OOf o_of, LseOf lse_of, const Me
   }
 }
 
+// Merge `count` partials of one (row, head) with one warp: lane l owns columns
+// 128 j + 4 l .. 128 j + 4 l + 3 (j = 0..3), so each load and store instruction of the warp
+// covers 512 contiguous bytes of fp32 (256 of bf16).  All of a row's columns share one max
+// and one weight sum, so the exponentials are taken once per partial.
+template <int U, class OOf, class LseOf>
+__device__ void merge_row_warp(int count, OOf o_of, LseOf lse_of, const MergeOut& out) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY, w = 0.f;
+  float4 a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < count; k0 += U) {
+    float l[U];
+    float4 v[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = k0 + u;
+      l[u] = (k < count) ? lse_of(k) : -INFINITY;
+      const float* src = (k < count) ? o_of(k) : nullptr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[u][j] = (k < count) ? *reinterpret_cast<const float4*>(src + 128 * j + 4 * lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (l[u] == -INFINITY) continue;
+      const float M = fmaxf(m, l[u]);
+      const float f1 = (m == -INFINITY) ? 0.f : __expf(m - M);
+      const float f2 = __expf(l[u] - M);
+      w = w * f1 + f2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        a[j].x = a[j].x * f1 + v[u][j].x * f2;
+        a[j].y = a[j].y * f1 + v[u][j].y * f2;
+        a[j].z = a[j].z * f1 + v[u][j].z * f2;
+        a[j].w = a[j].w * f1 + v[u][j].w * f2;
+      }
+      m = M;
+    }
+  }
+  const float inv = (m == -INFINITY) ? 0.f : 1.f / w;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 r = make_float4(a[j].x * inv, a[j].y * inv, a[j].z * inv, a[j].w * inv);
+    const int64_t off = out.o_off + 128 * j + 4 * lane;
+    if (out.o_fp32) {
+      float* d = reinterpret_cast<float*>(out.o) + off;
+      if ((reinterpret_cast<uintptr_t>(d) & 15) == 0) {
+        *reinterpret_cast<float4*>(d) = r;
+      } else {
+        d[0] = r.x; d[1] = r.y; d[2] = r.z; d[3] = r.w;
+      }
+    } else {
+      __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(out.o) + off;
+      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(r.x, r.y);
+      const __nv_bfloat162 hi2 = __floats2bfloat162_rn(r.z, r.w);
+      if ((reinterpret_cast<uintptr_t>(d) & 7) == 0) {
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(d) = pk;
+      } else {
+        d[0] = lo2.x; d[1] = lo2.y; d[2] = hi2.x; d[3] = hi2.y;
+      }
+    }
+  }
+  if (lane == 0 && out.lse != nullptr) *out.lse = (m == -INFINITY) ? -INFINITY : m + __logf(w);
+}
+
 // Wait until the grid this one depends on (launched before it on the stream with
 // programmatic serialization) has completed and its writes are visible.
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -174,28 +253,34 @@ struct SplitMergeParams {
   int64_t o_stride_tok, o_stride_head;
   float* lse_out;
   int64_t n_q_rows;
+  int64_t n_merge_rows;    // units * NG
   int* err;
 };
 
-// grid = (units * NG, P / 2), block = 256.  Merges the units the scheduler split and writes
+// grid = (merge_blocks_x(units * NG), P / 2), block = 256.  Merges the units the scheduler split and writes
 // o = 0, lse = -inf for requests with no cache positions.  Units that ran whole on one
 // CTA were written by the decode kernel and are skipped here.
 template <int P, int U>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_merge_kernel(const SplitMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
-  const int64_t u = blockIdx.x / NG;
-  const int n = static_cast<int>(blockIdx.x - u * NG);
+  // P = 1: merged row = warp (eight per block); else merged row = block
+  const int64_t mrow = P == 1 ? static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5)
+                              : static_cast<int64_t>(blockIdx.x);
+  const bool lead = P == 1 ? (threadIdx.x & 31) == 0 : (threadIdx.x == 0 && blockIdx.y == 0);
+  if (mrow >= prm.n_merge_rows) return;
+  const int64_t u = mrow / NG;
+  const int n = static_cast<int>(mrow - u * NG);
   const int b = static_cast<int>(u / sp.groups);
   const int g = static_cast<int>(u - static_cast<int64_t>(b) * sp.groups);
-  const int col0 = blockIdx.y * (4 * kMergeThreads / P);
+  const int col0 = P == 1 ? 0 : blockIdx.y * (4 * kMergeThreads / P);
   const int T = sp.qo_indptr[b + 1] - sp.qo_indptr[b];
   const int rows = T * sp.H - g * NG;
   if (n >= rows || n >= NG) return;
   const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
   const int64_t r = static_cast<int64_t>(sp.qo_indptr[b]) * sp.H + static_cast<int64_t>(g) * NG + n;
   if (r < 0 || r >= prm.n_q_rows) {
-    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeRow);
+    if (lead) atomicOr(prm.err, kErrMergeRow);
     return;
   }
   MergeOut out;
@@ -209,7 +294,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
   if (L > 0) {
     if (!unit_partials<kSchedWhole>(sp, b, g, &first, &count)) return;   // written directly by its CTA
     if (first < 0 || first + count > prm.n_slots) {
-      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
+      if (lead) atomicOr(prm.err, kErrMergeSlot);
       return;
     }
   }
@@ -225,7 +310,10 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
     }
     return prm.part_lse[(first + k) * NG + n];
   };
-  merge_partials_block<P, U>(count, o_of, lse_of, out, col0);
+  if constexpr (P == 1)
+    merge_row_warp<U>(count, o_of, lse_of, out);
+  else
+    merge_partials_block<P, U>(count, o_of, lse_of, out, col0);
 }
 
 // ---------------------------------------------------------------- shared-prefix cascade
@@ -241,30 +329,35 @@ struct CascadeMergeParams {
   int64_t o_stride_tok, o_stride_head;
   float* lse_out;
   int64_t n_q_rows;
+  int64_t n_merge_rows;    // B * rows_per_req
   int* err;
 };
 
-// grid = (B * rows_per_req, P / 2), block = 256.  Row rr of request b merges the partials
+// grid = (merge_blocks_x(B * rows_per_req), P / 2), block = 256.  Row rr of request b merges the partials
 // of its group's prefix unit (at row (qo_b - qo_group) H + rr of the group's rows) with
 // those of its own unit (row rr).
 template <int P, int U>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
-  const int b = static_cast<int>(blockIdx.x / prm.rows_per_req);
-  const int rr = static_cast<int>(blockIdx.x - static_cast<int64_t>(b) * prm.rows_per_req);
-  const int col0 = blockIdx.y * (4 * kMergeThreads / P);
+  const int64_t mrow = P == 1 ? static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5)
+                              : static_cast<int64_t>(blockIdx.x);
+  const bool lead = P == 1 ? (threadIdx.x & 31) == 0 : (threadIdx.x == 0 && blockIdx.y == 0);
+  if (mrow >= prm.n_merge_rows) return;
+  const int b = static_cast<int>(mrow / prm.rows_per_req);
+  const int rr = static_cast<int>(mrow - static_cast<int64_t>(b) * prm.rows_per_req);
+  const int col0 = P == 1 ? 0 : blockIdx.y * (4 * kMergeThreads / P);
   const int qo0 = sp.qo_indptr[b];
   const int T = sp.qo_indptr[b + 1] - qo0;
   if (rr >= T * sp.H) return;
   const int64_t r = static_cast<int64_t>(qo0) * sp.H + rr;
   if (r < 0 || r >= prm.n_q_rows) {
-    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeRow);
+    if (lead) atomicOr(prm.err, kErrMergeRow);
     return;
   }
   const int64_t shared = sched_shared<kSchedCascade>(sp);
   const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
-  if (L - shared < T - 1 && threadIdx.x == 0 && blockIdx.y == 0)
+  if (L - shared < T - 1 && lead)
     atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
   const int VP = sched_prefix_units(sp);
   const int v = b / sp.gsize;
@@ -275,7 +368,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
   if (!unit_partials<kSchedCascade>(sp, VP + b, 0, &sf, &sc)) sc = 0;
   if (np >= NG || rr >= NG || (pc > 0 && (pf < 0 || pf + pc > prm.n_slots)) ||
       (sc > 0 && (sf < 0 || sf + sc > prm.n_slots))) {
-    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(prm.err, kErrMergeSlot);
+    if (lead) atomicOr(prm.err, kErrMergeSlot);
     return;
   }
   grid_dependency_wait();   // partials come from the decode kernel
@@ -291,7 +384,10 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
   auto lse_of = [&](int k) -> float {
     return k < pc ? prm.part_lse[(pf + k) * NG + np] : prm.part_lse[(sf + (k - pc)) * NG + rr];
   };
-  merge_partials_block<P, U>(pc + sc, o_of, lse_of, out, col0);
+  if constexpr (P == 1)
+    merge_row_warp<U>(pc + sc, o_of, lse_of, out);
+  else
+    merge_partials_block<P, U>(pc + sc, o_of, lse_of, out, col0);
 }
 
 struct CsrMergeParams {

@@ -77,3 +77,15 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_algorithmic_bytes_count_distinct_rows_under_a_shared_prefix():
+    import mla_inputs
+    case = mla_inputs.make_custom([300, 410, 257, 1200], q_lens=[1, 2, 1, 3], H=12,
+                                  shared_prefix=256, seed=3)
+    used = case.kv_indices[:case.total_kv]
+    distinct = int(used.unique().numel())
+    rows = sum(case.q_lens) * case.H
+    rest = rows * (576 + 1024 + 4)
+    assert mla_inputs.algorithmic_bytes(case) == 580 * case.total_kv + rest
+    assert mla_inputs.algorithmic_bytes(case, 256) == 580 * distinct + rest

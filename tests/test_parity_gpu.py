@@ -84,6 +84,52 @@ def test_output_row_strides(pm, dtype, width):
         assert bool((base[:, :, 512:] == 7.0).all()), "write past the row's 512 columns"
 
 
+def _many_rows_case():
+    # 64 requests x 4 drafts x 12 heads = 3,072 merged rows; ~10 tiles each over 152 CTAs
+    # gives each row ~3 partials, so the merge runs one warp per row
+    rng = np.random.default_rng(41)
+    kv_lens = [int(x) for x in rng.integers(900, 1600, size=64)]
+    return gu.to_device(mla_inputs.make_custom(kv_lens, q_lens=[4] * 64, H=12, seed=41,
+                                               q_scale=1.0, kv_scale=1.0, name="rows"))
+
+
+@pytest.mark.parametrize("dtype,width,with_lse", [(torch.bfloat16, 512, True),
+                                                   (torch.bfloat16, 516, False),
+                                                   (torch.float32, 512, True),
+                                                   (torch.float32, 514, True)])
+def test_many_rows_few_partials(pm, dtype, width, with_lse):
+    """Thousands of merged rows with a few partials each (the warp-per-row merge): aligned
+    and unaligned o rows, bf16 and fp32, with and without lse."""
+    case = _many_rows_case()
+    n_tok = case.q.shape[0]
+    base = torch.full((n_tok, 12, width), 7.0, dtype=dtype, device="cuda")
+    o = base[:, :, :512]
+    lse = torch.empty((n_tok, 12), dtype=torch.float32, device="cuda") if with_lse else None
+    ws = pm.make_workspace(case.B, 12, case.max_seqlen_q, 0, "cuda")
+    pm.mla_decode(case.q, case.kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                  case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale, case.q_scale,
+                  case.kv_scale, lse_out=lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert pm.mla_check_error(ws) == 0
+    o_ref, lse_ref = gu.run_oracle(case)
+    gu.compare(o, lse, o_ref, lse_ref if with_lse else None, what=f"rows {dtype} {width}")
+    assert bool((base[:, :, 512:] == 7.0).all()), "write past the row's 512 columns"
+
+
+def test_shared_prefix_cascade_many_requests(pm):
+    """64 requests of one shared prefix: 768 merged rows with ~15 partials each, merged one
+    warp per row."""
+    rng = np.random.default_rng(42)
+    lens = [1100 + int(x) for x in rng.integers(0, 300, size=64)]
+    case = gu.to_device(mla_inputs.make_custom(lens, H=12, seed=42, shared_prefix=1024,
+                                               q_scale=1.0, kv_scale=1.0, poison=True,
+                                               index_buffer=sum(lens) + 64, name="c64"))
+    o, lse, status = gu.run_gpu(case, shared_prefix=1024)
+    assert status == 0, f"device error {status}"
+    o_ref, lse_ref = gu.run_oracle(case)
+    gu.compare(o, lse, o_ref, lse_ref, what="cascade, 64 requests")
+
+
 @pytest.mark.parametrize("H", [16, 24, 40, 96])
 def test_head_counts(pm, H):
     """16 -> one 16-row group, 24 -> 32-row group, 40 -> 48-row group, 96 -> two 48-row groups."""
@@ -123,8 +169,8 @@ def test_shared_prefix(pm):
 @pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
 def test_shared_prefix_cascade(pm, kv_lens, q_lens, prefix, scales):
     """mla_decode_shared_prefix: the shared rows are attended in groups of requests (prefix
-    pass), each request's own rows separately (suffix pass), and the halves merged; the
-    result must equal the oracle.  Unattended rows are poisoned."""
+    units), each request's own rows separately (own units, same launch), and the two
+    merged; the result must equal the oracle.  Unattended rows are poisoned."""
     case = gu.to_device(mla_inputs.make_custom(kv_lens, q_lens=q_lens, H=12, seed=31,
                                                shared_prefix=prefix, q_scale=scales[0],
                                                kv_scale=scales[1], poison=True,
