@@ -278,6 +278,7 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   pp.sp.groups = 1;
   pp.sp.gsize = plan.gsize;
   pp.sp.shared = shared;
+  sched_set_costs(&pp.sp, max_rows);
   pp.part_lse = reinterpret_cast<float*>(ws + plan.plse_off);
   pp.part_o = reinterpret_cast<float*>(ws + plan.po_off);
   pp.n_slots = plan.pslots;
@@ -356,6 +357,7 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   prm.sp.mode = kSchedWhole;
   prm.sp.gsize = 1;
   prm.sp.shared = 0;
+  sched_set_costs(&prm.sp, static_cast<int>(cs.H) * max_seqlen_q);
   prm.kv = static_cast<const uint8_t*>(kv_buffer->ptr);
   prm.kv_pitch = cs.kv_pitch;
   prm.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);

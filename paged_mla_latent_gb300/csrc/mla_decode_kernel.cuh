@@ -441,10 +441,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
         if (t == nt - 1) {
           // ------------------------------------------------ piece epilogue
-          mbar_wait(mbase + kMiscPv + 8 * (it_g & 1), (it_g >> 1) & 1, abort_flag, prm.err);
-          tc_fence_after();
+          // The row sums and the per-row set-up need only the softmax state: they run while
+          // the piece's last PV is still in the tensor pipe; the output waits for it.
 #pragma unroll
           for (int ch = 0; ch < NG / 16; ++ch) {
+            if (ch > 0 && 16 * ch >= pc.rows) break;   // no real rows left
             float v[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = l_acc[16 * ch + k];
@@ -487,6 +488,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             s_off[n] = off;
           }
           bar_sync(1, 128);
+          mbar_wait(mbase + kMiscPv + 8 * (it_g & 1), (it_g >> 1) & 1, abort_flag, prm.err);
+          tc_fence_after();
           // normalised output.  TMEM lane = value column: a warp holds 32 adjacent columns
           // of every row.  Lanes exchange values (in-register transposes) so that each
           // writes 16 contiguous bytes of one row: 8 bf16 columns (rows i, i + 8 of the

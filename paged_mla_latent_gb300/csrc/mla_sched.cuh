@@ -11,13 +11,15 @@
 // N-tile and attends all L_b positions of its request.
 //
 // Two policies:
-//  * auto (num_kv_splits <= 0): the units are laid end to end in a "global position"
-//    line of length W = groups * (kv_indptr[B] - kv_indptr[0]) and CTA i of Gp takes
-//    [floor(i W / Gp), floor((i+1) W / Gp)).  Every CTA gets the same number of cache
-//    rows regardless of how lengths are distributed (batch 1 with a 142K history fills
-//    every SM; 16 requests of 68K split ~10 ways each).  The piece of unit u on CTA i
-//    writes partial slot i + u (unique: see unit_partials).  A unit lying on one CTA is
-//    written directly, with no merge.
+//  * auto (num_kv_splits <= 0): the units are laid end to end on a cost line and CTA i of
+//    Gp takes [floor(i W / Gp), floor((i+1) W / Gp)) of its length W.  Each (unit, row
+//    group) occupies e + w L: a fixed cost e for the piece's set-up and epilogue, then w
+//    per position.  Every CTA thus gets the same estimated time regardless of how
+//    lengths are distributed (batch 1 with a 142K history fills every SM; 16 requests of
+//    68K split ~10 ways each), and a CTA whose range crosses into another unit gets fewer
+//    positions for the extra piece.  The piece of unit u on CTA i writes partial slot
+//    i + u (unique: see unit_partials).  A unit lying on one CTA is written directly,
+//    with no merge.
 //  * fixed (num_kv_splits = k >= 1): unit u is cut into k equal pieces p = u*k + j,
 //    CTA i runs pieces i, i + grid, ...; partial slot = p; k = 1 writes directly.
 #pragma once
@@ -81,7 +83,28 @@ struct SchedParams {
   int mode;        // kSchedWhole / kSchedCascade
   int gsize;       // kSchedCascade: requests per prefix unit
   int shared;      // kSchedCascade: the shared prefix length P
+  // Cost line of the auto policy (0 reads as 1, as w_own, as 0 respectively):
+  int w_own;       // per position of a request's (own) positions
+  int w_prefix;    // kSchedCascade: per position of a prefix unit
+  int piece_cost;  // per (unit, row group): set-up and epilogue of a piece
 };
+
+// Cost-line weights.  A piece's fixed cost (the epilogue writing NG x 512 values, the
+// pipeline's refill) measured about 2.3 tiles' time on every variant; a 48-row prefix
+// tile (three 16-row softmax chunks) about 1.3 times a 12-row own tile (one chunk), the
+// tile's time modelled as 23 + 4 per chunk.
+constexpr int kPieceCostPositions = 288;
+PMLA_HD inline int chunk_weight(int rows) { return 23 + 4 * ((rows + 15) / 16); }
+inline void sched_set_costs(SchedParams* sp, int rows_per_request) {
+  if (sp->mode == kSchedCascade) {
+    sp->w_own = chunk_weight(rows_per_request < sp->NG ? rows_per_request : sp->NG);
+    sp->w_prefix = chunk_weight(sp->NG);
+  } else {
+    sp->w_own = 1;
+    sp->w_prefix = 0;
+  }
+  sp->piece_cost = kPieceCostPositions * sp->w_own;
+}
 
 struct Piece {
   int b, g;        // (virtual) request, row group
@@ -119,7 +142,7 @@ PMLA_HD inline int sched_requests(const SchedParams& sp) {
   return sched_mode<MODE>(sp) == kSchedCascade ? sched_prefix_units(sp) + sp.B : sp.B;
 }
 
-// Positions of all units before v on the line, and of v itself.
+// Cache positions of all units before v (per row group), and of v itself.
 template <int MODE = kSchedAny>
 PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
   if (sched_mode<MODE>(sp) == kSchedCascade) {
@@ -140,6 +163,45 @@ PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
   }
   return sp.kv_indptr[v + 1] - sp.kv_indptr[v];
 }
+// Cost-line weights of unit v and the fixed cost of a (unit, row group).
+PMLA_HD inline int64_t sched_w_own(const SchedParams& sp) {
+  return sp.w_own > 0 ? sp.w_own : 1;
+}
+template <int MODE = kSchedAny>
+PMLA_HD inline int64_t sched_weight(const SchedParams& sp, int v) {
+  if (sched_mode<MODE>(sp) == kSchedCascade && v < sched_prefix_units(sp))
+    return sp.w_prefix > 0 ? sp.w_prefix : sched_w_own(sp);
+  return sched_w_own(sp);
+}
+PMLA_HD inline int64_t sched_piece_cost(const SchedParams& sp) {
+  return sp.piece_cost > 0 ? sp.piece_cost : 0;
+}
+// Cost-line start of unit v (per row group): the units before it, each e + w L.
+template <int MODE = kSchedAny>
+PMLA_HD inline int64_t sched_line(const SchedParams& sp, int64_t P, int v) {
+  const int64_t e = sched_piece_cost(sp);
+  const int64_t wo = sched_w_own(sp);
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    const int64_t unit_p = e + sched_weight<MODE>(sp, 0) * P;
+    if (v <= VP) return static_cast<int64_t>(v) * unit_p;
+    const int b = v - VP;
+    return static_cast<int64_t>(VP) * unit_p + static_cast<int64_t>(b) * e +
+           wo * (static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0] -
+                 static_cast<int64_t>(b) * P);
+  }
+  return static_cast<int64_t>(v) * e +
+         wo * (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]);
+}
+// Positions [0, L) of a (unit, row group) whose line segment starts d before line point
+// x: position j sits at line point e + w j of the segment; returns how many positions lie
+// before x.
+PMLA_HD inline int line_positions(int64_t d, int64_t e, int64_t w, int L) {
+  if (d <= e) return 0;
+  const int64_t n = (d - e + w - 1) / w;
+  return n < L ? static_cast<int>(n) : L;
+}
+
 // First index-array entry, query tokens [qo0, qo1) and causal base of unit v.
 template <int MODE = kSchedAny>
 PMLA_HD inline int64_t sched_kv0(const SchedParams& sp, int64_t P, int v) {
@@ -185,19 +247,20 @@ PMLA_HD inline int auto_cta_of(int64_t x, int64_t W, int Gp) {
   return static_cast<int>(((x + 1) * Gp - 1) / W);
 }
 
-// Largest v in [0, VB) with groups * cum(v) <= x.
+// Largest v in [0, VB) with groups * line(v) <= x.
 template <int MODE = kSchedAny>
 PMLA_HD inline int find_request(const SchedParams& sp, int64_t P, int VB, int64_t x) {
   int lo = 0, hi = VB - 1;
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
-    const int64_t prefix_end = static_cast<int64_t>(sp.groups) * VP * P;
-    if (x < prefix_end) return static_cast<int>(x / (static_cast<int64_t>(sp.groups) * P));
+    const int64_t unit_p = static_cast<int64_t>(sp.groups) *
+                           (sched_piece_cost(sp) + sched_weight<MODE>(sp, 0) * P);
+    if (x < unit_p * VP) return static_cast<int>(x / unit_p);
     lo = VP;
   }
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, mid) <= x)
+    if (static_cast<int64_t>(sp.groups) * sched_line<MODE>(sp, P, mid) <= x)
       lo = mid;
     else
       hi = mid - 1;
@@ -222,7 +285,7 @@ struct PieceIterT {
   int64_t P;
   int64_t W;
   int Gp;
-  int64_t x, x1;       // auto policy cursor
+  int64_t x, x1;       // auto policy cursor (cost-line points)
   int64_t p, p_end;    // fixed policy cursor
   Piece held;          // returned again by the next call of next() when have_held
   bool have_held;
@@ -241,8 +304,9 @@ struct PieceIterT {
     have_held = false;
     held = Piece{0, 0, 0, 0, 0, 0, 0, 0, 0, false, 0, 0};
     if (sp.splits <= 0) {
-      W = static_cast<int64_t>(sp.groups) * (VB > 0 ? sched_cum<MODE>(sp, P, VB) : 0);
-      Gp = auto_ctas(W, sp.grid);
+      W = static_cast<int64_t>(sp.groups) * (VB > 0 ? sched_line<MODE>(sp, P, VB) : 0);
+      Gp = auto_ctas(static_cast<int64_t>(sp.groups) * (VB > 0 ? sched_cum<MODE>(sp, P, VB) : 0),
+                     sp.grid);
       if (W <= 0 || cta >= Gp) {
         x = x1 = 0;
       } else {
@@ -272,19 +336,27 @@ struct PieceIterT {
       if (sp.splits <= 0) {
         if (x >= x1) return false;
         const int v = find_request<MODE>(sp, P, VB, x);
-        const int64_t base = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, v);
+        const int64_t base = static_cast<int64_t>(sp.groups) * sched_line<MODE>(sp, P, v);
         const int L = sched_len<MODE>(sp, P, v);
+        const int64_t e = sched_piece_cost(sp);
+        const int64_t w = sched_weight<MODE>(sp, v);
+        const int64_t seg = e + w * (L > 0 ? L : 0);   // one row group's segment
         const int64_t off = x - base;
-        if (L <= 0 || off < 0 || off >= static_cast<int64_t>(L) * sp.groups) {
+        if (L < 0 || off < 0 || off >= seg * sp.groups) {
           *bad = 1;
           x = x1;
           return false;
         }
-        const int g = static_cast<int>(off / L);
-        const int j0 = static_cast<int>(off - static_cast<int64_t>(g) * L);
-        const int64_t room = x1 - x;
-        const int j1 = (L - j0 <= room) ? L : j0 + static_cast<int>(room);
-        x += j1 - j0;
+        if (L == 0) {   // an empty request: nothing to attend, skip its segments
+          x = (base + seg * sp.groups < x1) ? base + seg * sp.groups : x1;
+          continue;
+        }
+        const int g = static_cast<int>(off / seg);
+        const int64_t s0 = base + static_cast<int64_t>(g) * seg;
+        const int64_t xe = (s0 + seg < x1) ? s0 + seg : x1;
+        const int j0 = line_positions(x - s0, e, w, L);
+        const int j1 = line_positions(xe - s0, e, w, L);
+        x = xe;
         pc.b = v;
         pc.g = g;
         pc.j0 = j0;
@@ -354,12 +426,16 @@ PMLA_HD inline bool unit_partials(const SchedParams& sp, int v, int g, int64_t* 
   const bool all_partial = mode != kSchedWhole && P > 0;
   const int64_t u = static_cast<int64_t>(v) * sp.groups + g;
   if (sp.splits <= 0) {
-    const int64_t W = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, VB);
-    const int Gp = auto_ctas(W, sp.grid);
-    const int64_t xs = static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, v) +
-                       static_cast<int64_t>(g) * L;
-    const int i0 = auto_cta_of(xs, W, Gp);
-    const int i1 = auto_cta_of(xs + L - 1, W, Gp);
+    // position j of (v, g) is line point s0 + e + w j; its piece is on the CTA owning it
+    const int64_t W = static_cast<int64_t>(sp.groups) * sched_line<MODE>(sp, P, VB);
+    const int Gp = auto_ctas(static_cast<int64_t>(sp.groups) * sched_cum<MODE>(sp, P, VB),
+                             sp.grid);
+    const int64_t e = sched_piece_cost(sp);
+    const int64_t w = sched_weight<MODE>(sp, v);
+    const int64_t s0 = static_cast<int64_t>(sp.groups) * sched_line<MODE>(sp, P, v) +
+                       static_cast<int64_t>(g) * (e + w * L);
+    const int i0 = auto_cta_of(s0 + e, W, Gp);
+    const int i1 = auto_cta_of(s0 + e + w * (L - 1), W, Gp);
     if (i0 == i1 && !all_partial) return false;
     *first = static_cast<int64_t>(i0) + u;   // CTA i writes unit u's piece to slot i + u
     *count = i1 - i0 + 1;

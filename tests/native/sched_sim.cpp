@@ -70,6 +70,52 @@ int sched_unit_partials_mode(const int32_t* kv_indptr, const int32_t* qo_indptr,
   return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
 }
 
+// Any mode with explicit cost-line weights (w_own, w_prefix, piece_cost); 10 int64 per
+// piece as sched_pieces_mode.
+int64_t sched_pieces_cost(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H, int NG,
+                          int groups, int splits, int grid, int mode, int gsize, int shared,
+                          int w_own, int w_prefix, int piece_cost, int64_t* out, int64_t max_out) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared,
+                       w_own, w_prefix, piece_cost};
+  int64_t n = 0;
+  for (int cta = 0; cta < grid; ++cta) {
+    pmla::PieceIter it;
+    it.init(sp, cta);
+    pmla::Piece pc;
+    int bad = 0;
+    while (it.next(pc, &bad)) {
+      if (n >= max_out) return -1;
+      int64_t* o = out + 10 * n;
+      o[0] = cta; o[1] = pc.b; o[2] = pc.g; o[3] = pc.j0; o[4] = pc.j1; o[5] = pc.rows;
+      o[6] = pc.slot; o[7] = pc.direct ? 1 : 0; o[8] = pc.kv0; o[9] = pc.cfrom;
+      ++n;
+    }
+    if (bad) return -2;
+  }
+  return n;
+}
+
+int sched_unit_partials_cost(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H,
+                             int NG, int groups, int splits, int grid, int mode, int gsize,
+                             int shared, int w_own, int w_prefix, int piece_cost, int v, int g,
+                             int64_t* first, int* count) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared,
+                       w_own, w_prefix, piece_cost};
+  return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
+}
+
+// The weights the library sets for a call (mode, group rows NG, query rows per request).
+void sched_host_costs(int mode, int NG, int rows_per_request, int* w_own, int* w_prefix,
+                      int* piece_cost) {
+  pmla::SchedParams sp{};
+  sp.mode = mode;
+  sp.NG = NG;
+  pmla::sched_set_costs(&sp, rows_per_request);
+  *w_own = sp.w_own;
+  *w_prefix = sp.w_prefix;
+  *piece_cost = sp.piece_cost;
+}
+
 int64_t sched_partial_slots(int B, int groups, int splits, int grid) {
   return pmla::partial_slots(B, groups, splits, grid);
 }

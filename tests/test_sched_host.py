@@ -40,6 +40,14 @@ def sim():
     lib.sched_unit_partials_mode.restype = ctypes.c_int
     lib.sched_unit_partials_mode.argtypes = ([i32p, i32p] + [ctypes.c_int] * 11 +
                                              [i64p, ctypes.POINTER(ctypes.c_int)])
+    lib.sched_pieces_cost.restype = ctypes.c_int64
+    lib.sched_pieces_cost.argtypes = [i32p, i32p] + [ctypes.c_int] * 12 + [i64p, ctypes.c_int64]
+    lib.sched_unit_partials_cost.restype = ctypes.c_int
+    lib.sched_unit_partials_cost.argtypes = ([i32p, i32p] + [ctypes.c_int] * 14 +
+                                             [i64p, ctypes.POINTER(ctypes.c_int)])
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.sched_host_costs.restype = None
+    lib.sched_host_costs.argtypes = [ctypes.c_int] * 3 + [ip, ip, ip]
     lib.sched_partial_slots.restype = ctypes.c_int64
     lib.sched_partial_slots.argtypes = [ctypes.c_int] * 4
     return lib
@@ -49,35 +57,56 @@ def pick_ng(rows):
     return 16 if rows <= 16 else (32 if rows <= 32 else 48)
 
 
-def simulate(sim, kv_lens, q_lens, H, splits, grid):
+def host_costs(sim, mode, NG, rows):
+    w, wp, e = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    sim.sched_host_costs(mode, NG, rows, ctypes.byref(w), ctypes.byref(wp), ctypes.byref(e))
+    return w.value, wp.value, e.value
+
+
+# cost-line weights (w_own, w_prefix, piece_cost): none (plain position line), the ones the
+# library sets ("host"), and odd ones
+COSTS = ["none", "host", (7, 11, 999)]
+
+
+def resolve_costs(sim, costs, mode, NG, rows):
+    if costs == "none":
+        return (0, 0, 0)
+    if costs == "host":
+        return host_costs(sim, mode, NG, rows)
+    return costs
+
+
+def simulate(sim, kv_lens, q_lens, H, splits, grid, costs="none"):
     kvp = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
     qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     B = len(kv_lens)
     rows = max(q_lens) * H
     NG = pick_ng(rows)
     groups = (rows + NG - 1) // NG
+    w, wp, e = resolve_costs(sim, costs, 0, NG, rows)
     i32p = ctypes.POINTER(ctypes.c_int32)
     cap = 8 * (grid + B * groups * max(splits, 1) + 16)
-    out = np.zeros(cap * 8, dtype=np.int64)
-    n = sim.sched_pieces(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, groups,
-                         splits, grid, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
+    out = np.zeros(cap * 10, dtype=np.int64)
+    n = sim.sched_pieces_cost(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, groups,
+                              splits, grid, 0, 1, 0, w, wp, e,
+                              out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
     assert n >= 0, f"simulation failed with {n}"
-    pieces = out[:8 * n].reshape(n, 8)
+    pieces = out[:10 * n].reshape(n, 10)[:, :8]
     units = {}
     for b in range(B):
         for g in range(groups):
             first = ctypes.c_int64(0)
             count = ctypes.c_int(0)
-            need = sim.sched_unit_partials(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H,
-                                           NG, groups, splits, grid, b, g, ctypes.byref(first),
-                                           ctypes.byref(count))
+            need = sim.sched_unit_partials_cost(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p),
+                                                B, H, NG, groups, splits, grid, 0, 1, 0, w, wp, e,
+                                                b, g, ctypes.byref(first), ctypes.byref(count))
             units[(b, g)] = (need, first.value, count.value)
     slots = sim.sched_partial_slots(B, groups, splits, grid)
     return pieces, units, slots, NG, groups
 
 
-def check_schedule(sim, kv_lens, q_lens, H, splits, grid):
-    pieces, units, n_slots, NG, groups = simulate(sim, kv_lens, q_lens, H, splits, grid)
+def check_schedule(sim, kv_lens, q_lens, H, splits, grid, costs="none"):
+    pieces, units, n_slots, NG, groups = simulate(sim, kv_lens, q_lens, H, splits, grid, costs)
     B = len(kv_lens)
     by_unit = {}
     for cta, b, g, j0, j1, rows, slot, direct in pieces:
@@ -128,10 +157,45 @@ CASES = [
 
 
 @pytest.mark.parametrize("kv_lens,q_lens,H", CASES)
-@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+@pytest.mark.parametrize("splits,costs", [(0, c) for c in COSTS] + [(k, "none") for k in (1, 2, 7)])
 @pytest.mark.parametrize("grid", [1, 5, 152])
-def test_schedule_covers_every_position_once(sim, kv_lens, q_lens, H, splits, grid):
-    check_schedule(sim, kv_lens, q_lens, H, splits, grid)
+def test_schedule_covers_every_position_once(sim, kv_lens, q_lens, H, splits, grid, costs):
+    # (the fixed policy has no cost line)
+    check_schedule(sim, kv_lens, q_lens, H, splits, grid, costs)
+
+
+def test_library_costs(sim):
+    """The weights the library sets: one per position plus 288 per piece on the plain
+    line; 23 + 4 per 16-row chunk per position on the cascade line (a 12-row own unit 27, a
+    48-row prefix unit 35), 288 positions' worth per piece."""
+    assert host_costs(sim, 0, 16, 12) == (1, 0, 288)
+    assert host_costs(sim, 0, 48, 48) == (1, 0, 288)
+    assert host_costs(sim, 1, 48, 12) == (27, 35, 288 * 27)
+    assert host_costs(sim, 1, 48, 24) == (31, 35, 288 * 31)
+
+
+@pytest.mark.parametrize("costs", ["host", (7, 11, 999)])
+def test_cost_line_balances_estimated_time(sim, costs):
+    """With a piece cost e and weight w, every CTA's estimated time (e per piece it starts
+    plus w per position) stays within e + 2w of the line's share W / Gp."""
+    rng = np.random.default_rng(5)
+    for kv_lens, q_lens, H in [([68174 + i for i in range(16)], [1] * 16, 12),
+                               ([int(x) for x in rng.integers(9000, 30000, size=64)], [4] * 64, 12),
+                               ([int(x) for x in rng.integers(1, 5000, size=40)], [1] * 40, 12)]:
+        pieces = check_schedule(sim, kv_lens, q_lens, H, 0, 152, costs)
+        rows = max(q_lens) * H
+        NG = pick_ng(rows)
+        groups = (rows + NG - 1) // NG
+        w, _, e = resolve_costs(sim, costs, 0, NG, rows)
+        w = max(w, 1)
+        est = np.zeros(152, dtype=np.int64)
+        for cta, b, g, j0, j1, *_ in pieces:
+            est[cta] += w * (j1 - j0) + (e if j0 == 0 else 0)
+        W = groups * sum(e + w * L for L in kv_lens)
+        Gp = min(152, max(1, groups * sum(kv_lens) // 256))
+        used = est[:Gp]
+        assert np.abs(used - W / Gp).max() <= e + 2 * w + 1, (used.min(), used.max(), W / Gp)
+        assert (est[Gp:] == 0).all()
 
 
 def test_auto_policy_balances_rows(sim):
@@ -162,7 +226,8 @@ def test_random_batches(sim):
             continue
         for splits in (0, 1, 3):
             for grid in (1, 7, 152):
-                check_schedule(sim, kv, q, H, splits, grid)
+                for costs in (COSTS if splits == 0 else ["none"]):
+                    check_schedule(sim, kv, q, H, splits, grid, costs)
 
 
 # ------------------------------------------------------------------ shared-prefix cascade
@@ -170,28 +235,29 @@ def test_random_batches(sim):
 MIN_SHARED = 1024   # prefixes shorter than this are not split off
 
 
-def cascade_pieces(sim, kvp, qop, B, H, NG, groups, grid, mode, gsize, shared):
+def cascade_pieces(sim, kvp, qop, B, H, NG, groups, grid, mode, gsize, shared, costs=(0, 0, 0)):
     i32p = ctypes.POINTER(ctypes.c_int32)
     cap = 8 * (grid + B * groups + 16)
     out = np.zeros(cap * 10, dtype=np.int64)
-    n = sim.sched_pieces_mode(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, groups,
-                              0, grid, mode, gsize, shared,
+    n = sim.sched_pieces_cost(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, groups,
+                              0, grid, mode, gsize, shared, *costs,
                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
     assert n >= 0, f"simulation failed with {n}"
     return out[:10 * n].reshape(n, 10)
 
 
-def cascade_partials(sim, kvp, qop, B, H, NG, groups, grid, mode, gsize, shared, v, g):
+def cascade_partials(sim, kvp, qop, B, H, NG, groups, grid, mode, gsize, shared, v, g,
+                     costs=(0, 0, 0)):
     i32p = ctypes.POINTER(ctypes.c_int32)
     first = ctypes.c_int64(0)
     count = ctypes.c_int(0)
-    need = sim.sched_unit_partials_mode(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H,
-                                        NG, groups, 0, grid, mode, gsize, shared, v, g,
+    need = sim.sched_unit_partials_cost(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H,
+                                        NG, groups, 0, grid, mode, gsize, shared, *costs, v, g,
                                         ctypes.byref(first), ctypes.byref(count))
     return need, first.value, count.value
 
 
-def check_cascade(sim, kv_lens, q_lens, H, grid, shared):
+def check_cascade(sim, kv_lens, q_lens, H, grid, shared, costs="none"):
     """The cascade line (prefix units: groups of gsize requests over [0, P); own units:
     each request over [P, L)) attends every (request, query row, position) exactly once,
     with unique partial slots, each piece's index base at the right entry, causal limits
@@ -203,7 +269,8 @@ def check_cascade(sim, kv_lens, q_lens, H, grid, shared):
     gsize = 48 // rows
     P = shared
     VP = (B + gsize - 1) // gsize
-    pieces = cascade_pieces(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared)
+    cw = resolve_costs(sim, costs, 1, 48, rows)
+    pieces = cascade_pieces(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared, cw)
     n_slots = sim.sched_partial_slots(VP + B, 1, 0, grid)
     cover = {}
     for cta, v, g, j0, j1, prow, slot, direct, kv0, cfrom in pieces:
@@ -229,7 +296,7 @@ def check_cascade(sim, kv_lens, q_lens, H, grid, shared):
             pos = j1
         assert pos == max(L, 0)
         need, first, count = cascade_partials(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared,
-                                              v, 0)
+                                              v, 0, cw)
         if L <= 0:
             assert need == 0
         else:
@@ -250,5 +317,6 @@ CASCADE_CASES = [
 
 @pytest.mark.parametrize("kv_lens,q_lens,H,shared", CASCADE_CASES)
 @pytest.mark.parametrize("grid", [1, 7, 152])
-def test_cascade_halves_cover_every_position_once(sim, kv_lens, q_lens, H, shared, grid):
-    check_cascade(sim, kv_lens, q_lens, H, grid, shared)
+@pytest.mark.parametrize("costs", COSTS)
+def test_cascade_halves_cover_every_position_once(sim, kv_lens, q_lens, H, shared, grid, costs):
+    check_cascade(sim, kv_lens, q_lens, H, grid, shared, costs)
