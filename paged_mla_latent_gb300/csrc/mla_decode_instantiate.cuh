@@ -26,7 +26,7 @@ int launch_decode_mode(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
       attr_set[dev] = true;
     }
   }
-  mla_decode_kernel<NG, STAGES, MODE><<<grid, kDecodeThreads, LY::kSmemBytes, stream>>>(
+  mla_decode_kernel<NG, STAGES, MODE><<<grid, LY::kThreads, LY::kSmemBytes, stream>>>(
       q_lat, q_rope, prm);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

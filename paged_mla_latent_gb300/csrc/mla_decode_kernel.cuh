@@ -6,7 +6,7 @@
 // and their merge: "Scaling Kimi K3 on AMD Instinct MI355X" §1 "Cache" and §4 "MLA".
 //
 // One persistent CTA per SM walks the pieces the scheduler (mla_sched.cuh) gives it.
-// Per tile of 128 cache positions:
+// Per tile of 128 cache positions (96 in the three-stage 32/48-row variants):
 //   producer warps  : seven warps (0-3, 5-7), rows r = w + 7 j: load the row ids, then
 //                     copy every row with 16-byte cp.async (one instruction per row of
 //                     latent columns, lanes along the row; one per 8 rows of rope columns)
@@ -23,7 +23,8 @@
 //                     then O^T[c, n] += V^T[c, pos] . P^T[pos, n] for the four 128-wide
 //                     value blocks (A = the same cache rows read MN-major; N = 2 NG: the
 //                     two P planes side by side).
-//   softmax warps   : (warps 8-11) read S^T from TMEM (one position per thread), scale, mask,
+//   softmax warps   : (one warpgroup per 16 query rows: warps 8-11, 12-15, 16-19) read
+//                     their 16 columns of S^T from TMEM (one position per thread), scale, mask,
 //                     online softmax in the exp2 domain with a lazily moved reference
 //                     max, and write P (scaled by 2^6 relative to that max) as two FP8
 //                     planes: hi = e4m3(p) and lo = e4m3(16 * (p - hi)), so P reaches
@@ -80,22 +81,39 @@ enum : int {
   kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG], then int lim[NG]
 };
 
+// Cache positions per pipeline tile.  The MMA's M is always 128 (TMEM lanes = positions);
+// a three-stage ring of 128-position tiles does not fit in shared memory next to a 32- or
+// 48-row q tile, one of 96-position tiles does.  Its QK reads 32 rows past each block
+// (whatever the next block holds: finite or not, those logits are masked, their P is never
+// written) and its PV runs three 32-position K steps.
+constexpr int tile_positions(int NG, int STAGES) { return (STAGES >= 3 && NG >= 32) ? 96 : kTile; }
+
 template <int NG, int STAGES>
 struct DecodeLayout {
+  static constexpr int kTile = tile_positions(NG, STAGES);
   static constexpr int kNPV = 2 * NG;                 // PV N: hi plane + lo plane
-  static constexpr int kStageBytes = kTile * kD;      // 73,728
+  static constexpr int kStageBytes = kTile * kD;      // 73,728 (128 positions)
   static constexpr int kLatBlock = kTile * 128;       // one 128-column latent block
   static constexpr int kRopeOff = 4 * kLatBlock;      // rope block inside a stage
-  // P (2*NG rows x 128 positions) fits in the stage's rope block once QK has read it.
-  static constexpr bool kPInRope = kNPV * 128 <= kTile * 64;
+  // P (2*NG rows x kTile positions) fits in the stage's rope block once QK has read it.
+  static constexpr bool kPInRope = kNPV * kTile <= kTile * 64;
   static constexpr int kQOff = STAGES * kStageBytes;
   static constexpr int kQBytes = NG * kD;
   static constexpr int kPOff = kQOff + kQBytes;
-  static constexpr int kPBytes = kPInRope ? 0 : 2 * kNPV * 128;
+  static constexpr int kPBytes = kPInRope ? 0 : 2 * kNPV * kTile;
+  // P tile: MN-major, no swizzle.  Position j's bytes for columns 16m .. 16m+15 are at
+  // m * kPGroup + (j / 8) * 128 + (j % 8) * 16.
+  static constexpr int kPGroup = kTile * 16;
+  static constexpr int kRowsPerProducer = (kTile + 6) / 7;   // 19 (128) or 14 (96)
+  static_assert(kTile % 32 == 0 && kTile <= 128, "tile must be whole PV K steps of one M");
+  static_assert(kStageBytes % 1024 == 0 && kLatBlock % 1024 == 0, "swizzle atoms");
   static constexpr int kMiscOff = kPOff + kPBytes;
-  static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 2048;
+  static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 3072;
   static constexpr int kMiscLim = kMiscRed + 5 * NG * 4;        // int causal limit [NG]
-  static_assert(kMiscLim + 4 * NG <= kMiscBytes, "misc region overflow");
+  // tile-max exchange of each softmax warpgroup (64 floats; one group uses red)
+  static constexpr int kMiscXch = (kMiscLim + 4 * NG + 15) / 16 * 16;
+  static_assert((NG <= 16 ? kMiscLim + 4 * NG : kMiscXch + 256 * (NG / 16)) <= kMiscBytes,
+                "misc region overflow");
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
   // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
   static constexpr int kSStride = (NG + 31) / 32 * 32;
@@ -104,28 +122,30 @@ struct DecodeLayout {
   static_assert(kOBase + 4 * kNPV <= 512, "tensor memory overflow");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static_assert(NG % 16 == 0 && NG <= 48, "group rows must be 16, 32 or 48");
+  // Warps: 0-3 and 5-7 producers, 4 MMA issuer, then one softmax warpgroup per 16-column
+  // chunk of the group's rows (warp 8 + 4 g + q: chunk g, TMEM lane quadrant q).
+  static constexpr int kGroups = NG / 16;
+  static constexpr int kThreads = 32 * (8 + 4 * kGroups);              // 384 / 512 / 640
+  // Registers a thread is launched with (65,536 per SM, whole multiples of 8), and the
+  // setmaxnreg split: the two producer/issuer warpgroups give registers back, the softmax
+  // warpgroups take them.  The split must fit the launch allocation, or .inc waits forever.
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8 > 168 ? 168 : (65536 / kThreads) / 8 * 8;
+  static constexpr int kRegsLow = NG == 16 ? 120 : (NG == 32 ? 104 : 80);
+  static constexpr int kRegsHigh = NG == 16 ? 224 : (NG == 32 ? 152 : 104);
+  static_assert(2 * kRegsLow + kGroups * kRegsHigh <= (2 + kGroups) * kLaunchRegs,
+                "register split exceeds the launch allocation");
 };
 
 
-// Twelve warps in three warpgroups.  Warpgroups 0 and 1 (producers + MMA issuer) give
-// registers back with setmaxnreg.dec; warpgroup 2 (softmax) takes them with .inc.
+// Warpgroups 0 and 1 (producers + MMA issuer) give registers back with setmaxnreg.dec;
+// the softmax warpgroups (one per 16-column chunk, see DecodeLayout) take them with .inc.
 //   warps 0-3, 5-7 : producers (7 warps)      warp 4 : MMA issuer, TMEM owner
-//   warps 8-11     : softmax / epilogue (TMEM lane quadrants 0-3)
+//   warps 8 + 4 g + q : softmax / epilogue of chunk g, TMEM lane quadrant q
 constexpr int kProducerWarps = 7;
 constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kRowsPerProducer = (kTile + kProducerWarps - 1) / kProducerWarps;   // 19
 constexpr int kMmaWarp = 4;
 constexpr int kSoftmaxWarp0 = 8;
-constexpr int kDecodeThreads = 32 * (kSoftmaxWarp0 + 4);   // 384
-constexpr int kRegsLow = 120;     // producers and MMA issuer
-constexpr int kRegsHigh = 224;   // softmax
-static_assert(8 * 32 * kRegsLow + 4 * 32 * kRegsHigh <= kDecodeThreads * 168,
-              "register split exceeds the launch allocation");
 constexpr int kSoftmaxThread0 = 32 * kSoftmaxWarp0;
-
-// P tile in shared memory: MN-major, no swizzle.  Position j's bytes for columns
-// 16m .. 16m+15 are at m * kPGroup + (j / 8) * 128 + (j % 8) * 16.
-constexpr int kPGroup = kTile * 16;   // 2048
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -213,7 +233,7 @@ __device__ __forceinline__ void issue_q_load(uint32_t sQ, const CUtensorMap* lat
 // MODE: the schedule (kSchedWhole for a plain decode, kSchedCascade for the shared-prefix
 // cascade), fixed at compile time.
 template <int NG, int STAGES, int MODE>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
                       const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams prm) {
   using LY = DecodeLayout<NG, STAGES>;
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     iter.hold(pc);                 // every role starts from this piece
     first_qrow = pc.qo0 * prm.sp.H + pc.g * NG;
     // the first tile's row ids: their fetch overlaps the set-up below
-    if (threadIdx.x < kTile / 32) {
+    if (threadIdx.x < LY::kTile / 32) {
       const int64_t gi = pc.kv0 + pc.j0 + 32 * threadIdx.x;
       if (gi >= 0 && gi < prm.kv_indices_len) prefetch_l1(prm.kv_indices + gi);
     }
@@ -271,7 +291,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(mbase + kMiscSFull + 8 * s, 1);
-      mbar_init(mbase + kMiscPFull + 8 * s, 4);
+      mbar_init(mbase + kMiscPFull + 8 * s, 4 * LY::kGroups);   // every softmax warp
     }
     mbar_init(mbase + kMiscPv, 1);
     mbar_init(mbase + kMiscPv + 8, 1);
@@ -297,11 +317,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   int bad = 0;
 
   if (warp >= kSoftmaxWarp0) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    // ===================================================== softmax + epilogue (4 warps)
-    // The softmax warps read their first piece again (from memory: off their critical path,
-    // they wait for the first tile's logits) and so keep no held piece in registers.
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(LY::kRegsHigh));
+    // ===================================================== softmax + epilogue
+    // Warpgroup g owns columns (query rows of the group) c0 = 16 g .. c0 + 15, warp q of it
+    // TMEM lane quadrant q (positions 32 q .. 32 q + 31).  The warpgroups share only the
+    // tile handshakes (S full, P full, PV done); each votes, exchanges tile maxima, reduces
+    // and writes its rows out on its own named barrier, so they run side by side.
+    // They read their first piece again (from memory: off their critical path, they wait
+    // for the first tile's logits) and so keep no held piece in registers.
     iter.init(prm.sp, blockIdx.x);
+    const int grp = (warp - kSoftmaxWarp0) >> 2;
+    const int bar_g = 1 + grp;               // named barrier of this warpgroup (128 threads)
+    const int c0 = 16 * grp;                 // its first column
     const int q4 = warp & 3;                 // TMEM lane quadrant this warp may access
     const int prow = 32 * q4 + lane;         // position within the tile == TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
@@ -309,97 +336,92 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const float scale_log2 = prm.sm_scale * (*prm.q_scale) * kv_scale * kLog2e;
     const int H = prm.sp.H;
     // P is stored MN-major without swizzle (see the PV descriptor): this position's 16
-    // bytes of columns 16m .. 16m+15 sit at pofs + m * kPGroup.
+    // bytes of columns 16m .. 16m+15 sit at pofs + m * LY::kPGroup.
     const uint32_t pofs = (prow >> 3) * 128 + (prow & 7) * 16;
-    float* s_alpha = red + 4 * NG;
+    float* s_alpha = red + 4 * NG + c0;      // this chunk's rescale factors [16]
+    float* xch = LY::kGroups == 1 ? red
+                                  : reinterpret_cast<float*>(misc + LY::kMiscXch) + 64 * grp;
     int* s_lim = reinterpret_cast<int*>(misc + LY::kMiscLim);
+    constexpr int kCh = NG / 16;
 
     uint32_t it_g = 0;
     Piece pc;
-    float m_ref[NG];   // reference max - kPShift, per column
-    float l_acc[NG];
+    float m_ref[16];   // reference max - kPShift, per column of the chunk
+    float l_acc[16];
     while (iter.next(pc, &bad)) {
-      const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+      const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
+      // A chunk past the unit's real rows (a 12-row unit in a 48-row tile) is skipped: its P
+      // columns only feed O columns that are never written out.
+      const bool live = c0 < pc.rows;
 #pragma unroll
-      for (int n = 0; n < NG; ++n) {
-        m_ref[n] = kRefInit;
-        l_acc[n] = 0.f;
+      for (int k = 0; k < 16; ++k) {
+        m_ref[k] = kRefInit;
+        l_acc[k] = 0.f;
       }
       const int causal_from = pc.cfrom;   // positions beyond this need the causal test
       // draft t of this group's row n sees positions <= L - T + t
-      if (prow < NG) s_lim[prow] = causal_from + (pc.g * NG + prow) / H;
-      bar_sync(1, 128);
+      if (prow < 16) s_lim[c0 + prow] = causal_from + (pc.g * NG + c0 + prow) / H;
+      bar_sync(bar_g, 128);
       for (int t = 0; t < nt; ++t, ++it_g) {
         const int sb = it_g & 1;
         mbar_wait(mbase + kMiscSFull + 8 * sb, (it_g >> 1) & 1, abort_flag, prm.err);
         tc_fence_after();
-        const int pos = pc.j0 + t * kTile + prow;
-        const bool in_piece = pos < pc.j1;
-        const bool causal = in_piece && pos > causal_from;
-        const uint32_t s_tm = tl + sb * LY::kSStride;
-        // scaled logit (log2 units) of column n, with masks: past the piece or beyond the
-        // draft's causal limit -> -inf; padding rows -> 0 (finite, discarded)
-        auto xform = [&](float sraw, int n) -> float {
-          float v = in_piece ? sraw * scale_log2 : -INFINITY;
-          if (causal && pos > s_lim[n]) v = -INFINITY;
-          return (n >= pc.rows) ? 0.f : v;
-        };
-        constexpr int kCh = NG / 16;
-        const int stage = static_cast<int>(it_g % STAGES);
-        // P tile: this position's 16-byte vectors (see kPGroup)
-        uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
-                                    : smem + LY::kPOff + sb * NPV * 128) + pofs;
-        bool pv_prev_done = (t == 0);   // O holds nothing yet on a piece's first tile
-        // Columns are independent heads: each 16-column chunk is finished in one pass.
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) {
-          // chunks past the unit's real rows (a 12-row unit in a 48-row tile) are skipped:
-          // their P columns only feed O columns that are never written out
-          if (ch > 0 && 16 * ch >= pc.rows) break;
+        if (live) {
+          const int pos = pc.j0 + t * LY::kTile + prow;
+          // (lanes past a 96-position tile hold don't-care logits and write no P)
+          const bool in_piece = prow < LY::kTile && pos < pc.j1;
+          const bool causal = in_piece && pos > causal_from;
+          // scaled logit (log2 units) of column n, with masks: past the piece or beyond the
+          // draft's causal limit -> -inf; padding rows -> 0 (finite, discarded)
+          auto xform = [&](float sraw, int n) -> float {
+            float v = in_piece ? sraw * scale_log2 : -INFINITY;
+            if (causal && pos > s_lim[n]) v = -INFINITY;
+            return (n >= pc.rows) ? 0.f : v;
+          };
+          const int stage = static_cast<int>(it_g % STAGES);
+          // P tile: this position's 16-byte vectors (see LY::kPGroup)
+          uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
+                                      : smem + LY::kPOff + sb * NPV * LY::kTile) + pofs;
           float xs[16];
-          tmem_ld16(s_tm + 16 * ch, xs);
+          tmem_ld16(tl + sb * LY::kSStride + c0, xs);
           tmem_wait_ld();
           float dmax = -INFINITY;
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            xs[k] = xform(xs[k], 16 * ch + k);
-            dmax = fmaxf(dmax, xs[k] - m_ref[16 * ch + k]);
+            xs[k] = xform(xs[k], c0 + k);
+            dmax = fmaxf(dmax, xs[k] - m_ref[k]);
           }
-          if (bar_red_or(1, 128, dmax > kMoveAt)) {
+          if (bar_red_or(bar_g, 128, dmax > kMoveAt)) {
             // rare: move these columns' reference to their tile maxima
             {
               float v[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) v[k] = xs[k];
               const float wmax = reduce_scatter16<true>(v, lane);
-              if ((lane & 1) == 0) red[col16(lane) * 4 + q4] = wmax;
+              if ((lane & 1) == 0) xch[col16(lane) * 4 + q4] = wmax;
             }
-            bar_sync(1, 128);
+            bar_sync(bar_g, 128);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const int n = 16 * ch + k;
-              const float4 r4 = *reinterpret_cast<const float4*>(red + 4 * k);
+              const float4 r4 = *reinterpret_cast<const float4*>(xch + 4 * k);
               const float tmax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
-              const float m_new = fmaxf(m_ref[n], tmax - kPShift);
-              const float alpha = ex2_approx(m_ref[n] - m_new);   // 0 from the initial reference
-              l_acc[n] *= alpha;
-              m_ref[n] = m_new;
+              const float m_new = fmaxf(m_ref[k], tmax - kPShift);
+              const float alpha = ex2_approx(m_ref[k] - m_new);   // 0 from the initial reference
+              l_acc[k] *= alpha;
+              m_ref[k] = m_new;
               if (prow == 0) s_alpha[k] = alpha;
             }
-            bar_sync(1, 128);
+            bar_sync(bar_g, 128);
             if (t > 0) {
               // O holds this piece's earlier tiles: wait for the last PV, then rescale the
               // chunk's hi and lo columns in the four value blocks
-              if (!pv_prev_done) {
-                mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag,
-                          prm.err);
-                tc_fence_after();
-                pv_prev_done = true;
-              }
+              mbar_wait(mbase + kMiscPv + 8 * ((it_g - 1) & 1), ((it_g - 1) >> 1) & 1, abort_flag,
+                        prm.err);
+              tc_fence_after();
 #pragma unroll 1
               for (int bp = 0; bp < 8; ++bp) {
                 float v[16];
-                const uint32_t a = tl + LY::kOBase + (bp >> 1) * NPV + (bp & 1) * NG + 16 * ch;
+                const uint32_t a = tl + LY::kOBase + (bp >> 1) * NPV + (bp & 1) * NG + c0;
                 tmem_ld16(a, v);
                 tmem_wait_ld();
 #pragma unroll
@@ -414,11 +436,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
-            const int n = 16 * ch + k;
-            const float p0 = ex2_approx(xs[k] - m_ref[n]);
-            const float p1 = ex2_approx(xs[k + 1] - m_ref[n + 1]);
-            l_acc[n] += p0;
-            l_acc[n + 1] += p1;
+            const float p0 = ex2_approx(xs[k] - m_ref[k]);
+            const float p1 = ex2_approx(xs[k + 1] - m_ref[k + 1]);
+            l_acc[k] += p0;
+            l_acc[k + 1] += p1;
             const uint32_t p16 = f32x2_to_f16x2(p1, p0);          // low half: p0
             const uint32_t hi = f16x2_to_e4m3x2(p16);             // byte 0: p0, byte 1: p1
             const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), kLoScaleF16x2);
@@ -431,64 +452,68 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               lw[k >> 2] |= lo << 16;
             }
           }
-          *reinterpret_cast<uint4*>(pb + ch * kPGroup) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(pb + (kCh + ch) * kPGroup) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          if (prow < LY::kTile) {
+            *reinterpret_cast<uint4*>(pb + grp * LY::kPGroup) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(pb + (kCh + grp) * LY::kPGroup) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(mbase + kMiscPFull + 8 * sb);
-
-        if (t == nt - 1) {
-          // ------------------------------------------------ piece epilogue
-          // The row sums and the per-row set-up need only the softmax state: they run while
-          // the piece's last PV is still in the tensor pipe; the output waits for it.
+      }
+      // ------------------------------------------------ piece epilogue (after its last
+      // tile's P was handed to the MMA issuer; kept out of the tile loop)
+      {
+        const uint32_t it_last = it_g - 1;
+        // The row sums and the per-row set-up need only the softmax state: they run while
+        // the piece's last PV is still in the tensor pipe; the output waits for it.
+        if (live) {
+          float v[16];
 #pragma unroll
-          for (int ch = 0; ch < NG / 16; ++ch) {
-            if (ch > 0 && 16 * ch >= pc.rows) break;   // no real rows left
-            float v[16];
+          for (int k = 0; k < 16; ++k) v[k] = l_acc[k];
+          const float wsum = reduce_scatter16<false>(v, lane);
+          if ((lane & 1) == 0) red[q4 * NG + c0 + col16(lane)] = wsum;
+        }
+        bar_sync(bar_g, 128);
+        // one thread per row: normaliser, lse and output offset of that row
+        float* s_scale = red + 4 * NG;                                   // [NG]
+        int64_t* s_off = reinterpret_cast<int64_t*>(misc + kMiscRowOff);  // [NG]
+        const bool direct = pc.direct;
+        const bool slot_ok = direct || (pc.slot >= 0 && pc.slot < prm.n_slots);
+        if (live && prow < 16) {
+          const int n = c0 + prow;
+          const float l = (red[n] + red[NG + n]) + (red[2 * NG + n] + red[3 * NG + n]);
+          float m = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = l_acc[16 * ch + k];
-            const float wsum = reduce_scatter16<false>(v, lane);
-            if ((lane & 1) == 0) red[q4 * NG + 16 * ch + col16(lane)] = wsum;
-          }
-          bar_sync(1, 128);
-          // one thread per row: normaliser, lse and output offset of that row
-          float* s_scale = red + 4 * NG;                                   // [NG]
-          int64_t* s_off = reinterpret_cast<int64_t*>(misc + kMiscRowOff);  // [NG]
-          const bool direct = pc.direct;
-          const bool slot_ok = direct || (pc.slot >= 0 && pc.slot < prm.n_slots);
-          if (prow < NG) {
-            const int n = prow;
-            const float l = (red[n] + red[NG + n]) + (red[2 * NG + n] + red[3 * NG + n]);
-            float m = 0.f;
-#pragma unroll
-            for (int k = 0; k < NG; ++k) m = (k == n) ? m_ref[k] : m;
-            const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
-            int64_t off = -1;
-            if (n < pc.rows) {
-              if (direct) {
-                const int rr = pc.g * NG + n;              // row within the request
-                const int64_t tok = static_cast<int64_t>(pc.qo0) + rr / H;
-                const int64_t r = tok * H + rr % H;
-                if (r < prm.n_q_rows) {
-                  off = tok * prm.o_stride_tok + (rr % H) * prm.o_stride_head;
-                  if (prm.lse_out) prm.lse_out[r] = lse;
-                } else {
-                  atomicOr(prm.err, kErrBadOutput);
-                }
-              } else if (slot_ok) {
-                off = (pc.slot * NG + n) * kDV;
-                prm.part_lse[pc.slot * NG + n] = lse;
+          for (int k = 0; k < 16; ++k) m = (k == prow) ? m_ref[k] : m;
+          const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+          int64_t off = -1;
+          if (n < pc.rows) {
+            if (direct) {
+              const int rr = pc.g * NG + n;              // row within the request
+              const int64_t tok = static_cast<int64_t>(pc.qo0) + rr / H;
+              const int64_t r = tok * H + rr % H;
+              if (r < prm.n_q_rows) {
+                off = tok * prm.o_stride_tok + (rr % H) * prm.o_stride_head;
+                if (prm.lse_out) prm.lse_out[r] = lse;
               } else {
                 atomicOr(prm.err, kErrBadOutput);
               }
+            } else if (slot_ok) {
+              off = (pc.slot * NG + n) * kDV;
+              prm.part_lse[pc.slot * NG + n] = lse;
+            } else {
+              atomicOr(prm.err, kErrBadOutput);
             }
-            s_scale[n] = (l > 0.f) ? kv_scale / l : 0.f;
-            s_off[n] = off;
           }
-          bar_sync(1, 128);
-          mbar_wait(mbase + kMiscPv + 8 * (it_g & 1), (it_g >> 1) & 1, abort_flag, prm.err);
+          s_scale[n] = (l > 0.f) ? kv_scale / l : 0.f;
+          s_off[n] = off;
+        }
+        bar_sync(bar_g, 128);
+        if (live) {
+          mbar_wait(mbase + kMiscPv + 8 * (it_last & 1), (it_last >> 1) & 1, abort_flag, prm.err);
           tc_fence_after();
           // normalised output.  TMEM lane = value column: a warp holds 32 adjacent columns
           // of every row.  Lanes exchange values (in-register transposes) so that each
@@ -499,63 +524,59 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const bool vec = !direct || prm.o_vec16;
           float* fdst = direct ? reinterpret_cast<float*>(prm.o) : prm.part_o;
           __nv_bfloat16* hdst = reinterpret_cast<__nv_bfloat16*>(prm.o);
-#pragma unroll 1
-          for (int ch = 0; ch < NG / 16; ++ch) {
-            if (ch > 0 && 16 * ch >= pc.rows) break;   // no real rows left
-#pragma unroll 1
-            for (int bk = 0; bk < 4; ++bk) {
-              float hi[16], lo[16];
-              tmem_ld16(tl + LY::kOBase + bk * NPV + 16 * ch, hi);
-              tmem_ld16(tl + LY::kOBase + bk * NPV + NG + 16 * ch, lo);
-              tmem_wait_ld();
+          #pragma unroll 1
+          for (int bk = 0; bk < 4; ++bk) {
+            float hi[16], lo[16];
+            tmem_ld16(tl + LY::kOBase + bk * NPV + c0, hi);
+            tmem_ld16(tl + LY::kOBase + bk * NPV + NG + c0, lo);
+            tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) hi[k] = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[16 * ch + k];
-              const int cw = bk * 128 + 32 * q4;   // first column of this warp
-              if (!vec) {
+            for (int k = 0; k < 16; ++k) hi[k] = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[c0 + k];
+            const int cw = bk * 128 + 32 * q4;   // first column of this warp
+            if (!vec) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const int64_t off = s_off[16 * ch + k];
-                  if (off < 0) continue;
-                  if (to_bf16)
-                    hdst[off + cw + lane] = __float2bfloat16_rn(hi[k]);
-                  else
-                    fdst[off + cw + lane] = hi[k];
+              for (int k = 0; k < 16; ++k) {
+                const int64_t off = s_off[c0 + k];
+                if (off < 0) continue;
+                if (to_bf16)
+                  hdst[off + cw + lane] = __float2bfloat16_rn(hi[k]);
+                else
+                  fdst[off + cw + lane] = hi[k];
+              }
+            } else if (to_bf16) {
+              lane_transpose<8>(hi, lane);
+              lane_transpose<8>(hi + 8, lane);
+              const int cs = cw + 8 * (lane >> 3);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int64_t off = s_off[c0 + 8 * h + (lane & 7)];
+                if (off >= 0) {
+                  const float* a = hi + 8 * h;
+                  *reinterpret_cast<uint4*>(hdst + off + cs) =
+                      make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                 pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
                 }
-              } else if (to_bf16) {
-                lane_transpose<8>(hi, lane);
-                lane_transpose<8>(hi + 8, lane);
-                const int c0 = cw + 8 * (lane >> 3);
+              }
+            } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int64_t off = s_off[16 * ch + 8 * h + (lane & 7)];
-                  if (off >= 0) {
-                    const float* a = hi + 8 * h;
-                    *reinterpret_cast<uint4*>(hdst + off + c0) =
-                        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                                   pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
-                  }
-                }
-              } else {
+              for (int g = 0; g < 4; ++g) lane_transpose<4>(hi + 4 * g, lane);
+              const int cs = cw + 4 * (lane >> 2);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) lane_transpose<4>(hi + 4 * g, lane);
-                const int c0 = cw + 4 * (lane >> 2);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                  const int64_t off = s_off[16 * ch + 4 * g + (lane & 3)];
-                  if (off >= 0)
-                    *reinterpret_cast<float4*>(fdst + off + c0) =
-                        make_float4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
-                }
+              for (int g = 0; g < 4; ++g) {
+                const int64_t off = s_off[c0 + 4 * g + (lane & 3)];
+                if (off >= 0)
+                  *reinterpret_cast<float4*>(fdst + off + cs) =
+                      make_float4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
               }
             }
           }
-          bar_sync(1, 128);   // s_off / s_scale are rewritten by the next piece
-          tc_fence_before();
         }
+        bar_sync(bar_g, 128);   // s_off / s_scale are rewritten by the next piece
+        tc_fence_before();
       }
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LY::kRegsLow));
     if (warp != kMmaWarp) {
       // ===================================================== producers (7 warps)
       const int pw = warp < kMmaWarp ? warp : warp - 1;   // producer index 0..6
@@ -567,9 +588,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const uint8_t* kv = prm.kv;
       const int64_t pitch = prm.kv_pitch;
       // Producer pw copies tile rows r = pw + 7 j (j < rows_w); lane j loads row j's id.
-      const int rows_w = (kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 19 or 18
+      const int rows_w = (LY::kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 19 / 18 (14 / 13)
       while (!aborted && iter.next(pc, &bad)) {
-        const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+        const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
         if (warp == 0 && lane == 0) {
           // q rows of this piece, once the previous piece's QK has released the buffer
           // (the first piece's load was issued during the set-up)
@@ -589,7 +610,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // row id of row j of this warp in tile t (-1: past the piece or invalid)
         auto load_row = [&](int t, int j) -> int {
           if (j >= rows_w) return -1;
-          const int pos = pc.j0 + t * kTile + pw + kProducerWarps * j;
+          const int pos = pc.j0 + t * LY::kTile + pw + kProducerWarps * j;
           if (pos >= pc.j1) return -1;
           const int64_t gi = kvbase + pos;
           if (gi < 0 || gi >= prm.kv_indices_len) {
@@ -628,7 +649,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           // rope columns: 8 rows x 4 chunks per instruction
   #pragma unroll
-          for (int m = 0; m < (kRowsPerProducer + 7) / 8; ++m) {
+          for (int m = 0; m < (LY::kRowsPerProducer + 7) / 8; ++m) {
             const int j = 8 * m + (lane >> 2);
             const int c = lane & 3;
             const int v = __shfl_sync(0xffffffffu, rid, j);
@@ -660,18 +681,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int stage = static_cast<int>(i % STAGES);
           tc_fence_after();
           const uint32_t st = sbase + stage * LY::kStageBytes;
-          const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * 128;
+          const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * LY::kTile;
   #pragma unroll
           for (int bk = 0; bk < 4; ++bk) {
             const uint32_t d = tmem + LY::kOBase + bk * NPV;
   #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < LY::kTile / 32; ++kk) {
               // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
               const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
               // B = P, MN-major without swizzle: 32 positions (K) in 8-position core
               // matrices of 128 bytes, 128 bytes apart (leading byte offset); NPV columns
-              // (MN) in groups of 16, kPGroup apart (stride byte offset)
-              const uint64_t b = smem_desc(pbuf + kk * 4 * 128, 128, kPGroup, kSwNone);
+              // (MN) in groups of 16, LY::kPGroup apart (stride byte offset)
+              const uint64_t b = smem_desc(pbuf + kk * 4 * 128, 128, LY::kPGroup, kSwNone);
               mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
             }
           }
@@ -721,7 +742,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             pend = false;
           };
           while (ok && iter.next(pc, &bad)) {
-            const int nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+            const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
             for (int t = 0; t < nt && ok; ++t) {
               if (t == 0 && !mbar_wait(mbase + kMiscQFull, n_piece & 1, abort_flag, prm.err)) {
                 ok = false;
@@ -762,7 +783,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 break;
               }
               have_piece = true;
-              nt = (pc.j1 - pc.j0 + kTile - 1) / kTile;
+              nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
               t_in = 0;
               q_ready = false;
             }
