@@ -18,7 +18,7 @@
 //                     128-byte boxes issues 5 requests per 4 rows and measured 2-4 TB/s on
 //                     this access pattern; per-thread copies reach the random-row gather
 //                     limit of ~5.3 TB/s.)
-//   MMA thread      : (warp 4) S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
+//   MMA warp        : (warp 4) S^T[pos, n] = K[pos, :] . Q[n, :]  (tcgen05 kind::f8f6f4,
 //                     M = 128 positions, N = NG query rows, K = 576; FP32 in TMEM),
 //                     then O^T[c, n] += V^T[c, pos] . P^T[pos, n] for the four 128-wide
 //                     value blocks (A = the same cache rows read MN-major; N = 2 NG: the
@@ -670,8 +670,21 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
         mbar_wait_drain(mbase + kMiscQFull, (q_loads - 1) & 1);
       __syncwarp();
     } else {
-      // ===================================================== MMA issuer (one thread)
-      if (lane == 0) {
+      // ===================================================== MMA issuer (one warp)
+      // The whole warp runs the issue loop, so that the descriptors are warp-uniform values,
+      // and one elected lane issues each MMA and commit (mma_f8_warp).  Every lane waits on
+      // a barrier together (each wait is bounded); lane 0's outcome decides for the warp, so
+      // its control flow stays uniform.  (A wait by lane 0 alone while the other lanes sat
+      // in the broadcast made the first MMAs of a CTA take ~5 us.)
+      {
+        auto wait1 = [&](uint32_t bar_, uint32_t parity) -> bool {
+          return warp_bcast(mbar_wait(bar_, parity, abort_flag, prm.err));
+        };
+        auto test1 = [&](uint32_t bar_, uint32_t parity) -> bool {
+          bool r = false;
+          if (lane == 0) r = mbar_test(bar_, parity);
+          return warp_bcast(r);
+        };
         constexpr uint32_t idesc_qk = idesc_f8(128, NG, false, false);
         constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, true);
         int n_piece = 0;
@@ -693,11 +706,11 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
               // matrices of 128 bytes, 128 bytes apart (leading byte offset); NPV columns
               // (MN) in groups of 16, LY::kPGroup apart (stride byte offset)
               const uint64_t b = smem_desc(pbuf + kk * 4 * 128, 128, LY::kPGroup, kSwNone);
-              mma_f8(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
+              mma_f8_warp(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
             }
           }
-          mma_commit(mbase + kMiscEmpty + 8 * stage);
-          mma_commit(mbase + kMiscPv + 8 * (i & 1));
+          mma_commit_warp(mbase + kMiscEmpty + 8 * stage);
+          mma_commit_warp(mbase + kMiscPv + 8 * (i & 1));
         };
         auto issue_qk = [&](uint32_t i) {
           const int stage = static_cast<int>(i % STAGES);
@@ -711,15 +724,15 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           for (int kk = 0; kk < 16; ++kk) {   // latent columns 0..511, 32 per MMA
             const uint64_t a = smem_desc(st + (kk >> 2) * LY::kLatBlock + (kk & 3) * 32, 16, 1024, kSw128);
             const uint64_t b = smem_desc(sQ + (kk >> 2) * NG * 128 + (kk & 3) * 32, 16, 1024, kSw128);
-            mma_f8(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+            mma_f8_warp(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
   #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {    // rope columns 512..575
             const uint64_t a = smem_desc(st + LY::kRopeOff + kk * 32, 16, 512, kSw64);
             const uint64_t b = smem_desc(sQ + 4 * NG * 128 + kk * 32, 16, 512, kSw64);
-            mma_f8(d, a, b, idesc_qk, 1u);
+            mma_f8_warp(d, a, b, idesc_qk, 1u);
           }
-          mma_commit(mbase + kMiscSFull + 8 * (i & 1));
+          mma_commit_warp(mbase + kMiscSFull + 8 * (i & 1));
         };
         if constexpr (STAGES >= 3) {
           // Issue order: QK(0), QK(1), PV(0), QK(2), PV(1), ... (CTA-wide tile numbers): QK
@@ -734,7 +747,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           bool ok = true;
           auto pv_step = [&]() {
             const uint32_t j = pend_j;
-            if (!mbar_wait(mbase + kMiscPFull + 8 * (j & 1), (j >> 1) & 1, abort_flag, prm.err)) {
+            if (!wait1(mbase + kMiscPFull + 8 * (j & 1), (j >> 1) & 1)) {
               ok = false;
               return;
             }
@@ -744,17 +757,17 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           while (ok && iter.next(pc, &bad)) {
             const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
             for (int t = 0; t < nt && ok; ++t) {
-              if (t == 0 && !mbar_wait(mbase + kMiscQFull, n_piece & 1, abort_flag, prm.err)) {
+              if (t == 0 && !wait1(mbase + kMiscQFull, n_piece & 1)) {
                 ok = false;
                 break;
               }
               const int stage = static_cast<int>(i % STAGES);
-              if (!mbar_wait(mbase + kMiscFull + 8 * stage, (i / STAGES) & 1, abort_flag, prm.err)) {
+              if (!wait1(mbase + kMiscFull + 8 * stage, (i / STAGES) & 1)) {
                 ok = false;
                 break;
               }
               issue_qk(i);
-              if (t == nt - 1) mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q
+              if (t == nt - 1) mma_commit_warp(mbase + kMiscQEmpty);   // the producers may overwrite q
               if (pend) pv_step();
               pend = true;
               pend_j = i;
@@ -789,19 +802,19 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             }
             if (!have_piece && p_next == q_next) break;   // everything issued
             bool progressed = false;
-            if (p_next < q_next && mbar_test(mbase + kMiscPFull + 8 * (p_next & 1), (p_next >> 1) & 1)) {
+            if (p_next < q_next && test1(mbase + kMiscPFull + 8 * (p_next & 1), (p_next >> 1) & 1)) {
               issue_pv(p_next, pv_first[p_next & 1]);
               ++p_next;
               progressed = true;
             } else if (have_piece && q_next <= p_next + 1) {
-              if (t_in == 0 && !q_ready) q_ready = mbar_test(mbase + kMiscQFull, n_piece & 1);
+              if (t_in == 0 && !q_ready) q_ready = test1(mbase + kMiscQFull, n_piece & 1);
               const int stage = static_cast<int>(q_next % STAGES);
               if ((t_in > 0 || q_ready) &&
-                  mbar_test(mbase + kMiscFull + 8 * stage, (q_next / STAGES) & 1)) {
+                  test1(mbase + kMiscFull + 8 * stage, (q_next / STAGES) & 1)) {
                 issue_qk(q_next);
                 pv_first[q_next & 1] = (t_in == 0);
                 if (t_in == nt - 1) {
-                  mma_commit(mbase + kMiscQEmpty);   // the producers may overwrite q rows
+                  mma_commit_warp(mbase + kMiscQEmpty);   // the producers may overwrite q rows
                   ++n_piece;
                 }
                 ++q_next;
@@ -812,21 +825,23 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             if (progressed) {
               idle_since = 0;
             } else {
-              if (*abort_flag) break;
-              const unsigned long long now = globaltimer_ns();
+              if (warp_bcast(*abort_flag != 0)) break;
+              const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
               if (idle_since == 0) {
                 idle_since = now;
               } else if (now - idle_since > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(prm.err, kErrTimeout);
+                if (lane == 0) {
+                  *abort_flag = 1;
+                  atomicOr(prm.err, kErrTimeout);
+                }
                 break;
               }
             }
           }
         }
         // Drain: all MMAs must complete before tensor memory is released.
-        mma_commit(mbase + kMiscDrain);
-        mbar_wait_drain(mbase + kMiscDrain, 0);
+        mma_commit_warp(mbase + kMiscDrain);
+        if (lane == 0) mbar_wait_drain(mbase + kMiscDrain, 0);
       }
       __syncwarp();
     }

@@ -207,6 +207,34 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// The same two operations for a converged warp: every lane computes the (warp-uniform)
+// descriptors and one elected lane issues.  Issued this way an M=128, K=32 MMA costs its
+// tensor time (measured 52 cycles at N <= 48, 58 at N = 96 on GB300); issued from inside a
+// one-lane branch the descriptor arithmetic between MMAs cost ~96 cycles each.
+__device__ __forceinline__ void mma_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 p, %4, 0, e;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+// Lane 0's value of a predicate, for every lane of the warp (keeps a warp's control flow
+// converged where only one lane polls a barrier).
+__device__ __forceinline__ bool warp_bcast(bool v) {
+  return __shfl_sync(0xffffffffu, v ? 1 : 0, 0) != 0;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
