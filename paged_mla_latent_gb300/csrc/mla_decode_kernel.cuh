@@ -630,6 +630,12 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const uint32_t use = it_g / STAGES;
           const int rid = nxt;
           if (t + 1 < nt) nxt = load_row(t + 1, lane);   // next tile's row ids overlap the wait
+          if (t + 2 < nt && lane < rows_w) {   // and the one after is fetched into L1
+            const int64_t gi = kvbase + pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane;
+            if (gi >= 0 && gi < prm.kv_indices_len &&
+                pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane < pc.j1)
+              prefetch_l1(prm.kv_indices + gi);
+          }
           if (use > 0 &&
               !mbar_wait(mbase + kMiscEmpty + 8 * stage, (use - 1) & 1, abort_flag, prm.err)) {
             aborted = true;
