@@ -89,21 +89,16 @@ struct SchedParams {
   int piece_cost;  // per (unit, row group): set-up and epilogue of a piece
 };
 
-// Cost-line weights.  A piece's fixed cost (the epilogue writing NG x 512 values, the
-// pipeline's refill) measured about 2.3 tiles' time on every variant; a 48-row prefix
-// tile (three 16-row softmax chunks) about 1.3 times a 12-row own tile (one chunk), the
-// tile's time modelled as 23 + 4 per chunk.
-constexpr int kPieceCostPositions = 288;
-PMLA_HD inline int chunk_weight(int rows) { return 23 + 4 * ((rows + 15) / 16); }
-inline void sched_set_costs(SchedParams* sp, int rows_per_request) {
-  if (sp->mode == kSchedCascade) {
-    sp->w_own = chunk_weight(rows_per_request < sp->NG ? rows_per_request : sp->NG);
-    sp->w_prefix = chunk_weight(sp->NG);
-  } else {
-    sp->w_own = 1;
-    sp->w_prefix = 0;
-  }
-  sp->piece_cost = kPieceCostPositions * sp->w_own;
+// Cost-line weights the library sets.  A piece's fixed cost (its epilogue, the pipeline's
+// refill) is charged as 512 positions: a sweep of 192 .. 768 on every workload put the
+// optimum at 512 to 768.  Prefix and own units take the same weight per position: with one
+// softmax warpgroup per 16 query rows a 48-row prefix tile costs what a 12-row own tile
+// does (cheaper prefix weights measured slower).
+constexpr int kPieceCostPositions = 512;
+inline void sched_set_costs(SchedParams* sp, int /*rows_per_request*/) {
+  sp->w_own = 1;
+  sp->w_prefix = 0;   // reads as w_own
+  sp->piece_cost = kPieceCostPositions;
 }
 
 struct Piece {

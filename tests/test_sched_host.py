@@ -165,13 +165,12 @@ def test_schedule_covers_every_position_once(sim, kv_lens, q_lens, H, splits, gr
 
 
 def test_library_costs(sim):
-    """The weights the library sets: one per position plus 288 per piece on the plain
-    line; 23 + 4 per 16-row chunk per position on the cascade line (a 12-row own unit 27, a
-    48-row prefix unit 35), 288 positions' worth per piece."""
-    assert host_costs(sim, 0, 16, 12) == (1, 0, 288)
-    assert host_costs(sim, 0, 48, 48) == (1, 0, 288)
-    assert host_costs(sim, 1, 48, 12) == (27, 35, 288 * 27)
-    assert host_costs(sim, 1, 48, 24) == (31, 35, 288 * 31)
+    """The weights the library sets: one per position and 512 per piece, on the plain and
+    the cascade line alike."""
+    assert host_costs(sim, 0, 16, 12) == (1, 0, 512)
+    assert host_costs(sim, 0, 48, 48) == (1, 0, 512)
+    assert host_costs(sim, 1, 48, 12) == (1, 0, 512)
+    assert host_costs(sim, 1, 48, 24) == (1, 0, 512)
 
 
 @pytest.mark.parametrize("costs", ["host", (7, 11, 999)])
