@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = [
     "MlaError", "mla_decode", "mla_decode_shared_prefix", "mla_decode_noalloc", "mla_merge_partials",
     "mla_validate", "mla_check_error", "mla_get_workspace_size", "mla_get_shared_prefix_workspace_size",
-    "mla_status_string", "make_workspace", "library_path",
+    "mla_status_string", "make_workspace", "library_path", "PreparedDecode",
 ]
 
 MLA_DTYPE_FP8_E4M3FN = 1
@@ -93,25 +93,27 @@ _DTYPES = {
 }
 
 
+_I64x4 = ctypes.c_int64 * 4
+_PAD = ((), (0,), (0, 0), (0, 0, 0), (0, 0, 0, 0))
+
+
 def _desc(t):
+    """The mla_tensor_t of a torch tensor: pointer, dtype, shape and strides (elements)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError("expected a torch.Tensor")
-    if t.dim() > 4:
+    shape = t.shape
+    n = len(shape)
+    if n > 4:
         raise ValueError("at most 4 dimensions")
     try:
         code = _DTYPES[t.dtype]
     except KeyError:
         raise TypeError(f"unsupported dtype {t.dtype}") from None
-    d = MlaTensor()
-    d.ptr = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
-    d.ndim = t.dim()
-    d.dtype = code
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    pad = _PAD[4 - n]
+    return MlaTensor(t.data_ptr() or None, n, code, _I64x4(*shape, *pad),
+                     _I64x4(*t.stride(), *pad))
 
 
 def _ref(d):
@@ -203,6 +205,52 @@ def mla_decode_shared_prefix(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
         workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     _check(rc, "mla_decode_shared_prefix")
     return workspace
+
+
+class PreparedDecode:
+    """One mla_decode (or, with shared_prefix_len, mla_decode_shared_prefix) call whose
+    argument descriptors are built once, for a caller that runs the same buffers every step
+    (fresh data in the same tensors).  run() enqueues the call through the C ABI with no
+    per-call argument marshalling.  The descriptors hold the tensors' addresses, shapes and
+    strides as they were here: prepare again after reallocating or reshaping any of them.
+    The object keeps the tensors alive.
+    """
+
+    def __init__(self, q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                 max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits=0, lse_out=None,
+                 workspace=None, shared_prefix_len=None, stream=None):
+        shared = shared_prefix_len is not None
+        if workspace is None:
+            workspace = make_workspace(len(kv_indptr) - 1, q.shape[1], max_seqlen_q,
+                                       0 if shared else num_kv_splits, q.device,
+                                       shared_prefix=shared)
+        self.workspace = workspace
+        self._keep = (q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                      q_scale, kv_scale, lse_out, workspace)
+        self._descs = [_desc(t) for t in self._keep[:10]]
+        r = [_ref(d) for d in self._descs]
+        tail = (ctypes.c_void_p(workspace.data_ptr()),
+                ctypes.c_size_t(workspace.numel() * workspace.element_size()))
+        if shared:
+            self._fn, self._where = _lib.mla_decode_shared_prefix, "mla_decode_shared_prefix"
+            self._args = (r[0], r[1], r[2], r[3], r[4], r[5], r[6], int(max_seqlen_q),
+                          float(sm_scale), r[7], r[8], int(shared_prefix_len), r[9]) + tail
+        else:
+            self._fn, self._where = _lib.mla_decode, "mla_decode"
+            self._args = (r[0], r[1], r[2], r[3], r[4], r[5], r[6], int(max_seqlen_q),
+                          float(sm_scale), r[7], r[8], int(num_kv_splits), r[9]) + tail
+        self._device = q.device
+        self._stream = None if stream is None else _stream(stream, q.device)
+
+    def run(self, stream=None):
+        """Enqueue the call on `stream` (default: the stream given when prepared, else
+        torch's current stream)."""
+        st = _stream(stream, self._device) if stream is not None else (
+            self._stream if self._stream is not None else _stream(None, self._device))
+        rc = self._fn(*self._args, st)
+        if rc != 0:
+            raise MlaError(rc, self._where)
+        return self.workspace
 
 
 def mla_decode_noalloc(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,

@@ -181,6 +181,34 @@ def test_shared_prefix_cascade(pm, kv_lens, q_lens, prefix, scales):
     gu.compare(o, lse, o_ref, lse_ref, what="cascade")
 
 
+@pytest.mark.parametrize("shared", [None, 2048])
+def test_prepared_call(pm, shared):
+    """PreparedDecode: descriptors built once, run() twice; the second run after new q
+    data written in place gives that data's answer, equal to the one-shot call's."""
+    case = gu.to_device(mla_inputs.make_custom([3000, 3100, 2900, 3050, 3200], H=12, seed=34,
+                                               shared_prefix=2048 if shared else 0,
+                                               q_scale=1.0, kv_scale=1.0, name="prepared"))
+    n_tok = case.q.shape[0]
+    q = case.q.clone()
+    o = torch.empty((n_tok, 12, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((n_tok, 12), dtype=torch.float32, device="cuda")
+    prep = pm.PreparedDecode(q, case.kv, o, case.qo_indptr, case.kv_indptr, case.kv_indices,
+                             case.kv_last_page_lens, case.max_seqlen_q, case.sm_scale,
+                             case.q_scale, case.kv_scale, lse_out=lse, shared_prefix_len=shared)
+    prep.run()
+    torch.cuda.synchronize()
+    o_one, lse_one, st = gu.run_gpu(case, shared_prefix=shared)
+    assert st == 0 and pm.mla_check_error(prep.workspace) == 0
+    assert torch.equal(o, o_one) and torch.equal(lse, lse_one)
+    q2 = torch.flip(case.q, dims=[1]).contiguous()
+    q.copy_(q2)
+    prep.run()
+    torch.cuda.synchronize()
+    o2, lse2, st2 = gu.run_gpu(case, shared_prefix=shared, q_override=q2)
+    assert st2 == 0 and torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert not torch.equal(o2, o_one)
+
+
 def test_shared_prefix_with_the_plain_workspace(pm):
     """With only the plain decode's workspace the call runs the plain decode: same answer."""
     case = gu.to_device(mla_inputs.make_custom([3000] * 5, H=12, seed=32, shared_prefix=2500,
