@@ -784,9 +784,9 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           }
           if (ok && pend) pv_step();
         } else {
-          // With two stages, QK(i+1) needs the stage PV(i-1) is about to release: a fixed
-          // order would idle the tensor pipe on that reload, so issue whichever step is
-          // ready first.
+          // (Rings of two stages; no current instantiation.)  With two stages, QK(i+1)
+          // needs the stage PV(i-1) is about to release: a fixed order would idle the tensor
+          // pipe on that reload, so issue whichever step is ready first.
           // Issue loop.  QK of tile q needs its cache rows (full), the piece's q rows and a
           // free S buffer (PV of tile q-2 issued); PV of tile p needs P (p_full).  Whichever
           // is ready goes first, PV preferred: it releases a ring stage to the producers.
