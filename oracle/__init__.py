@@ -20,6 +20,9 @@ table, §5.2 page_size = 1; "Scaling Kimi K3 on AMD Instinct MI355X", §1 DCP me
   merge of partials (o_i, lse_i):  M = max lse_i, w_i = exp(lse_i - M),
     o = sum w_i o_i / sum w_i,  lse = M + ln sum w_i.
 
+Paged caches (page_size > 1) are reduced to this token view by expand_pages: a request's
+positions are its pages' slots in order, the last page holding last_page_lens[b] of them.
+
 Every function has a pin in ``tests/test_oracle_pins.py`` (brute force, closed forms,
 invariants); none is "parity unpinned".
 """
@@ -171,6 +174,45 @@ def decode(q, kv, qo_indptr, kv_indptr, kv_indices, sm_scale, q_scale, kv_scale,
     if rc != 0:
         raise ValueError(f"oracle decode failed with status {rc}")
     return o, lse
+
+
+def expand_pages(kv_indptr, kv_indices, last_page_lens, page_size: int):
+    """Token view of a paged cache: request b holds pages kv_indices[kv_indptr[b] ..
+    kv_indptr[b+1]) in order; every page but the last contributes its page_size slots,
+    the last one its first last_page_lens[b] slots; slot s of page p is cache row
+    p * page_size + s.  Returns (token indptr (B+1,), row ids) as int32 arrays.
+
+    ("[Kimi-K3 MLA TP8] MLA performance" §5.2: page-granular addressing of the same cache,
+    page_size = the allocator's block size; a request's length is
+    (pages - 1) * page_size + last_page_len.)
+    """
+    kvp = np.asarray(kv_indptr, dtype=np.int64)
+    idx = np.asarray(kv_indices, dtype=np.int64)
+    last = np.asarray(last_page_lens, dtype=np.int64)
+    B = kvp.size - 1
+    ptr = [0]
+    rows = []
+    for b in range(B):
+        pages = idx[kvp[b]:kvp[b + 1]]
+        n = 0
+        for i, pg in enumerate(pages):
+            used = page_size if i + 1 < pages.size else int(last[b])
+            if not 1 <= used <= page_size:
+                raise ValueError("last_page_lens must lie in [1, page_size]")
+            rows.extend(int(pg) * page_size + s for s in range(used))
+            n += used
+        ptr.append(ptr[-1] + n)
+    return (np.asarray(ptr, dtype=np.int32),
+            np.asarray(rows if rows else [0], dtype=np.int32))
+
+
+def decode_paged(q, kv_pages, qo_indptr, kv_indptr, kv_indices, last_page_lens, page_size,
+                 sm_scale, q_scale, kv_scale, n_threads: int = 0):
+    """decode() of a paged cache: kv_pages (N_pages, page_size, 576) (or with a head axis),
+    kv_indptr in pages, kv_indices page ids, last_page_lens the last page's valid slots."""
+    tok_ptr, rows = expand_pages(kv_indptr, kv_indices, last_page_lens, page_size)
+    kv = _u8(kv_pages).reshape(-1, D)
+    return decode(q, kv, qo_indptr, tok_ptr, rows, sm_scale, q_scale, kv_scale, n_threads)
 
 
 def merge(o_parts, lse_parts):

@@ -305,3 +305,68 @@ def test_workload_shapes():
     assert all(68000 <= L < 68350 for L in lens)
     m = mla_inputs._mtp_lens(64, 0)
     assert all(2048 <= L <= 65536 for L in m)
+
+
+# ---------------------------------------------------------------- paged caches (page_size > 1)
+
+def test_expand_pages_hand_example():
+    """Pages [3, 0] with 2 slots used in the last, then page [5] full, at 4 slots a page."""
+    ptr, rows = oracle.expand_pages([0, 2, 3], [3, 0, 5], [2, 4], 4)
+    assert ptr.tolist() == [0, 6, 10]
+    assert rows.tolist() == [12, 13, 14, 15, 0, 1, 20, 21, 22, 23]
+    with pytest.raises(ValueError):
+        oracle.expand_pages([0, 1], [0], [5], 4)      # more slots than a page holds
+    with pytest.raises(ValueError):
+        oracle.expand_pages([0, 1], [0], [0], 4)      # an empty last page
+
+
+def _paged_case(seed, page_size, lens, q_lens, H=3, n_pages=40):
+    rng = np.random.default_rng(seed)
+    kv = _rows(rng, n_pages * page_size).reshape(n_pages, page_size, 576)
+    perm = rng.permutation(n_pages)
+    counts = [(L + page_size - 1) // page_size for L in lens]
+    kvp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    idx = perm[:kvp[-1]].astype(np.int32)
+    last = np.array([L - (c - 1) * page_size for L, c in zip(lens, counts)], dtype=np.int32)
+    qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q = _rows(rng, int(qo[-1]) * H).reshape(int(qo[-1]), H, 576)
+    return q, kv, qo, kvp, idx, last
+
+
+@pytest.mark.parametrize("page_size", [4, 16])
+def test_paged_decode_matches_brute_force(page_size):
+    """Brute force gathers each request's rows by the page axis of the cache
+    (kv[pages].reshape(-1, 576)[:L]), not by row arithmetic."""
+    lens, q_lens = [37, 5, 64, 17], [1, 3, 2, 1]
+    q, kv, qo, kvp, idx, last = _paged_case(11 + page_size, page_size, lens, q_lens)
+    sm, qs, ks = 0.11, 0.8, 0.9
+    o, lse = oracle.decode_paged(q, kv, qo, kvp, idx, last, page_size, sm, qs, ks)
+    for b, (L, T) in enumerate(zip(lens, q_lens)):
+        rows_b = kv[idx[kvp[b]:kvp[b + 1]]].reshape(-1, 576)[:L]
+        for t in range(T):
+            r = qo[b] + t
+            for h in range(q.shape[1]):
+                bo, blse = brute.attend(q[r, h], rows_b[:L - T + t + 1], sm * qs * ks, ks)
+                assert np.allclose(o[r, h], bo, rtol=1e-12, atol=1e-14)
+                assert abs(lse[r, h] - blse) < 1e-12
+
+
+def test_paged_page_size_one_is_the_token_decode():
+    q, kv, qo, kvp, idx, last = _paged_case(5, 1, [9, 30, 2], [1, 2, 1], n_pages=64)
+    a = oracle.decode_paged(q, kv, qo, kvp, idx, last, 1, 0.2, 1.0, 1.0)
+    b = oracle.decode(q, kv.reshape(-1, 576), qo, kvp, idx, 0.2, 1.0, 1.0)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_paged_unused_slots_are_never_attended():
+    """Filling the unused slots of every last page with the largest finite e4m3 value
+    (logits far above the rest) leaves the result unchanged."""
+    page_size, lens = 8, [13, 3, 24]
+    q, kv, qo, kvp, idx, last = _paged_case(7, page_size, lens, [1, 1, 2])
+    base = oracle.decode_paged(q, kv, qo, kvp, idx, last, page_size, 0.3, 1.0, 1.0)
+    kv2 = kv.copy()
+    for b in range(len(lens)):
+        pg = idx[kvp[b + 1] - 1]
+        kv2[pg, last[b]:, :] = 0x7E   # 448
+    poisoned = oracle.decode_paged(q, kv2, qo, kvp, idx, last, page_size, 0.3, 1.0, 1.0)
+    assert np.array_equal(base[0], poisoned[0]) and np.array_equal(base[1], poisoned[1])
