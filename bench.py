@@ -46,6 +46,10 @@ WORKLOAD_TEXT = {
     "long96": "long single request, 96 heads (context-shard reference shape), kv_len 142,000",
     "mtp": "multi-token verification: batch 64, 12 heads, q_len 4 causal, kv_len "
            "log-uniform [2,048, 65,536], 2^22-row fp8 pool",
+    "c16p64": "concurrency-16 decode on 64-token pages: c16's lengths, the shared prefix's "
+              "998 whole pages shared, 82,560-page fp8 pool, plain entry",
+    "longp64": "long single request on 64-token pages: kv_len 142,000 (2,219 pages), "
+               "4,096-page fp8 pool",
 }
 
 
@@ -177,7 +181,12 @@ def oracle_sample(case, n_requests: int, n_heads: int):
     off = 0
     for b in reqs:
         s, e = int(case.kv_indptr[b]), int(case.kv_indptr[b + 1])
-        r = case.kv.index_select(0, case.kv_indices[s:e].long()).cpu().numpy()
+        ps = int(case.meta.get("page_size", 1))
+        ids = case.kv_indices[s:e].long()
+        if ps > 1:   # token rows of the request's pages, in position order
+            ids = (ids[:, None] * ps + torch.arange(ps, device=ids.device)[None, :]).reshape(-1)
+            ids = ids[:case.kv_lens[b]]
+        r = case.kv.reshape(-1, 576).index_select(0, ids).cpu().numpy()
         rows.append(r)
         idx.append(np.arange(off, off + r.shape[0], dtype=np.int32))
         off += r.shape[0]
@@ -285,8 +294,11 @@ def main():
     lse = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
     shared = int(case.meta.get("shared_prefix", 0))
     entry = args.entry
+    paged = int(case.meta.get("page_size", 1)) > 1
     if entry == "auto":
-        entry = "shared_prefix" if shared > 0 and args.num_kv_splits <= 0 else "plain"
+        # the cascade runs on one-token pages only
+        entry = ("shared_prefix" if shared > 0 and args.num_kv_splits <= 0 and not paged
+                 else "plain")
     ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev,
                            shared_prefix=(entry == "shared_prefix"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -417,7 +429,7 @@ def main():
         # The step's inputs sit in one pinned host buffer and go over in one copy; o and
         # lse are written into one device buffer and come back in one copy (the used part
         # of kv_indices only).
-        used = case.total_kv
+        used = int(case.kv_indptr[-1])
         parts = [("q", case.q), ("qo", case.qo_indptr), ("kvp", case.kv_indptr),
                  ("idx", case.kv_indices[:used]), ("last", case.kv_last_page_lens)]
         offs, tot = {}, 0
@@ -511,6 +523,9 @@ def main():
                                            "once for the whole batch), 580 B per row with its "
                                            "index, plus q, o and lse"
                                            if entry == "shared_prefix" else
+                                           ("576 B per attended position plus 4 B per page id "
+                                            "(%d-token pages), plus q, o and lse"
+                                            % int(case.meta["page_size"])) if paged else
                                            "580 B per attended position (row + index), plus q, "
                                            "o and lse")},
             "cpu_baseline": cpu_base,

@@ -164,6 +164,72 @@ def make_custom(kv_lens, q_lens=None, H: int = 12, pool_rows: Optional[int] = No
                    dict(shared_prefix=shared_prefix, pool_rows=pool_rows))
 
 
+def make_paged(kv_lens, q_lens=None, H: int = 12, page_size: int = 64,
+               pool_pages: Optional[int] = None, seed: int = 0, device="cpu",
+               q_scale: float = DEFAULT_Q_SCALE, kv_scale: float = DEFAULT_KV_SCALE,
+               poison: bool = False, shared_prefix: int = 0, index_buffer: int = 0,
+               name: str = "paged") -> Case:
+    """Requests over a cache of page_size-token pages (kv (pool_pages, page_size, 1, 576)).
+
+    kv_indptr counts pages, kv_indices are page ids from a seeded permutation, and
+    kv_last_page_lens[b] = the valid slots of request b's last page, so that
+    kv_lens[b] = (pages_b - 1) * page_size + last_b.  The first shared_prefix tokens (a
+    multiple of page_size) are the same pages in every request.  poison: every slot no
+    request attends, the unused tails of last pages included, holds an e4m3 NaN.
+    """
+    kv_lens = [int(x) for x in kv_lens]
+    B = len(kv_lens)
+    q_lens = [1] * B if q_lens is None else [int(x) for x in q_lens]
+    if shared_prefix % page_size:
+        raise ValueError("a shared prefix of whole pages only")
+    sp = shared_prefix // page_size
+    counts = [(L + page_size - 1) // page_size for L in kv_lens]
+    need = sp + sum(max(c - sp, 0) for c in counts)
+    if pool_pages is None:
+        pool_pages = max(need, 1) + 8
+    if need > pool_pages:
+        raise ValueError("pool too small for the requested lengths")
+    gen = _gen(seed, device)
+    kv = fp8_normal_bytes(pool_pages * page_size * D, gen, device).view(pool_pages, page_size, 1, D)
+    q = fp8_normal_bytes(sum(q_lens) * H * D, gen, device).view(sum(q_lens), H, D)
+    perm = torch.randperm(pool_pages, generator=gen, device=device).to(torch.int32)
+    off = sp
+    parts = []
+    for c in counts:
+        p = min(c, sp)
+        parts.append(perm[:p])
+        parts.append(perm[off:off + c - p])
+        off += c - p
+    pages = torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int32, device=device)
+    kv_indptr = torch.tensor(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32),
+                             device=device)
+    qo_indptr = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
+                             device=device)
+    last = torch.tensor([L - (c - 1) * page_size if c > 0 else 1
+                         for L, c in zip(kv_lens, counts)], dtype=torch.int32, device=device)
+    n_buf = max(int(index_buffer or 0), int(pages.numel()))
+    idx = torch.empty(max(n_buf, 1), dtype=torch.int32, device=device)
+    idx[:pages.numel()] = pages
+    if n_buf > pages.numel():
+        idx[pages.numel():] = (pool_pages + 7) if poison else 0
+    if poison:
+        used = torch.zeros(pool_pages, page_size, dtype=torch.bool, device=device)
+        for b in range(B):
+            pg = idx[int(kv_indptr[b]):int(kv_indptr[b + 1])].long()
+            if pg.numel() == 0:
+                continue
+            used[pg[:-1]] = True
+            used[pg[-1], :int(last[b])] = True
+        kv[~used] = POISON_FP8
+    return Case(name=name, q=q, kv=kv, qo_indptr=qo_indptr, kv_indptr=kv_indptr,
+                kv_indices=idx, kv_last_page_lens=last,
+                q_scale=torch.tensor(q_scale, dtype=torch.float32, device=device),
+                kv_scale=torch.tensor(kv_scale, dtype=torch.float32, device=device),
+                sm_scale=SM_SCALE, kv_lens=kv_lens, q_lens=q_lens,
+                meta=dict(page_size=page_size, shared_prefix=shared_prefix,
+                          pool_pages=pool_pages))
+
+
 def _shared_prefix_lens(B: int, seed: int):
     """kv_len = 63,911 shared + 4,089 unique + U[0, 350) generated (issue §1, §4.1)."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -189,6 +255,11 @@ CONFIGS = {
               "for the 8-shard context-parallel merge)",
     "mtp": "batch 64, 12 heads, q_len 4 (causal within the drafts), kv_len log-uniform "
            "[2,048, 65,536], 2^22-row pool",
+    "c16p64": "c16's lengths on 64-token pages: 82,560-page pool (c16's 5,283,840 rows), "
+              "the 998 whole pages of the shared prefix shared, the rest of each request "
+              "on its own pages, 73,728-entry page-index buffer",
+    "longp64": "long's 142,000 positions on 64-token pages (2,219 pages, the last holding "
+               "48), 4,096-page pool in random page order",
 }
 
 
@@ -227,6 +298,14 @@ def make_case(name: str, seed: int = 0, device="cpu", q_scale: float = DEFAULT_Q
         return make_custom(lens, q_lens=[4] * 64, H=12, pool_rows=1 << 22, seed=seed,
                            device=device, q_scale=q_scale, kv_scale=kv_scale, poison=poison,
                            name=name)
+    if name == "c16p64":
+        return make_paged(_shared_prefix_lens(16, seed), H=12, page_size=64, pool_pages=82_560,
+                          seed=seed, device=device, q_scale=q_scale, kv_scale=kv_scale,
+                          poison=poison, shared_prefix=63_872, index_buffer=73_728, name=name)
+    if name == "longp64":
+        return make_paged([142000], H=12, page_size=64, pool_pages=4096, seed=seed,
+                          device=device, q_scale=q_scale, kv_scale=kv_scale, poison=poison,
+                          name=name)
     raise KeyError(f"unknown workload {name!r}; known: {sorted(CONFIGS)}")
 
 
@@ -265,6 +344,11 @@ def algorithmic_bytes(case: Case, shared_prefix: int = 0) -> int:
     """
     n_rows = int(sum(case.q_lens)) * case.H
     positions = case.total_kv - (case.B - 1) * shared_prefix if shared_prefix > 0 else case.total_kv
+    if int(case.meta.get("page_size", 1)) > 1:
+        # one 4-byte page id per page (requests' pages are distinct, shared prefix or not:
+        # a paged call reads each request's pages, shared ones included)
+        return (D * case.total_kv + 4 * int(case.kv_indptr[-1]) + n_rows * D
+                + n_rows * DV * 2 + n_rows * 4)
     return (580 * positions + n_rows * D + n_rows * DV * 2 + n_rows * 4)
 
 

@@ -19,6 +19,7 @@ constexpr size_t kHeaderBytes = 256;   // device error words live here
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSeqlenQ = 64;
 constexpr int kMaxHeads = 1024;
+constexpr int kMaxPageSize = 1024;   // tokens per page (a power of two)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -121,6 +122,8 @@ int check_lse(const mla_tensor_t* l, int64_t rows, int64_t H) {
 // Shared checks of q / kv_buffer / indptrs.  Fills the sizes it derives.
 struct CallShape {
   int64_t n_tok = 0, H = 0, n_kv_rows = 0, kv_pitch = 0, kv_indices_len = 0;
+  int64_t page_pitch = 0;   // bytes between pages (= kv_pitch for one-token pages)
+  int log2_page = 0;        // pages of 2^log2_page tokens
   int B = 0;
 };
 
@@ -139,20 +142,27 @@ int check_inputs(const mla_tensor_t* q, const mla_tensor_t* kv, const mla_tensor
   if (kv->ndim == 2) {
     if (kv->shape[1] != kD) return MLA_ERR_UNSUPPORTED;
     if (kv->stride[1] != 1) return MLA_ERR_INVALID_ARG;
-    cs->kv_pitch = kv->stride[0];
+    cs->kv_pitch = cs->page_pitch = kv->stride[0];
   } else if (kv->ndim == 4) {
-    // (N_rows, page_size = 1, nhead_kv = 1, 576): issue §4.1 kv_buffer shape
-    if (kv->shape[1] != 1 || kv->shape[2] != 1) return MLA_ERR_UNSUPPORTED;
-    if (kv->shape[3] != kD) return MLA_ERR_UNSUPPORTED;
+    // (N_pages, page_size, nhead_kv = 1, 576): issue §4.1 kv_buffer shape, page_size 1 as
+    // captured (§5.2) or a power of two up to kMaxPageSize (block-granular addressing)
+    const int64_t ps = kv->shape[1];
+    if (kv->shape[2] != 1 || kv->shape[3] != kD) return MLA_ERR_UNSUPPORTED;
+    if (ps < 1 || ps > kMaxPageSize || (ps & (ps - 1)) != 0) return MLA_ERR_UNSUPPORTED;
     if (kv->stride[3] != 1) return MLA_ERR_INVALID_ARG;
-    cs->kv_pitch = kv->stride[0];
+    while ((int64_t{1} << cs->log2_page) < ps) ++cs->log2_page;
+    cs->page_pitch = kv->stride[0];
+    cs->kv_pitch = ps > 1 ? kv->stride[1] : kv->stride[0];
+    if (ps > 1 && (cs->page_pitch % 16 != 0 || cs->page_pitch < (ps - 1) * cs->kv_pitch + kD))
+      return MLA_ERR_INVALID_ARG;   // pages may not overlap
   } else {
     return MLA_ERR_INVALID_ARG;
   }
-  cs->n_kv_rows = kv->shape[0];
-  if (cs->n_kv_rows < 1 || cs->n_kv_rows >= 0x7FFFFFFF) return MLA_ERR_INVALID_ARG;
+  cs->n_kv_rows = kv->shape[0];   // pages
+  if (cs->n_kv_rows < 1 || (cs->n_kv_rows << cs->log2_page) >= 0x7FFFFFFF)
+    return MLA_ERR_INVALID_ARG;   // virtual row ids (page * page_size + slot) fit int32
   if (cs->kv_pitch < kD || cs->kv_pitch % 16 != 0 || !is_aligned(kv->ptr, 16))
-    return MLA_ERR_INVALID_ARG;   // TMA: 16-byte aligned base and row pitch
+    return MLA_ERR_INVALID_ARG;   // 16-byte aligned base and row pitch
   int64_t nq = 0, nk = 0;
   int rc = check_i32_vec(qo_indptr, -1, &nq);
   if (rc) return rc;
@@ -165,6 +175,8 @@ int check_inputs(const mla_tensor_t* q, const mla_tensor_t* kv, const mla_tensor
   if (last_page_lens && last_page_lens->ptr) {
     rc = check_i32_vec(last_page_lens, cs->B, nullptr);
     if (rc) return rc;
+  } else if (cs->log2_page > 0 && cs->B > 0) {
+    return MLA_ERR_INVALID_ARG;   // with pages of several tokens the last page's fill is needed
   }
   return MLA_OK;
 }
@@ -358,8 +370,12 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   prm.sp.gsize = 1;
   prm.sp.shared = 0;
   sched_set_costs(&prm.sp, static_cast<int>(cs.H) * max_seqlen_q);
+  prm.sp.log2_page = cs.log2_page;
+  prm.sp.last_page_lens = (cs.log2_page > 0) ? static_cast<const int32_t*>(kv_last_page_lens->ptr)
+                                             : nullptr;
   prm.kv = static_cast<const uint8_t*>(kv_buffer->ptr);
   prm.kv_pitch = cs.kv_pitch;
+  prm.page_pitch = cs.page_pitch;
   prm.kv_indices = static_cast<const int32_t*>(kv_indices->ptr);
   prm.kv_indices_len = cs.kv_indices_len;
   prm.n_kv_rows = cs.n_kv_rows;
@@ -382,7 +398,8 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   prm.n_slots = plan.slots;
   prm.err = reinterpret_cast<int*>(ws);
 
-  if (plan.cascade_ok && shared_len >= kMinShared && workspace_bytes >= plan.cbytes)
+  if (plan.cascade_ok && cs.log2_page == 0 && shared_len >= kMinShared &&
+      workspace_bytes >= plan.cbytes)
     return launch_cascade(plan, prm, q->ptr, q_rows, shared_len,
                           static_cast<int>(cs.H * max_seqlen_q), stream);
 
@@ -567,6 +584,7 @@ int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
   prm.last_page_lens = (kv_last_page_lens && kv_last_page_lens->ptr)
                            ? static_cast<const int32_t*>(kv_last_page_lens->ptr)
                            : nullptr;
+  prm.log2_page = cs.log2_page;
   prm.B = cs.B;
   prm.n_q_tokens = cs.n_tok;
   prm.kv_indices_len = cs.kv_indices_len;

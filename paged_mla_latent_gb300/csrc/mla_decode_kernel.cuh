@@ -43,11 +43,12 @@ namespace pmla {
 
 struct DecodeParams {
   SchedParams sp;
-  const uint8_t* kv;       // cache rows, 576 bytes each at a pitch of kv_pitch bytes
-  int64_t kv_pitch;
+  const uint8_t* kv;       // cache: slot s of page p at kv + p * page_pitch + s * kv_pitch
+  int64_t kv_pitch;        // bytes between a page's slots (pages of one token: unused)
+  int64_t page_pitch;      // bytes between pages (pages of 2^sp.log2_page tokens)
   const int32_t* kv_indices;
   int64_t kv_indices_len;
-  int64_t n_kv_rows;
+  int64_t n_kv_rows;       // pages in the cache
   int64_t n_q_rows;        // sum_T * H
   const float* q_scale;
   const float* kv_scale;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
     first_qrow = pc.qo0 * prm.sp.H + pc.g * NG;
     // the first tile's row ids: their fetch overlaps the set-up below
     if (threadIdx.x < LY::kTile / 32) {
-      const int64_t gi = pc.kv0 + pc.j0 + 32 * threadIdx.x;
+      const int64_t gi = pc.kv0 + ((pc.j0 + 32 * threadIdx.x) >> prm.sp.log2_page);
       if (gi >= 0 && gi < prm.kv_indices_len) prefetch_l1(prm.kv_indices + gi);
     }
   }
@@ -586,7 +587,15 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
       bool aborted = false;
       Piece pc;
       const uint8_t* kv = prm.kv;
-      const int64_t pitch = prm.kv_pitch;
+      // A row is named by its virtual id page * page_size + slot (one token a page: the
+      // row id itself); its bytes start at kv + page * page_pitch + slot * kv_pitch.
+      const int lg = prm.sp.log2_page;
+      const int smask = (1 << lg) - 1;
+      const int64_t ppitch = prm.page_pitch;
+      const int64_t spitch = prm.kv_pitch;
+      auto row_src = [&](int v) -> const uint8_t* {
+        return kv + static_cast<int64_t>(v >> lg) * ppitch + static_cast<int64_t>(v & smask) * spitch;
+      };
       // Producer pw copies tile rows r = pw + 7 j (j < rows_w); lane j loads row j's id.
       const int rows_w = (LY::kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 19 / 18 (14 / 13)
       while (!aborted && iter.next(pc, &bad)) {
@@ -612,7 +621,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           if (j >= rows_w) return -1;
           const int pos = pc.j0 + t * LY::kTile + pw + kProducerWarps * j;
           if (pos >= pc.j1) return -1;
-          const int64_t gi = kvbase + pos;
+          const int64_t gi = kvbase + (pos >> lg);
           if (gi < 0 || gi >= prm.kv_indices_len) {
             atomicOr(prm.err, kErrBadIndex);
             return -1;
@@ -622,7 +631,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             atomicOr(prm.err, kErrBadRowId);
             return -1;
           }
-          return v;
+          return (v << lg) | (pos & smask);
         };
         int nxt = load_row(0, lane);
         for (int t = 0; t < nt; ++t, ++it_g) {
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const int rid = nxt;
           if (t + 1 < nt) nxt = load_row(t + 1, lane);   // next tile's row ids overlap the wait
           if (t + 2 < nt && lane < rows_w) {   // and the one after is fetched into L1
-            const int64_t gi = kvbase + pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane;
+            const int64_t gi = kvbase + ((pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane) >> lg);
             if (gi >= 0 && gi < prm.kv_indices_len &&
                 pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane < pc.j1)
               prefetch_l1(prm.kv_indices + gi);
@@ -649,7 +658,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           for (int j = 0; j < rows_w; ++j) {
             const int r = pw + kProducerWarps * j;
             const int v = __shfl_sync(0xffffffffu, rid, j);
-            const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 16 * lane;
+            const uint8_t* src = (v >= 0 ? row_src(v) : kv) + 16 * lane;
             const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
             cp_async_16(dst, src, v >= 0 ? 16u : 0u);
           }
@@ -661,7 +670,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             const int v = __shfl_sync(0xffffffffu, rid, j);
             if (j < rows_w) {
               const int r = pw + kProducerWarps * j;
-              const uint8_t* src = kv + (v >= 0 ? static_cast<int64_t>(v) * pitch : 0) + 512 + 16 * c;
+              const uint8_t* src = (v >= 0 ? row_src(v) : kv) + 512 + 16 * c;
               const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
               cp_async_16(dst, src, v >= 0 ? 16u : 0u);
             }

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
   const int T = sp.qo_indptr[b + 1] - sp.qo_indptr[b];
   const int rows = T * sp.H - g * NG;
   if (n >= rows || n >= NG) return;
-  const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+  const int L = sched_real_len<kSchedWhole>(sp, 0, b);
   const int64_t r = static_cast<int64_t>(sp.qo_indptr[b]) * sp.H + static_cast<int64_t>(g) * NG + n;
   if (r < 0 || r >= prm.n_q_rows) {
     if (lead) atomicOr(prm.err, kErrMergeRow);
@@ -444,7 +444,8 @@ struct ValidateParams {
   const int32_t* qo_indptr;
   const int32_t* kv_indptr;
   const int32_t* kv_indices;
-  const int32_t* last_page_lens;   // may be null
+  const int32_t* last_page_lens;   // may be null (pages of one token)
+  int log2_page;                   // kv_indptr counts pages of 2^log2_page tokens
   int B;
   int64_t n_q_tokens;
   int64_t kv_indices_len;
@@ -464,9 +465,13 @@ __global__ void mla_validate_kernel(const ValidateParams prm) {
   }
   for (int64_t b = tid; b < prm.B; b += nth) {
     const int T = prm.qo_indptr[b + 1] - prm.qo_indptr[b];
-    const int L = prm.kv_indptr[b + 1] - prm.kv_indptr[b];
+    const int pages = prm.kv_indptr[b + 1] - prm.kv_indptr[b];
+    const int ps = 1 << prm.log2_page;
+    const int last = prm.last_page_lens ? prm.last_page_lens[b] : 1;
+    if (pages > 0 && (last < 1 || last > ps)) flags |= kErrBadInput;
+    if (ps == 1 && last != 1) flags |= kErrBadInput;
+    const int64_t L = pages > 0 ? (static_cast<int64_t>(pages) - 1) * ps + last : pages;
     if (T < 0 || L < 0 || L < T) flags |= kErrBadInput;
-    if (prm.last_page_lens && prm.last_page_lens[b] != 1) flags |= kErrBadInput;
   }
   int64_t lo = prm.kv_indptr[0], hi = prm.kv_indptr[prm.B];
   if (lo < 0) lo = 0;

@@ -87,6 +87,10 @@ struct SchedParams {
   int w_own;       // per position of a request's (own) positions
   int w_prefix;    // kSchedCascade: per position of a prefix unit
   int piece_cost;  // per (unit, row group): set-up and epilogue of a piece
+  // Paged caches (kSchedWhole only): kv_indptr counts pages of 2^log2_page tokens and the
+  // last page of request b holds last_page_lens[b] of them.  0 / null: one token a page.
+  int log2_page;
+  const int32_t* last_page_lens;
 };
 
 // Cost-line weights the library sets.  A piece's fixed cost (its epilogue, the pipeline's
@@ -147,7 +151,7 @@ PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
     return static_cast<int64_t>(VP) * P + sp.kv_indptr[b] - sp.kv_indptr[0] -
            static_cast<int64_t>(b) * P;
   }
-  return static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0];
+  return (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) << sp.log2_page;
 }
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
@@ -156,7 +160,20 @@ PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
     if (v < VP) return static_cast<int>(P);
     return sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP] - static_cast<int>(P);
   }
-  return sp.kv_indptr[v + 1] - sp.kv_indptr[v];
+  return (sp.kv_indptr[v + 1] - sp.kv_indptr[v]) << sp.log2_page;
+}
+// Positions unit v really holds: its page-rounded length (sched_len) less the unused slots
+// of its last page.  The schedule line is laid out in page-rounded lengths (prefix sums of
+// kv_indptr); pieces and merge ranges are clipped to this.
+template <int MODE = kSchedAny>
+PMLA_HD inline int sched_real_len(const SchedParams& sp, int64_t P, int v) {
+  const int L = sched_len<MODE>(sp, P, v);
+  if (sched_mode<MODE>(sp) != kSchedWhole || sp.log2_page == 0 || L <= 0 || !sp.last_page_lens)
+    return L;
+  const int ps = 1 << sp.log2_page;
+  int last = sp.last_page_lens[v];
+  last = last < 1 ? 1 : (last > ps ? ps : last);   // out of range: flagged by mla_validate
+  return L - ps + last;
 }
 // Cost-line weights of unit v and the fixed cost of a (unit, row group).
 PMLA_HD inline int64_t sched_w_own(const SchedParams& sp) {
@@ -186,7 +203,7 @@ PMLA_HD inline int64_t sched_line(const SchedParams& sp, int64_t P, int v) {
                  static_cast<int64_t>(b) * P);
   }
   return static_cast<int64_t>(v) * e +
-         wo * (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]);
+         wo * ((static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) << sp.log2_page);
 }
 // Positions [0, L) of a (unit, row group) whose line segment starts d before line point
 // x: position j sits at line point e + w j of the segment; returns how many positions lie
@@ -350,22 +367,24 @@ struct PieceIterT {
         const int64_t s0 = base + static_cast<int64_t>(g) * seg;
         const int64_t xe = (s0 + seg < x1) ? s0 + seg : x1;
         const int j0 = line_positions(x - s0, e, w, L);
-        const int j1 = line_positions(xe - s0, e, w, L);
+        const int Lr = sched_real_len<MODE>(sp, P, v);   // <= L: a paged cache's last page
+        const int j1v = line_positions(xe - s0, e, w, L);
+        const int j1 = j1v < Lr ? j1v : Lr;
         x = xe;
         pc.b = v;
         pc.g = g;
         pc.j0 = j0;
         pc.j1 = j1;
-        pc.L = L;
+        pc.L = Lr;
         pc.slot = static_cast<int64_t>(cta) + static_cast<int64_t>(v) * sp.groups + g;
-        pc.direct = (j0 == 0 && j1 == L);
+        pc.direct = (j0 == 0 && j1 == Lr);
       } else {
         if (p >= p_end) return false;
         const int64_t u = p / sp.splits;
         const int k = static_cast<int>(p - u * sp.splits);
         const int v = static_cast<int>(u / sp.groups);
         const int g = static_cast<int>(u - static_cast<int64_t>(v) * sp.groups);
-        const int L = sched_len<MODE>(sp, P, v);
+        const int L = sched_real_len<MODE>(sp, P, v);
         if (L < 0) {
           *bad = 1;
           p = p_end;
@@ -416,8 +435,9 @@ PMLA_HD inline bool unit_partials(const SchedParams& sp, int v, int g, int64_t* 
   const int64_t P = sched_shared<MODE>(sp);
   const int mode = sched_mode<MODE>(sp);
   const int VB = sched_requests<MODE>(sp);
-  const int L = sched_len<MODE>(sp, P, v);
-  if (L <= 0) return false;
+  const int L = sched_len<MODE>(sp, P, v);        // page-rounded: the line's geometry
+  const int Lr = sched_real_len<MODE>(sp, P, v);  // positions the unit holds
+  if (Lr <= 0) return false;
   const bool all_partial = mode != kSchedWhole && P > 0;
   const int64_t u = static_cast<int64_t>(v) * sp.groups + g;
   if (sp.splits <= 0) {
@@ -430,7 +450,7 @@ PMLA_HD inline bool unit_partials(const SchedParams& sp, int v, int g, int64_t* 
     const int64_t s0 = static_cast<int64_t>(sp.groups) * sched_line<MODE>(sp, P, v) +
                        static_cast<int64_t>(g) * (e + w * L);
     const int i0 = auto_cta_of(s0 + e, W, Gp);
-    const int i1 = auto_cta_of(s0 + e + w * (L - 1), W, Gp);
+    const int i1 = auto_cta_of(s0 + e + w * (Lr - 1), W, Gp);
     if (i0 == i1 && !all_partial) return false;
     *first = static_cast<int64_t>(i0) + u;   // CTA i writes unit u's piece to slot i + u
     *count = i1 - i0 + 1;

@@ -50,6 +50,11 @@ def run_gpu(case, num_kv_splits=0, o_dtype=torch.bfloat16, with_lse=True, worksp
 def run_oracle(case, q_override=None):
     sm, qs, ks = case.scales()
     q = (case.q if q_override is None else q_override).cpu().numpy()
+    ps = int(case.meta.get("page_size", 1))
+    if ps > 1:
+        return oracle.decode_paged(q, case.kv.cpu().numpy(), case.qo_indptr.cpu().numpy(),
+                                   case.kv_indptr.cpu().numpy(), case.kv_indices.cpu().numpy(),
+                                   case.kv_last_page_lens.cpu().numpy(), ps, sm, qs, ks)
     return oracle.decode(q, case.kv.cpu().numpy(), case.qo_indptr.cpu().numpy(),
                          case.kv_indptr.cpu().numpy(), case.kv_indices.cpu().numpy(), sm, qs, ks)
 

@@ -133,7 +133,11 @@ def _call(a):
     (dict(q=_t(1 << 40, 3, [2, 12, 576])), 1),                             # q not fp8
     (dict(q=_t(1 << 40, 1, [2, 12, 512])), 2),                             # head dim != 576
     (dict(q=_t((1 << 40) + 8, 1, [2, 12, 576])), 1),                       # q not 16-B aligned
-    (dict(kv=_t((1 << 40) + (1 << 20), 1, [1024, 2, 1, 576])), 2),         # page_size != 1
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [1024, 3, 1, 576])), 2),         # page_size not 2^k
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [4, 2048, 1, 576])), 2),         # page_size > 1024
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [512, 2, 1, 576]), last=None), 1),   # no last lens
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [512, 2, 1, 576], [576, 576, 576, 1])), 1),  # overlap
+    (dict(kv=_t((1 << 40) + (1 << 20), 1, [1 << 24, 256, 1, 576])), 1),    # rows past int32
     (dict(kv=_t((1 << 40) + (1 << 20), 1, [1024, 576], [584, 1])), 1),    # pitch not 16-B multiple
     (dict(o=_t((1 << 40) + (2 << 20), 2, [2, 12, 256])), 1),               # o width != 512
     (dict(o=_t((1 << 40) + (2 << 20), 4, [2, 12, 512])), 1),               # o int32

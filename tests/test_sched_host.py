@@ -48,6 +48,12 @@ def sim():
     ip = ctypes.POINTER(ctypes.c_int)
     lib.sched_host_costs.restype = None
     lib.sched_host_costs.argtypes = [ctypes.c_int] * 3 + [ip, ip, ip]
+    lib.sched_pieces_paged.restype = ctypes.c_int64
+    lib.sched_pieces_paged.argtypes = ([i32p, i32p] + [ctypes.c_int] * 7 + [i32p] +
+                                       [ctypes.c_int] * 2 + [i64p, ctypes.c_int64])
+    lib.sched_unit_partials_paged.restype = ctypes.c_int
+    lib.sched_unit_partials_paged.argtypes = ([i32p, i32p] + [ctypes.c_int] * 7 + [i32p] +
+                                              [ctypes.c_int] * 4 + [i64p, ctypes.POINTER(ctypes.c_int)])
     lib.sched_partial_slots.restype = ctypes.c_int64
     lib.sched_partial_slots.argtypes = [ctypes.c_int] * 4
     return lib
@@ -319,3 +325,87 @@ CASCADE_CASES = [
 @pytest.mark.parametrize("costs", COSTS)
 def test_cascade_halves_cover_every_position_once(sim, kv_lens, q_lens, H, shared, grid, costs):
     check_cascade(sim, kv_lens, q_lens, H, grid, shared, costs)
+
+
+# ------------------------------------------------------------------ paged caches
+
+def check_paged(sim, kv_lens, q_lens, H, page_size, splits, grid, costs=(1, 512)):
+    """kv_indptr in pages of page_size tokens, last page partly filled: the pieces cover
+    each request's real positions [0, L) exactly once, index bases are page bases, causal
+    bases use the real length, and the merge's slot ranges match what the decode wrote."""
+    B = len(kv_lens)
+    counts = [(L + page_size - 1) // page_size for L in kv_lens]
+    kvp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    last = np.array([L - (c - 1) * page_size if c else 1 for L, c in zip(kv_lens, counts)],
+                    dtype=np.int32)
+    qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    rows = max(q_lens) * H
+    NG = pick_ng(rows)
+    groups = (rows + NG - 1) // NG
+    lg = page_size.bit_length() - 1
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    cap = 8 * (grid + B * groups * max(splits, 1) + 16)
+    out = np.zeros(cap * 10, dtype=np.int64)
+    w, e = costs
+    n = sim.sched_pieces_paged(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG,
+                               groups, splits, grid, lg, last.ctypes.data_as(i32p), w, e,
+                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
+    assert n >= 0, f"simulation failed with {n}"
+    pieces = out[:10 * n].reshape(n, 10)
+    by_unit = {}
+    for cta, b, g, j0, j1, prow, slot, direct, kv0, cfrom in pieces:
+        L, T = kv_lens[b], q_lens[b]
+        assert 0 <= j0 < j1 <= L, (b, j0, j1, L)
+        assert kv0 == kvp[b] and cfrom == L - T
+        by_unit.setdefault((b, g), []).append((j0, j1, slot, direct))
+    n_slots = sim.sched_partial_slots(B, groups, splits, grid)
+    for b in range(B):
+        for g in range(groups):
+            real = q_lens[b] * H - g * NG > 0
+            ps = sorted(by_unit.get((b, g), []))
+            if not real or kv_lens[b] == 0:
+                assert not ps
+                continue
+            pos = 0
+            for j0, j1, _, _ in ps:
+                assert j0 == pos, f"gap/overlap in unit {(b, g)}"
+                pos = j1
+            assert pos == kv_lens[b]
+            first, count = ctypes.c_int64(0), ctypes.c_int(0)
+            need = sim.sched_unit_partials_paged(kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p),
+                                                 B, H, NG, groups, splits, grid, lg,
+                                                 last.ctypes.data_as(i32p), w, e, b, g,
+                                                 ctypes.byref(first), ctypes.byref(count))
+            if len(ps) == 1 and ps[0][3]:
+                assert need == 0
+            else:
+                assert need == 1 and not any(p[3] for p in ps)
+                got = {p[2] for p in ps}
+                expect = set(range(first.value, first.value + count.value))
+                if splits <= 0:
+                    assert got == expect
+                else:
+                    assert got <= expect
+                assert all(0 <= s < n_slots for s in got)
+
+
+@pytest.mark.parametrize("page_size", [2, 16, 64, 128])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("grid", [1, 7, 152])
+def test_paged_schedule_covers_real_positions(sim, page_size, splits, grid):
+    check_paged(sim, [1, 2, 127, 128, 129, 3000, 0, 5000], [1, 1, 2, 1, 4, 1, 1, 3], 12,
+                page_size, splits, grid)
+
+
+def test_paged_random_batches(sim):
+    rng = np.random.default_rng(7)
+    for _ in range(30):
+        B = int(rng.integers(1, 12))
+        kv = [int(x) for x in rng.integers(0, 9000, size=B)]
+        q = [int(min(t, L)) if L > 0 else 0 for t, L in zip(rng.integers(1, 5, size=B), kv)]
+        if max(q) == 0:
+            continue
+        ps = int(rng.choice([2, 8, 32, 64, 256]))
+        H = int(rng.choice([12, 16, 96]))
+        for grid in (5, 152):
+            check_paged(sim, kv, q, H, ps, 0, grid)
