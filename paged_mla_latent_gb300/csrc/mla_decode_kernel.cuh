@@ -587,15 +587,13 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
       bool aborted = false;
       Piece pc;
       const uint8_t* kv = prm.kv;
-      // A row is named by its virtual id page * page_size + slot (one token a page: the
-      // row id itself); its bytes start at kv + page * page_pitch + slot * kv_pitch.
+      // Position pos of a request lies in its page pos >> log2_page, slot pos & (size - 1);
+      // the row's bytes start at kv + page * page_pitch + slot * kv_pitch.  Each lane turns
+      // its row into that byte offset once; the copy loops only shuffle it.
       const int lg = prm.sp.log2_page;
       const int smask = (1 << lg) - 1;
       const int64_t ppitch = prm.page_pitch;
       const int64_t spitch = prm.kv_pitch;
-      auto row_src = [&](int v) -> const uint8_t* {
-        return kv + static_cast<int64_t>(v >> lg) * ppitch + static_cast<int64_t>(v & smask) * spitch;
-      };
       // Producer pw copies tile rows r = pw + 7 j (j < rows_w); lane j loads row j's id.
       const int rows_w = (LY::kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 19 / 18 (14 / 13)
       while (!aborted && iter.next(pc, &bad)) {
@@ -616,8 +614,8 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
         aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
         if (aborted) break;
         const int64_t kvbase = pc.kv0;
-        // row id of row j of this warp in tile t (-1: past the piece or invalid)
-        auto load_row = [&](int t, int j) -> int {
+        // byte offset of row j of this warp in tile t (-1: past the piece or invalid)
+        auto load_row = [&](int t, int j) -> int64_t {
           if (j >= rows_w) return -1;
           const int pos = pc.j0 + t * LY::kTile + pw + kProducerWarps * j;
           if (pos >= pc.j1) return -1;
@@ -631,13 +629,15 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             atomicOr(prm.err, kErrBadRowId);
             return -1;
           }
-          return (v << lg) | (pos & smask);
+          return static_cast<int64_t>(v) * ppitch + static_cast<int64_t>(pos & smask) * spitch;
         };
-        int nxt = load_row(0, lane);
+        int64_t nxt = load_row(0, lane);
         for (int t = 0; t < nt; ++t, ++it_g) {
           const int stage = static_cast<int>(it_g % STAGES);
           const uint32_t use = it_g / STAGES;
-          const int rid = nxt;
+          // rows past the piece or invalid copy nothing: a bit mask by row, offsets clamped
+          const uint32_t vmask = __ballot_sync(0xffffffffu, nxt >= 0);
+          const int64_t rid = nxt >= 0 ? nxt : 0;
           if (t + 1 < nt) nxt = load_row(t + 1, lane);   // next tile's row ids overlap the wait
           if (t + 2 < nt && lane < rows_w) {   // and the one after is fetched into L1
             const int64_t gi = kvbase + ((pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane) >> lg);
@@ -657,22 +657,20 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
   #pragma unroll 4
           for (int j = 0; j < rows_w; ++j) {
             const int r = pw + kProducerWarps * j;
-            const int v = __shfl_sync(0xffffffffu, rid, j);
-            const uint8_t* src = (v >= 0 ? row_src(v) : kv) + 16 * lane;
+            const int64_t off = __shfl_sync(0xffffffffu, rid, j);
             const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
-            cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+            cp_async_16(dst, kv + off + 16 * lane, ((vmask >> j) & 1u) << 4);
           }
           // rope columns: 8 rows x 4 chunks per instruction
   #pragma unroll
           for (int m = 0; m < (LY::kRowsPerProducer + 7) / 8; ++m) {
             const int j = 8 * m + (lane >> 2);
             const int c = lane & 3;
-            const int v = __shfl_sync(0xffffffffu, rid, j);
+            const int64_t off = __shfl_sync(0xffffffffu, rid, j);
             if (j < rows_w) {
               const int r = pw + kProducerWarps * j;
-              const uint8_t* src = (v >= 0 ? row_src(v) : kv) + 512 + 16 * c;
               const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-              cp_async_16(dst, src, v >= 0 ? 16u : 0u);
+              cp_async_16(dst, kv + off + 512 + 16 * c, ((vmask >> j) & 1u) << 4);
             }
           }
           cp_async_arrive_noinc(mbase + kMiscFull + 8 * stage);

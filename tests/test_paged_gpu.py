@@ -137,7 +137,9 @@ def test_paged_empty_request(pm):
         one = mla_inputs.Case(**{**case.__dict__})
         one.q, one.kv_lens, one.q_lens = case.q[1:2], [400], [1]
         one.qo_indptr = torch.tensor([0, 1], dtype=torch.int32)
-        one.kv_indptr = case.kv_indptr[:2].cpu()
+        base = int(case.kv_indptr[1])
+        one.kv_indptr = case.kv_indptr[1:3].cpu() - base
+        one.kv_indices = case.kv_indices[base:].cpu()
         one.kv_last_page_lens = case.kv_last_page_lens[1:2].cpu()
         o_ref, lse_ref = gu.run_oracle(one)
         gu.compare(o[1:2], lse[1:2], o_ref, lse_ref, what="paged-empty")
