@@ -46,10 +46,10 @@ WORKLOAD_TEXT = {
     "long96": "long single request, 96 heads (context-shard reference shape), kv_len 142,000",
     "mtp": "multi-token verification: batch 64, 12 heads, q_len 4 causal, kv_len "
            "log-uniform [2,048, 65,536], 2^22-row fp8 pool",
-    "c16p64": "concurrency-16 decode on 64-token pages: c16's lengths, the shared prefix's "
-              "998 whole pages shared, 82,560-page fp8 pool, plain entry",
-    "longp64": "long single request on 64-token pages: kv_len 142,000 (2,219 pages), "
-               "4,096-page fp8 pool",
+    "c16p128": "concurrency-16 decode on 128-token pages: c16's lengths, the shared "
+               "prefix's 499 whole pages shared, 41,280-page fp8 pool",
+    "longp128": "long single request on 128-token pages: kv_len 142,000 (1,110 pages), "
+                "2,048-page fp8 pool",
 }
 
 
@@ -296,9 +296,7 @@ def main():
     entry = args.entry
     paged = int(case.meta.get("page_size", 1)) > 1
     if entry == "auto":
-        # the cascade runs on one-token pages only
-        entry = ("shared_prefix" if shared > 0 and args.num_kv_splits <= 0 and not paged
-                 else "plain")
+        entry = "shared_prefix" if shared > 0 and args.num_kv_splits <= 0 else "plain"
     ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev,
                            shared_prefix=(entry == "shared_prefix"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -418,7 +416,9 @@ def main():
             raise RuntimeError(f"device error in the plain timing: {pm.mla_status_string(st)}")
 
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
-    algo = mla_inputs.algorithmic_bytes(case, shared if entry == "shared_prefix" else 0)
+    # the shared prefix's rows count once where the call is told of it, and on paged caches,
+    # whose shared pages are the same memory in every request
+    algo = mla_inputs.algorithmic_bytes(case, shared if (entry == "shared_prefix" or paged) else 0)
     value = whole_job_rate(world, gathered, mean_ms)
     peak, peak_kind = measured_peaks()
     achieved = algo / (mean_ms * 1e-3) / 1e9
@@ -519,13 +519,14 @@ def main():
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": recorded_traffic(args.config, entry),
-                         "bytes_counted": ("each distinct cache row once (the shared prefix's rows "
+                         "bytes_counted": (("576 B per distinct cache row (the %d shared-prefix "
+                                            "positions' pages once), 4 B per page id of every "
+                                            "request (%d-token pages), plus q, o and lse"
+                                            % (shared, int(case.meta["page_size"]))) if paged else
+                                           "each distinct cache row once (the shared prefix's rows "
                                            "once for the whole batch), 580 B per row with its "
                                            "index, plus q, o and lse"
                                            if entry == "shared_prefix" else
-                                           ("576 B per attended position plus 4 B per page id "
-                                            "(%d-token pages), plus q, o and lse"
-                                            % int(case.meta["page_size"])) if paged else
                                            "580 B per attended position (row + index), plus q, "
                                            "o and lse")},
             "cpu_baseline": cpu_base,

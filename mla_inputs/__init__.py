@@ -255,11 +255,11 @@ CONFIGS = {
               "for the 8-shard context-parallel merge)",
     "mtp": "batch 64, 12 heads, q_len 4 (causal within the drafts), kv_len log-uniform "
            "[2,048, 65,536], 2^22-row pool",
-    "c16p64": "c16's lengths on 64-token pages: 82,560-page pool (c16's 5,283,840 rows), "
-              "the 998 whole pages of the shared prefix shared, the rest of each request "
-              "on its own pages, 73,728-entry page-index buffer",
-    "longp64": "long's 142,000 positions on 64-token pages (2,219 pages, the last holding "
-               "48), 4,096-page pool in random page order",
+    "c16p128": "c16's lengths on 128-token pages (the allocator's block size): 41,280-page "
+               "pool (c16's 5,283,840 rows), the shared prefix's 499 whole pages shared, the "
+               "rest of each request on its own pages, 36,864-entry page-index buffer",
+    "longp128": "long's 142,000 positions on 128-token pages (1,110 pages, the last holding "
+                "48), 2,048-page pool in random page order",
 }
 
 
@@ -298,12 +298,12 @@ def make_case(name: str, seed: int = 0, device="cpu", q_scale: float = DEFAULT_Q
         return make_custom(lens, q_lens=[4] * 64, H=12, pool_rows=1 << 22, seed=seed,
                            device=device, q_scale=q_scale, kv_scale=kv_scale, poison=poison,
                            name=name)
-    if name == "c16p64":
-        return make_paged(_shared_prefix_lens(16, seed), H=12, page_size=64, pool_pages=82_560,
+    if name == "c16p128":
+        return make_paged(_shared_prefix_lens(16, seed), H=12, page_size=128, pool_pages=41_280,
                           seed=seed, device=device, q_scale=q_scale, kv_scale=kv_scale,
-                          poison=poison, shared_prefix=63_872, index_buffer=73_728, name=name)
-    if name == "longp64":
-        return make_paged([142000], H=12, page_size=64, pool_pages=4096, seed=seed,
+                          poison=poison, shared_prefix=63_872, index_buffer=36_864, name=name)
+    if name == "longp128":
+        return make_paged([142000], H=12, page_size=128, pool_pages=2048, seed=seed,
                           device=device, q_scale=q_scale, kv_scale=kv_scale, poison=poison,
                           name=name)
     raise KeyError(f"unknown workload {name!r}; known: {sorted(CONFIGS)}")
@@ -345,9 +345,9 @@ def algorithmic_bytes(case: Case, shared_prefix: int = 0) -> int:
     n_rows = int(sum(case.q_lens)) * case.H
     positions = case.total_kv - (case.B - 1) * shared_prefix if shared_prefix > 0 else case.total_kv
     if int(case.meta.get("page_size", 1)) > 1:
-        # one 4-byte page id per page (requests' pages are distinct, shared prefix or not:
-        # a paged call reads each request's pages, shared ones included)
-        return (D * case.total_kv + 4 * int(case.kv_indptr[-1]) + n_rows * D
+        # 576 B per distinct cache row (shared pages once) and 4 B per page id of every
+        # request (each request names its pages, shared ones included)
+        return (D * positions + 4 * int(case.kv_indptr[-1]) + n_rows * D
                 + n_rows * DV * 2 + n_rows * 4)
     return (580 * positions + n_rows * D + n_rows * DV * 2 + n_rows * 4)
 

@@ -398,9 +398,11 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   prm.n_slots = plan.slots;
   prm.err = reinterpret_cast<int*>(ws);
 
-  if (plan.cascade_ok && cs.log2_page == 0 && shared_len >= kMinShared &&
-      workspace_bytes >= plan.cbytes)
-    return launch_cascade(plan, prm, q->ptr, q_rows, shared_len,
+  // On pages of several tokens the prefix units take the shared prefix's whole pages
+  // (positions past the last whole page go with each request's own positions).
+  const int32_t shared_whole = shared_len & ~((int32_t{1} << cs.log2_page) - 1);
+  if (plan.cascade_ok && shared_whole >= kMinShared && workspace_bytes >= plan.cbytes)
+    return launch_cascade(plan, prm, q->ptr, q_rows, shared_whole,
                           static_cast<int>(cs.H * max_seqlen_q), stream);
 
   switch (plan.NG) {

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
   const int T = sp.qo_indptr[b + 1] - sp.qo_indptr[b];
   const int rows = T * sp.H - g * NG;
   if (n >= rows || n >= NG) return;
-  const int L = sched_real_len<kSchedWhole>(sp, 0, b);
+  const int L = sched_req_len(sp, b);
   const int64_t r = static_cast<int64_t>(sp.qo_indptr[b]) * sp.H + static_cast<int64_t>(g) * NG + n;
   if (r < 0 || r >= prm.n_q_rows) {
     if (lead) atomicOr(prm.err, kErrMergeRow);
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
     return;
   }
   const int64_t shared = sched_shared<kSchedCascade>(sp);
-  const int L = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+  const int L = sched_req_len(sp, b);
   if (L - shared < T - 1 && lead)
     atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
   const int VP = sched_prefix_units(sp);

@@ -87,8 +87,9 @@ struct SchedParams {
   int w_own;       // per position of a request's (own) positions
   int w_prefix;    // kSchedCascade: per position of a prefix unit
   int piece_cost;  // per (unit, row group): set-up and epilogue of a piece
-  // Paged caches (kSchedWhole only): kv_indptr counts pages of 2^log2_page tokens and the
-  // last page of request b holds last_page_lens[b] of them.  0 / null: one token a page.
+  // Paged caches: kv_indptr counts pages of 2^log2_page tokens and the last page of request
+  // b holds last_page_lens[b] of them (0 / null: one token a page).  kSchedCascade: the
+  // shared prefix P is a whole number of pages.
   int log2_page;
   const int32_t* last_page_lens;
 };
@@ -148,32 +149,49 @@ PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
     const int VP = sched_prefix_units(sp);
     if (v <= VP) return static_cast<int64_t>(v) * P;
     const int b = v - VP;
-    return static_cast<int64_t>(VP) * P + sp.kv_indptr[b] - sp.kv_indptr[0] -
+    return static_cast<int64_t>(VP) * P +
+           (static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0]) * (int64_t{1} << sp.log2_page) -
            static_cast<int64_t>(b) * P;
   }
-  return (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) << sp.log2_page;
+  return (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) * (int64_t{1} << sp.log2_page);
 }
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
     if (v < VP) return static_cast<int>(P);
-    return sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP] - static_cast<int>(P);
+    return (sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP]) * (1 << sp.log2_page) -
+           static_cast<int>(P);
   }
-  return (sp.kv_indptr[v + 1] - sp.kv_indptr[v]) << sp.log2_page;
+  return (sp.kv_indptr[v + 1] - sp.kv_indptr[v]) * (1 << sp.log2_page);
 }
 // Positions unit v really holds: its page-rounded length (sched_len) less the unused slots
-// of its last page.  The schedule line is laid out in page-rounded lengths (prefix sums of
-// kv_indptr); pieces and merge ranges are clipped to this.
+// of its request's last page (a prefix unit's P positions are whole pages).  The schedule
+// line is laid out in page-rounded lengths (prefix sums of kv_indptr); pieces and merge
+// ranges are clipped to this.
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_real_len(const SchedParams& sp, int64_t P, int v) {
   const int L = sched_len<MODE>(sp, P, v);
-  if (sched_mode<MODE>(sp) != kSchedWhole || sp.log2_page == 0 || L <= 0 || !sp.last_page_lens)
-    return L;
+  if (sp.log2_page == 0 || L <= 0 || !sp.last_page_lens) return L;
+  int b = v;
+  if (sched_mode<MODE>(sp) == kSchedCascade) {
+    const int VP = sched_prefix_units(sp);
+    if (v < VP) return L;
+    b = v - VP;
+  }
   const int ps = 1 << sp.log2_page;
-  int last = sp.last_page_lens[v];
+  int last = sp.last_page_lens[b];
   last = last < 1 ? 1 : (last > ps ? ps : last);   // out of range: flagged by mla_validate
   return L - ps + last;
+}
+// Tokens request b holds (its pages' slots less the unused ones of its last page).
+PMLA_HD inline int sched_req_len(const SchedParams& sp, int b) {
+  const int pages = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
+  const int ps = 1 << sp.log2_page;
+  if (ps == 1 || pages <= 0 || !sp.last_page_lens) return pages * ps;
+  int last = sp.last_page_lens[b];
+  last = last < 1 ? 1 : (last > ps ? ps : last);
+  return (pages - 1) * ps + last;
 }
 // Cost-line weights of unit v and the fixed cost of a (unit, row group).
 PMLA_HD inline int64_t sched_w_own(const SchedParams& sp) {
@@ -199,11 +217,13 @@ PMLA_HD inline int64_t sched_line(const SchedParams& sp, int64_t P, int v) {
     if (v <= VP) return static_cast<int64_t>(v) * unit_p;
     const int b = v - VP;
     return static_cast<int64_t>(VP) * unit_p + static_cast<int64_t>(b) * e +
-           wo * (static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0] -
+           wo * ((static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0]) *
+                     (int64_t{1} << sp.log2_page) -
                  static_cast<int64_t>(b) * P);
   }
   return static_cast<int64_t>(v) * e +
-         wo * ((static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) << sp.log2_page);
+         wo * ((static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) *
+               (int64_t{1} << sp.log2_page));
 }
 // Positions [0, L) of a (unit, row group) whose line segment starts d before line point
 // x: position j sits at line point e + w j of the segment; returns how many positions lie
@@ -220,7 +240,7 @@ PMLA_HD inline int64_t sched_kv0(const SchedParams& sp, int64_t P, int v) {
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
     if (v < VP) return sp.kv_indptr[v * sp.gsize];
-    return static_cast<int64_t>(sp.kv_indptr[v - VP]) + P;
+    return static_cast<int64_t>(sp.kv_indptr[v - VP]) + (P >> sp.log2_page);   // P: whole pages
   }
   return sp.kv_indptr[v];
 }

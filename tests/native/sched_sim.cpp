@@ -139,6 +139,51 @@ int sched_unit_partials_paged(const int32_t* kv_indptr, const int32_t* qo_indptr
   return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
 }
 
+// Every field: any mode on a paged cache.  10 int64 per piece as sched_pieces_mode.
+int64_t sched_pieces_full(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H,
+                          int NG, int groups, int splits, int grid, int mode, int gsize,
+                          int shared, int w_own, int w_prefix, int piece_cost, int log2_page,
+                          const int32_t* last_page_lens, int64_t* out, int64_t max_out) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared,
+                       w_own, w_prefix, piece_cost, log2_page, last_page_lens};
+  int64_t n = 0;
+  for (int cta = 0; cta < grid; ++cta) {
+    pmla::PieceIter it;
+    it.init(sp, cta);
+    pmla::Piece pc;
+    int bad = 0;
+    while (it.next(pc, &bad)) {
+      if (n >= max_out) return -1;
+      int64_t* o = out + 10 * n;
+      o[0] = cta; o[1] = pc.b; o[2] = pc.g; o[3] = pc.j0; o[4] = pc.j1; o[5] = pc.rows;
+      o[6] = pc.slot; o[7] = pc.direct ? 1 : 0; o[8] = pc.kv0; o[9] = pc.cfrom;
+      ++n;
+    }
+    if (bad) return -2;
+  }
+  return n;
+}
+
+int sched_unit_partials_full(const int32_t* kv_indptr, const int32_t* qo_indptr, int B, int H,
+                             int NG, int groups, int splits, int grid, int mode, int gsize,
+                             int shared, int w_own, int w_prefix, int piece_cost, int log2_page,
+                             const int32_t* last_page_lens, int v, int g, int64_t* first,
+                             int* count) {
+  pmla::SchedParams sp{kv_indptr, qo_indptr, B, H, NG, groups, splits, grid, mode, gsize, shared,
+                       w_own, w_prefix, piece_cost, log2_page, last_page_lens};
+  return pmla::unit_partials(sp, v, g, first, count) ? 1 : 0;
+}
+
+// Tokens request b holds, as the merge kernels read it.
+int sched_request_len(const int32_t* kv_indptr, int log2_page, const int32_t* last_page_lens,
+                      int b) {
+  pmla::SchedParams sp{};
+  sp.kv_indptr = kv_indptr;
+  sp.log2_page = log2_page;
+  sp.last_page_lens = last_page_lens;
+  return pmla::sched_req_len(sp, b);
+}
+
 // The weights the library sets for a call (mode, group rows NG, query rows per request).
 void sched_host_costs(int mode, int NG, int rows_per_request, int* w_own, int* w_prefix,
                       int* piece_cost) {

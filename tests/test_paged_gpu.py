@@ -70,13 +70,36 @@ def test_paged_index_buffer_tail(pm):
     _check(case)
 
 
-def test_shared_prefix_entry_on_paged_cache(pm):
-    """The cascade needs one token a page; on larger pages the shared-prefix entry point
-    runs the plain schedule and still agrees with the oracle."""
-    case = mla_inputs.make_paged([2048 + 100 * i + 7 for i in range(16)], H=12, page_size=64,
-                                 seed=11, q_scale=1.0, kv_scale=1.0, poison=True,
-                                 shared_prefix=2048, name="paged-shared")
-    _check(case, shared_prefix=2048)
+@pytest.mark.parametrize("page_size,call_prefix", [(64, 2048), (64, 2000), (128, 2048),
+                                                   (16, 1030), (1024, 2048)])
+@pytest.mark.parametrize("scales", [(0.05, 0.1), (1.0, 1.0)])
+def test_shared_prefix_cascade_on_pages(pm, page_size, call_prefix, scales):
+    """The cascade over whole shared pages: the prefix units take the largest whole number
+    of pages within the declared prefix (2000 -> 31 pages of 64; 1030 -> 64 pages of 16)
+    and each request's own units the rest, last page ragged; results as the oracle."""
+    case = mla_inputs.make_paged([2048 + 100 * i + 7 for i in range(16)], H=12,
+                                 page_size=page_size, seed=11 + page_size,
+                                 q_scale=scales[0], kv_scale=scales[1], poison=True,
+                                 shared_prefix=2048, name=f"paged-shared{page_size}")
+    _check(case, shared_prefix=call_prefix)
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 4])
+def test_shared_prefix_cascade_on_pages_with_drafts(pm, q_len):
+    lens = [4096 + 61 * i + q_len for i in range(9)]
+    case = mla_inputs.make_paged(lens, q_lens=[q_len] * 9, H=12, page_size=128, seed=40 + q_len,
+                                 q_scale=1.0, kv_scale=1.0, poison=True, shared_prefix=4096,
+                                 name=f"paged-shared-drafts{q_len}")
+    _check(case, shared_prefix=4096)
+
+
+def test_shared_prefix_below_a_page_runs_plain(pm):
+    """A declared prefix of less than one whole page (1000 positions of 1024-token pages)
+    leaves the cascade nothing to share: the plain decode runs, same results."""
+    case = mla_inputs.make_paged([3000 + 9 * i for i in range(8)], H=12, page_size=1024,
+                                 seed=12, q_scale=1.0, kv_scale=1.0, poison=True,
+                                 shared_prefix=2048, name="paged-shared-small")
+    _check(case, shared_prefix=1000)
 
 
 def test_padded_page_and_slot_pitch(pm):

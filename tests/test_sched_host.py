@@ -54,6 +54,14 @@ def sim():
     lib.sched_unit_partials_paged.restype = ctypes.c_int
     lib.sched_unit_partials_paged.argtypes = ([i32p, i32p] + [ctypes.c_int] * 7 + [i32p] +
                                               [ctypes.c_int] * 4 + [i64p, ctypes.POINTER(ctypes.c_int)])
+    lib.sched_pieces_full.restype = ctypes.c_int64
+    lib.sched_pieces_full.argtypes = ([i32p, i32p] + [ctypes.c_int] * 13 + [i32p] +
+                                      [i64p, ctypes.c_int64])
+    lib.sched_unit_partials_full.restype = ctypes.c_int
+    lib.sched_unit_partials_full.argtypes = ([i32p, i32p] + [ctypes.c_int] * 13 + [i32p] +
+                                             [ctypes.c_int] * 2 + [i64p, ctypes.POINTER(ctypes.c_int)])
+    lib.sched_request_len.restype = ctypes.c_int
+    lib.sched_request_len.argtypes = [i32p, ctypes.c_int, i32p, ctypes.c_int]
     lib.sched_partial_slots.restype = ctypes.c_int64
     lib.sched_partial_slots.argtypes = [ctypes.c_int] * 4
     return lib
@@ -411,3 +419,91 @@ def test_paged_random_batches(sim):
         H = int(rng.choice([12, 16, 96]))
         for grid in (5, 152):
             check_paged(sim, kv, q, H, ps, 0, grid)
+
+
+def _paged_csr(kv_lens, page_size):
+    counts = [(L + page_size - 1) // page_size for L in kv_lens]
+    kvp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    last = np.array([L - (c - 1) * page_size if c else 1 for L, c in zip(kv_lens, counts)],
+                    dtype=np.int32)
+    return kvp, last
+
+
+def test_request_len_reads_pages_and_last_fill(sim):
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    for ps in (1, 2, 64, 1024):
+        lens = [0, 1, ps, ps + 1, 3 * ps - 1, 5000]
+        kvp, last = _paged_csr(lens, ps)
+        lg = ps.bit_length() - 1
+        got = [sim.sched_request_len(kvp.ctypes.data_as(i32p), lg, last.ctypes.data_as(i32p), b)
+               for b in range(len(lens))]
+        assert got == lens
+    # out-of-range fills are clamped to [1, page_size] (mla_validate flags them)
+    kvp = np.array([0, 2, 4], dtype=np.int32)
+    last = np.array([0, 99], dtype=np.int32)
+    got = [sim.sched_request_len(kvp.ctypes.data_as(i32p), 4, last.ctypes.data_as(i32p), b)
+           for b in range(2)]
+    assert got == [17, 32]
+
+
+def check_cascade_paged(sim, kv_lens, q_lens, H, grid, shared, page_size, costs=(1, 0, 512)):
+    """The cascade on a paged cache (P whole pages): prefix units cover [0, P) of their lead
+    request's pages, own units [P, L) of each request's real length, with the own units'
+    index base P / page_size pages into the request, exactly once each."""
+    assert shared % page_size == 0
+    B = len(kv_lens)
+    kvp, last = _paged_csr(kv_lens, page_size)
+    qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    rows = max(q_lens) * H
+    gsize = 48 // rows
+    P = shared
+    VP = (B + gsize - 1) // gsize
+    lg = page_size.bit_length() - 1
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    cap = 8 * (grid + 2 * (VP + B) + 16)
+    out = np.zeros(cap * 10, dtype=np.int64)
+    args = (kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, 48, 1, 0, grid, 1, gsize,
+            shared, *costs, lg, last.ctypes.data_as(i32p))
+    n = sim.sched_pieces_full(*args, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
+    assert n >= 0
+    pieces = out[:10 * n].reshape(n, 10)
+    n_slots = sim.sched_partial_slots(VP + B, 1, 0, grid)
+    cover = {}
+    for cta, v, g, j0, j1, prow, slot, direct, kv0, cfrom in pieces:
+        assert g == 0 and not direct and 0 <= slot < n_slots and j0 < j1
+        if v < VP:
+            assert kv0 == kvp[v * gsize] and cfrom == P and j1 <= P
+        else:
+            b = v - VP
+            Ls = kv_lens[b] - P
+            assert kv0 == kvp[b] + P // page_size and cfrom == Ls - q_lens[b] and j1 <= Ls
+        cover.setdefault(v, []).append((j0, j1, slot))
+    slots = [p[6] for p in pieces]
+    assert len(slots) == len(set(slots))
+    for v in range(VP + B):
+        L = P if v < VP else kv_lens[v - VP] - P
+        ps = sorted(cover.get(v, []))
+        pos = 0
+        for j0, j1, _ in ps:
+            assert j0 == pos
+            pos = j1
+        assert pos == max(L, 0)
+        first, count = ctypes.c_int64(0), ctypes.c_int(0)
+        need = sim.sched_unit_partials_full(*args, v, 0, ctypes.byref(first), ctypes.byref(count))
+        if L <= 0:
+            assert need == 0
+        else:
+            assert need == 1 and {p[2] for p in ps} == set(range(first.value, first.value + count.value))
+
+
+@pytest.mark.parametrize("page_size", [2, 64, 128])
+@pytest.mark.parametrize("grid", [1, 7, 152])
+def test_paged_cascade_covers_every_position_once(sim, page_size, grid):
+    P = (63911 // page_size) * page_size
+    check_cascade_paged(sim, [68000 + 37 * i for i in range(16)], [1] * 16, 12, grid, P, page_size)
+    check_cascade_paged(sim, [5000, 5000, 7000, 6000, 5500], [1] * 5, 12, grid,
+                        (4000 // page_size) * page_size, page_size)
+    check_cascade_paged(sim, [9000] * 4, [2] * 4, 12, grid, (8960 // page_size) * page_size,
+                        page_size)
+    # a request that ends exactly with the prefix (no own positions)
+    check_cascade_paged(sim, [2048, 2500, 4000, 2200, 2600], [1] * 5, 12, grid, 2048, page_size)
