@@ -3,24 +3,31 @@
  *
  * The operation is absorbed (latent) multi-head latent attention decode over a paged
  * FP8 KV cache with page size 1, as captured in "[Kimi-K3 MLA TP8] MLA performance"
- * (ROCm/aiter issue 4541):
+ * (ROCm/aiter issue 4541), or with pages of 2^k tokens (k <= 10), the block-granular
+ * addressing that issue's §5.2 proposes (page_size 128, the allocator's block):
  *   §2 "K3 MLA geometry": every cached token is one 576-wide latent entry (512 latent +
  *      64 rope) shared by all query heads; sm_scale = 1/sqrt(192).
  *   §3 "Entry point": the argument list of the decode call this ABI mirrors, with
  *      page_size = 1 and a single latent KV head.
  *   §4.1 / §4.2 argument tables: q and kv_buffer are float8_e4m3fn, q_scale and kv_scale
  *      are float32 scalars on the device, o is bfloat16 (tokens, heads, 512).
- *   §5.2: kv_indptr holds per-request token counts (CSR), kv_indices one cache row id per
- *      token, kv_last_page_lens is all ones.
+ *   §5.2: with page_size 1, kv_indptr holds per-request token counts (CSR), kv_indices
+ *      one cache row id per token, kv_last_page_lens is all ones.  With page_size PS > 1
+ *      (the paged-attention reading of the same arguments): kv_indptr counts pages,
+ *      kv_indices holds one page id per page, kv_last_page_lens[b] in [1, PS] is the
+ *      number of valid tokens in request b's last page.
  * and the partial-result merge of "Scaling Kimi K3 on AMD Instinct MI355X" §1 "Cache"
  * (decode context parallelism: partial answers carry normalisation information so that
  * a softmax-weighted merge is exact) and §4 "MLA" (history split into partitions).
  *
  * For request b, query token t < T_b = qo_indptr[b+1]-qo_indptr[b], head h:
- *   L_b   = kv_indptr[b+1] - kv_indptr[b]
+ *   n_b   = kv_indptr[b+1] - kv_indptr[b]           (pages)
+ *   L_b   = (n_b - 1) * PS + kv_last_page_lens[b]   (n_b > 0; 0 when n_b = 0;
+ *                                                    = n_b when PS = 1)
+ *   row_j = kv_buffer[kv_indices[kv_indptr[b] + j / PS]][j % PS]   (j < L_b)
  *   J     = { j : 0 <= j <= L_b - T_b + t }      (causal within the draft tokens;
  *                                                  every position when T_b = 1)
- *   s_j   = sm_scale * q_scale * kv_scale * sum_{d<576} q[r,h,d] * kv[kv_indices[kv_indptr[b]+j], d]
+ *   s_j   = sm_scale * q_scale * kv_scale * sum_{d<576} q[r,h,d] * row_j[d]
  *   lse   = ln sum_{j in J} exp(s_j)
  *   o[c]  = kv_scale * sum_{j in J} exp(s_j - lse) * kv[row_j, c],   c < 512
  * with r = qo_indptr[b] + t.  An empty J gives o = 0 and lse = -inf.
@@ -79,7 +86,8 @@ typedef enum {
     MLA_ERR_BAD_INDEX = 5,           /* device-side: index or indptr outside its buffer */
     MLA_ERR_TIMEOUT = 6,             /* device-side: a pipeline wait gave up (no fault) */
     MLA_ERR_BAD_INPUT = 7            /* mla_validate: indptr not monotone, kv_len < q_len,
-                                        or kv_last_page_lens != 1 */
+                                        or kv_last_page_lens outside [1, page_size]
+                                        (!= 1 for one-token pages) */
 } mla_status_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -104,15 +112,19 @@ int mla_get_workspace_size(int32_t batch_size, int32_t num_heads, int32_t max_se
  * Latent-MLA decode.  The first 13 arguments follow the captured decode call (issue §3,
  * §4.1); the last three are this library's.
  *   q                 (sum_T, H, 576) FP8_E4M3FN, contiguous; 16-byte aligned.
- *   kv_buffer         (N_rows, 576) or (N_rows, 1, 1, 576) FP8_E4M3FN; last dim
- *                     contiguous, row stride a multiple of 16 bytes; 16-byte aligned.
+ *   kv_buffer         (N_rows, 576), or (N_pages, PS, 1, 576) FP8_E4M3FN with PS a power
+ *                     of two <= 1024 (PS = 1: one token a page); last dim contiguous,
+ *                     token (slot) stride and page stride multiples of 16 bytes, pages not
+ *                     overlapping; 16-byte aligned; N_pages * PS < 2^31.
  *   o                 (sum_T, H, 512) BF16 or FP32, last dim contiguous (written).
  *   qo_indptr         (B+1,) INT32: query-token CSR; qo_indptr[B] = sum_T.
- *   kv_indptr         (B+1,) INT32: cache-position CSR in tokens (page_size 1).
+ *   kv_indptr         (B+1,) INT32: page CSR (tokens when PS = 1).
  *   kv_indices        (n,) INT32 with n >= kv_indptr[B]; only [kv_indptr[0], kv_indptr[B])
- *                     is read.  Entries must lie in [0, N_rows).
- *   kv_last_page_lens (B,) INT32 or NULL ptr; accepted for interface parity, must be all 1
- *                     (checked by mla_validate only).
+ *                     is read.  Entries (page ids) must lie in [0, N_pages).
+ *   kv_last_page_lens (B,) INT32: valid tokens of each request's last page, in [1, PS].
+ *                     Required when PS > 1 (MLA_ERR_INVALID_ARG if NULL).  With PS = 1 it
+ *                     may be NULL and must be all 1; values outside [1, PS] are clamped by
+ *                     the decode and flagged by mla_validate only.
  *   max_seqlen_q      >= every T_b, 1..64.
  *   sm_scale          softmax scale (1/sqrt(192) for the captured model).
  *   q_scale, kv_scale 0-dim (or 1-element) FP32 device tensors: per-tensor dequant scales.
@@ -143,9 +155,11 @@ int mla_get_shared_prefix_workspace_size(int32_t batch_size, int32_t num_heads,
  * cache pattern of the captured concurrency-16/24 decode steps ("[Kimi-K3 MLA TP8] MLA
  * performance" §1 "Environment", §5.4 "Possible cross-request KV reuse").  Same
  * arguments and results as mla_decode with num_kv_splits = 0, except:
- *   shared_prefix_len  P >= 0: for every request b, kv_indices[kv_indptr[b] + j] is the
- *                      same row for all j < P, and every query sees all P positions
- *                      (P <= kv_len_b - q_len_b + 1).  The caller knows this from its
+ *   shared_prefix_len  P >= 0: for every request b, its first P positions are the same
+ *                      cache rows (with PS > 1: its first floor(P / PS) pages are the same
+ *                      page ids), and every query sees all P positions
+ *                      (P <= kv_len_b - q_len_b + 1).  With PS > 1 the cascade shares the
+ *                      floor(P / PS) whole pages and leaves the rest to each request.  The caller knows this from its
  *                      prefix cache; it is not searched for.  A request breaking the
  *                      second condition is flagged (MLA_ERR_BAD_INPUT through
  *                      mla_check_error); breaking the first gives wrong results.
@@ -157,7 +171,8 @@ int mla_get_shared_prefix_workspace_size(int32_t batch_size, int32_t num_heads,
  * 4 requests at 12 heads and q_len 1), so each shared row is read once per group instead
  * of once per request; each request's own positions run separately and the two halves
  * are merged by their log-sum-exp.  Batches with fewer requests than one group, more
- * than 24 query rows per request, or P < 1024 run the plain decode.
+ * than 24 query rows per request, or fewer than 1024 shared positions (whole pages) run
+ * the plain decode.
  */
 int mla_decode_shared_prefix(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
                              const mla_tensor_t* o, const mla_tensor_t* qo_indptr,
@@ -194,8 +209,9 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
 /*
  * Debug check of a decode call's index inputs on the device, then a host status:
  * MLA_OK, MLA_ERR_BAD_INPUT (indptr not monotone or not starting at 0 for qo, kv_len <
- * q_len, kv_last_page_lens != 1, qo_indptr[B] != sum_T) or MLA_ERR_BAD_INDEX (kv_indptr[B]
- * beyond kv_indices, or an attended index outside [0, N_rows)).  Same arguments as
+ * q_len, kv_last_page_lens outside [1, PS] (!= 1 when PS = 1), qo_indptr[B] != sum_T) or
+ * MLA_ERR_BAD_INDEX (kv_indptr[B] beyond kv_indices, or an attended page id outside
+ * [0, N_pages)).  Same arguments as
  * mla_decode minus the arithmetic ones.  Synchronises `stream`.
  */
 int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,

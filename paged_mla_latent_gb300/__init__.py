@@ -7,8 +7,10 @@ in the library's CUDA kernels; there is no Python or CPU fallback: if the librar
 be loaded, importing this package raises.
 
 The operation ("[Kimi-K3 MLA TP8] MLA performance", §2-§5; "Scaling Kimi K3 on AMD
-Instinct MI355X", §1 and §4): absorbed MLA decode over a page_size=1 FP8 cache, each
-query head scoring every 576-wide latent row, softmax over the request's positions
+Instinct MI355X", §1 and §4): absorbed MLA decode over a paged FP8 cache (one token a
+page as captured, or pages of 2..1024 tokens with kv_indptr counting pages and
+kv_last_page_lens the last page's fill), each query head scoring every 576-wide latent
+row, softmax over the request's positions
 (causal within draft tokens), 512-wide BF16 latent output plus optional FP32 lse, and the
 softmax-weighted merge of split-KV or context-shard partials.
 """
