@@ -241,7 +241,13 @@ struct SplitMergeK {
 };
 template <int P, int U>
 struct CascadeMergeK {
-  static void* fn() { return reinterpret_cast<void*>(mla_cascade_merge_kernel<P, U>); }
+  static void* fn() { return reinterpret_cast<void*>(mla_cascade_merge_kernel<P, U, kSchedCascade>); }
+};
+template <int P, int U>
+struct CascadeMergePagedK {
+  static void* fn() {
+    return reinterpret_cast<void*>(mla_cascade_merge_kernel<P, U, kSchedCascadePaged>);
+  }
 };
 
 template <template <int, int> class K>
@@ -285,7 +291,7 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
   if ((rc = make_map(&p_rope, q_ptr, q_rows, kD, 64, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
   DecodeParams pp = prm;
-  pp.sp.mode = kSchedCascade;
+  pp.sp.mode = pp.sp.log2_page > 0 ? kSchedCascadePaged : kSchedCascade;
   pp.sp.NG = kPrefixNG;
   pp.sp.groups = 1;
   pp.sp.gsize = plan.gsize;
@@ -316,7 +322,9 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   // partials per row: the CTAs one prefix unit spans plus those of the request's own unit
   // (the shape counts the rows that do work: q_rows <= n_rows)
   const MergeShape ms = merge_shape_for(plan.grid / VP + plan.grid / B + 4, q_rows, plan.grid);
-  const cudaError_t e = launch_merge<CascadeMergeK>(ms, n_rows, mp, stream);
+  const cudaError_t e = pp.sp.mode == kSchedCascadePaged
+                            ? launch_merge<CascadeMergePagedK>(ms, n_rows, mp, stream)
+                            : launch_merge<CascadeMergeK>(ms, n_rows, mp, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

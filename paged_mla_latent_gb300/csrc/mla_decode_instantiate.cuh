@@ -31,14 +31,19 @@ int launch_decode_mode(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-// The plain decode, or (CASCADE = kSchedCascade) the shared-prefix cascade.
+// The plain decode, or (CASCADE = kSchedCascade) also the shared-prefix cascade on pages of
+// one token (kSchedCascade) and of several (kSchedCascadePaged).
 template <int NG, int STAGES, int CASCADE>
 int launch_decode_impl(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream) {
   if (prm.sp.mode == kSchedWhole)
     return launch_decode_mode<NG, STAGES, kSchedWhole>(q_lat, q_rope, prm, grid, stream);
-  if (CASCADE != kSchedWhole && prm.sp.mode == CASCADE)
-    return launch_decode_mode<NG, STAGES, CASCADE>(q_lat, q_rope, prm, grid, stream);
+  if constexpr (CASCADE == kSchedCascade) {
+    if (prm.sp.mode == kSchedCascade)
+      return launch_decode_mode<NG, STAGES, kSchedCascade>(q_lat, q_rope, prm, grid, stream);
+    if (prm.sp.mode == kSchedCascadePaged)
+      return launch_decode_mode<NG, STAGES, kSchedCascadePaged>(q_lat, q_rope, prm, grid, stream);
+  }
   return MLA_ERR_UNSUPPORTED;
 }
 

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_split_me
   const int T = sp.qo_indptr[b + 1] - sp.qo_indptr[b];
   const int rows = T * sp.H - g * NG;
   if (n >= rows || n >= NG) return;
-  const int L = sched_req_len(sp, b);
+  const int L = sched_req_len<kSchedWhole>(sp, b);
   const int64_t r = static_cast<int64_t>(sp.qo_indptr[b]) * sp.H + static_cast<int64_t>(g) * NG + n;
   if (r < 0 || r >= prm.n_q_rows) {
     if (lead) atomicOr(prm.err, kErrMergeRow);
@@ -336,7 +336,10 @@ struct CascadeMergeParams {
 // grid = (merge_blocks_x(B * rows_per_req), P / 2), block = 256.  Row rr of request b merges the partials
 // of its group's prefix unit (at row (qo_b - qo_group) H + rr of the group's rows) with
 // those of its own unit (row rr).
-template <int P, int U>
+// M: kSchedCascade (pages of one token, no page arithmetic compiled in; the merge's
+// set-up is on the critical path after the decode grid, and a runtime choice of the two
+// made the c16 call 2 us longer) or kSchedCascadePaged.
+template <int P, int U, int M>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_merge_kernel(const CascadeMergeParams prm) {
   const SchedParams& sp = prm.sp;
   const int NG = sp.NG;
@@ -355,17 +358,17 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeBlocksPerSm) mla_cascade_
     if (lead) atomicOr(prm.err, kErrMergeRow);
     return;
   }
-  const int64_t shared = sched_shared<kSchedCascade>(sp);
-  const int L = sched_req_len(sp, b);
-  if (L - shared < T - 1 && lead)
-    atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
+  const int64_t shared = sched_shared<M>(sp);
   const int VP = sched_prefix_units(sp);
   const int v = b / sp.gsize;
-  const int np = (qo0 - sp.qo_indptr[v * sp.gsize]) * sp.H + rr;
+  const int L = sched_req_len<M>(sp, b);
   int64_t pf = 0, sf = 0;
   int pc = 0, sc = 0;
-  if (!unit_partials<kSchedCascade>(sp, v, 0, &pf, &pc)) pc = 0;
-  if (!unit_partials<kSchedCascade>(sp, VP + b, 0, &sf, &sc)) sc = 0;
+  if (!unit_partials<M>(sp, v, 0, &pf, &pc)) pc = 0;
+  if (!unit_partials<M>(sp, VP + b, 0, &sf, &sc)) sc = 0;
+  if (L - shared < T - 1 && lead)
+    atomicOr(prm.err, kErrBadInput);   // a query would not see the whole shared prefix
+  const int np = (qo0 - sp.qo_indptr[v * sp.gsize]) * sp.H + rr;
   if (np >= NG || rr >= NG || (pc > 0 && (pf < 0 || pf + pc > prm.n_slots)) ||
       (sc > 0 && (sf < 0 || sf + sc > prm.n_slots))) {
     if (lead) atomicOr(prm.err, kErrMergeSlot);

@@ -64,7 +64,10 @@ PMLA_HD inline int groups_for(int rows_per_request, int ng) {
 // Every unit writes partials; the cascade merge combines each row's prefix and own parts.
 // P comes from the caller, who knows its prefix cache (mla_decode_shared_prefix);
 // prefixes shorter than kMinShared are not split off.
-enum : int { kSchedWhole = 0, kSchedCascade = 1 };
+// kSchedCascadePaged is the cascade on pages of several tokens: the same schedule, in its
+// own kernel instantiation, so that the one-token-page cascade carries no page arithmetic
+// (with it, the c16 cascade call took 2 us longer).
+enum : int { kSchedWhole = 0, kSchedCascade = 1, kSchedCascadePaged = 2 };
 constexpr int kMinShared = 1024;
 // The schedule functions take the mode as a template argument: a compile-time mode gives
 // the decode kernel only its own code path (the plain decode carries none of the cascade's
@@ -120,7 +123,13 @@ struct Piece {
 
 template <int MODE>
 PMLA_HD inline int sched_mode(const SchedParams& sp) {
-  return MODE == kSchedAny ? sp.mode : MODE;
+  const int m = MODE == kSchedAny ? sp.mode : MODE;
+  return m == kSchedCascadePaged ? kSchedCascade : m;
+}
+// log2 of the tokens a page: 0 at compile time for the one-token-page cascade.
+template <int MODE>
+PMLA_HD inline int sched_lg(const SchedParams& sp) {
+  return MODE == kSchedCascade ? 0 : sp.log2_page;
 }
 
 // The shared prefix length a schedule uses (0 in whole mode or below kMinShared).
@@ -150,20 +159,20 @@ PMLA_HD inline int64_t sched_cum(const SchedParams& sp, int64_t P, int v) {
     if (v <= VP) return static_cast<int64_t>(v) * P;
     const int b = v - VP;
     return static_cast<int64_t>(VP) * P +
-           (static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0]) * (int64_t{1} << sp.log2_page) -
+           (static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0]) * (int64_t{1} << sched_lg<MODE>(sp)) -
            static_cast<int64_t>(b) * P;
   }
-  return (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) * (int64_t{1} << sp.log2_page);
+  return (static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) * (int64_t{1} << sched_lg<MODE>(sp));
 }
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
     if (v < VP) return static_cast<int>(P);
-    return (sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP]) * (1 << sp.log2_page) -
+    return (sp.kv_indptr[v - VP + 1] - sp.kv_indptr[v - VP]) * (1 << sched_lg<MODE>(sp)) -
            static_cast<int>(P);
   }
-  return (sp.kv_indptr[v + 1] - sp.kv_indptr[v]) * (1 << sp.log2_page);
+  return (sp.kv_indptr[v + 1] - sp.kv_indptr[v]) * (1 << sched_lg<MODE>(sp));
 }
 // Positions unit v really holds: its page-rounded length (sched_len) less the unused slots
 // of its request's last page (a prefix unit's P positions are whole pages).  The schedule
@@ -172,22 +181,23 @@ PMLA_HD inline int sched_len(const SchedParams& sp, int64_t P, int v) {
 template <int MODE = kSchedAny>
 PMLA_HD inline int sched_real_len(const SchedParams& sp, int64_t P, int v) {
   const int L = sched_len<MODE>(sp, P, v);
-  if (sp.log2_page == 0 || L <= 0 || !sp.last_page_lens) return L;
+  if (sched_lg<MODE>(sp) == 0 || L <= 0 || !sp.last_page_lens) return L;
   int b = v;
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
     if (v < VP) return L;
     b = v - VP;
   }
-  const int ps = 1 << sp.log2_page;
+  const int ps = 1 << sched_lg<MODE>(sp);
   int last = sp.last_page_lens[b];
   last = last < 1 ? 1 : (last > ps ? ps : last);   // out of range: flagged by mla_validate
   return L - ps + last;
 }
 // Tokens request b holds (its pages' slots less the unused ones of its last page).
+template <int MODE = kSchedAny>
 PMLA_HD inline int sched_req_len(const SchedParams& sp, int b) {
   const int pages = sp.kv_indptr[b + 1] - sp.kv_indptr[b];
-  const int ps = 1 << sp.log2_page;
+  const int ps = 1 << sched_lg<MODE>(sp);
   if (ps == 1 || pages <= 0 || !sp.last_page_lens) return pages * ps;
   int last = sp.last_page_lens[b];
   last = last < 1 ? 1 : (last > ps ? ps : last);
@@ -218,12 +228,12 @@ PMLA_HD inline int64_t sched_line(const SchedParams& sp, int64_t P, int v) {
     const int b = v - VP;
     return static_cast<int64_t>(VP) * unit_p + static_cast<int64_t>(b) * e +
            wo * ((static_cast<int64_t>(sp.kv_indptr[b]) - sp.kv_indptr[0]) *
-                     (int64_t{1} << sp.log2_page) -
+                     (int64_t{1} << sched_lg<MODE>(sp)) -
                  static_cast<int64_t>(b) * P);
   }
   return static_cast<int64_t>(v) * e +
          wo * ((static_cast<int64_t>(sp.kv_indptr[v]) - sp.kv_indptr[0]) *
-               (int64_t{1} << sp.log2_page));
+               (int64_t{1} << sched_lg<MODE>(sp)));
 }
 // Positions [0, L) of a (unit, row group) whose line segment starts d before line point
 // x: position j sits at line point e + w j of the segment; returns how many positions lie
@@ -240,7 +250,7 @@ PMLA_HD inline int64_t sched_kv0(const SchedParams& sp, int64_t P, int v) {
   if (sched_mode<MODE>(sp) == kSchedCascade) {
     const int VP = sched_prefix_units(sp);
     if (v < VP) return sp.kv_indptr[v * sp.gsize];
-    return static_cast<int64_t>(sp.kv_indptr[v - VP]) + (P >> sp.log2_page);   // P: whole pages
+    return static_cast<int64_t>(sp.kv_indptr[v - VP]) + (P >> sched_lg<MODE>(sp));   // P: whole pages
   }
   return sp.kv_indptr[v];
 }

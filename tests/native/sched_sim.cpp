@@ -181,7 +181,7 @@ int sched_request_len(const int32_t* kv_indptr, int log2_page, const int32_t* la
   sp.kv_indptr = kv_indptr;
   sp.log2_page = log2_page;
   sp.last_page_lens = last_page_lens;
-  return pmla::sched_req_len(sp, b);
+  return pmla::sched_req_len<pmla::kSchedAny>(sp, b);
 }
 
 // The weights the library sets for a call (mode, group rows NG, query rows per request).

@@ -462,7 +462,9 @@ def check_cascade_paged(sim, kv_lens, q_lens, H, grid, shared, page_size, costs=
     i32p = ctypes.POINTER(ctypes.c_int32)
     cap = 8 * (grid + 2 * (VP + B) + 16)
     out = np.zeros(cap * 10, dtype=np.int64)
-    args = (kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, 48, 1, 0, grid, 1, gsize,
+    # mode 2: the paged cascade the library launches on pages of several tokens
+    mode = 2 if page_size > 1 else 1
+    args = (kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, 48, 1, 0, grid, mode, gsize,
             shared, *costs, lg, last.ctypes.data_as(i32p))
     n = sim.sched_pieces_full(*args, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
     assert n >= 0
@@ -496,7 +498,7 @@ def check_cascade_paged(sim, kv_lens, q_lens, H, grid, shared, page_size, costs=
             assert need == 1 and {p[2] for p in ps} == set(range(first.value, first.value + count.value))
 
 
-@pytest.mark.parametrize("page_size", [2, 64, 128])
+@pytest.mark.parametrize("page_size", [1, 2, 64, 128])
 @pytest.mark.parametrize("grid", [1, 7, 152])
 def test_paged_cascade_covers_every_position_once(sim, page_size, grid):
     P = (63911 // page_size) * page_size
