@@ -23,6 +23,10 @@ table, §5.2 page_size = 1; "Scaling Kimi K3 on AMD Instinct MI355X", §1 DCP me
 Paged caches (page_size > 1) are reduced to this token view by expand_pages: a request's
 positions are its pages' slots in order, the last page holding last_page_lens[b] of them.
 
+The step after the decode (same issue, §2 geometry and §3: the 512-wide latent o is mapped
+to v_head_dim = 128 by a separate batched matmul, one 512 x 128 matrix per head):
+    v[t, h, n] = sum_{k<512} o[t, h, k] * w_uv[h, k, n]       (latent_to_v)
+
 Every function has a pin in ``tests/test_oracle_pins.py`` (brute force, closed forms,
 invariants); none is "parity unpinned".
 """
@@ -241,3 +245,27 @@ def merge_rows(o_parts, lse_parts):
     for r in range(R):
         o[r], lse[r] = merge(o_parts[:, r, :], lse_parts[:, r])
     return o, lse
+
+
+def bf16_to_f64(a) -> np.ndarray:
+    """Exact float64 values of bfloat16 bit patterns (uint16 / int16 array): the bf16 word
+    is the high half of a float32."""
+    u = np.asarray(a).view(np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def latent_to_v(o, w_uv) -> np.ndarray:
+    """v[t, h, :] = o[t, h, :] @ w_uv[h] in float64: o (T, H, K) and w_uv (H, K, N) real
+    arrays (K = kv_lora_rank 512, N = v_head_dim 128 for the model; any sizes here).
+
+    ("[Kimi-K3 MLA TP8] MLA performance" §2: kv_lora_rank 512, v_head_dim 128, 12 heads a
+    GPU; §3: the decode's latent o goes through a separate per-head matmul to v_head_dim.)
+    """
+    o = np.asarray(o, dtype=np.float64)
+    w = np.asarray(w_uv, dtype=np.float64)
+    if o.ndim != 3 or w.ndim != 3 or o.shape[1] != w.shape[0] or o.shape[2] != w.shape[1]:
+        raise ValueError("o (T, H, K) and w_uv (H, K, N) must agree in H and K")
+    out = np.empty((o.shape[0], o.shape[1], w.shape[2]), dtype=np.float64)
+    for h in range(o.shape[1]):
+        out[:, h, :] = o[:, h, :] @ w[h]
+    return out

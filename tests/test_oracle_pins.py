@@ -370,3 +370,62 @@ def test_paged_unused_slots_are_never_attended():
         kv2[pg, last[b]:, :] = 0x7E   # 448
     poisoned = oracle.decode_paged(q, kv2, qo, kvp, idx, last, page_size, 0.3, 1.0, 1.0)
     assert np.array_equal(base[0], poisoned[0]) and np.array_equal(base[1], poisoned[1])
+
+
+# ---------------------------------------------------------------- latent o -> v_head_dim
+
+def test_bf16_decode_exact_values():
+    """bf16 words of known values: 1, -2, 0.5, the smallest normal, the largest finite,
+    +inf and a value with every mantissa bit set."""
+    words = np.array([0x3F80, 0xC000, 0x3F00, 0x0080, 0x7F7F, 0x7F80, 0x3FFF], dtype=np.uint16)
+    got = oracle.bf16_to_f64(words)
+    want = [1.0, -2.0, 0.5, 2.0 ** -126, (2 - 2 ** -7) * 2.0 ** 127, np.inf, 1 + (2 ** 7 - 1) / 2 ** 7]
+    assert list(got) == want
+    # agrees with torch's own bf16 -> float conversion on random words
+    rng = np.random.default_rng(3)
+    w = rng.integers(0, 1 << 16, size=4096, dtype=np.uint32).astype(np.uint16)
+    w = w[(w & 0x7F80) != 0x7F80]            # finite values only
+    ref = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.bf16_to_f64(w), ref)
+
+
+def test_latent_to_v_brute_force():
+    """Triple loop over (t, h, n) with a running sum over k, on small random sizes."""
+    rng = np.random.default_rng(21)
+    T, H, K, N = 3, 4, 7, 5
+    o = rng.standard_normal((T, H, K))
+    w = rng.standard_normal((H, K, N))
+    got = oracle.latent_to_v(o, w)
+    for t in range(T):
+        for h in range(H):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    acc += o[t, h, k] * w[h, k, n]
+                assert abs(got[t, h, n] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_latent_to_v_closed_forms():
+    rng = np.random.default_rng(22)
+    T, H, K, N = 2, 3, 512, 128
+    w = rng.standard_normal((H, K, N))
+    # a one-hot latent row picks row k0 of its own head's matrix
+    o = np.zeros((T, H, K))
+    o[1, 2, 300] = 1.0
+    v = oracle.latent_to_v(o, w)
+    assert np.array_equal(v[1, 2], w[2, 300]) and not v[0].any() and not v[1, :2].any()
+    # identity matrices (w[h, k, n] = [k == n]) return the first N latent columns
+    eye = np.zeros((H, K, N))
+    eye[:, np.arange(N), np.arange(N)] = 1.0
+    o = rng.standard_normal((T, H, K))
+    assert np.array_equal(oracle.latent_to_v(o, eye), o[:, :, :N])
+    # heads are independent: permuting the matrices permutes the outputs head by head
+    perm = np.array([2, 0, 1])
+    o_same = np.repeat(o[:, :1, :], H, axis=1)   # every head sees the same latent row
+    v1 = oracle.latent_to_v(o_same, w)
+    v2 = oracle.latent_to_v(o_same, w[perm])
+    assert np.allclose(v2, v1[:, perm], rtol=0, atol=1e-12)
+    # linear in o
+    o2 = rng.standard_normal((T, H, K))
+    assert np.allclose(oracle.latent_to_v(2 * o - o2, w),
+                       2 * oracle.latent_to_v(o, w) - oracle.latent_to_v(o2, w), atol=1e-9)
