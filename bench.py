@@ -275,6 +275,10 @@ def main():
                     help="time eager calls instead of a CUDA-graph replay of the call")
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--ref-heads", type=int, default=12)
+    ap.add_argument("--v-proj", action="store_true",
+                    help="also time mla_latent_to_v (the latent o mapped to v_head_dim 128) on "
+                         "this workload's o, L2 flushed before each call; reported under "
+                         "'v_proj', outside the decode's timed region")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -415,6 +419,27 @@ def main():
         if st != 0:
             raise RuntimeError(f"device error in the plain timing: {pm.mla_status_string(st)}")
 
+    v_proj = None
+    if args.v_proj:
+        _, w_uv = mla_inputs.make_vproj(1, H, seed=args.seed + 17, device=dev)
+        v_out = torch.empty((n_tok, H, 128), dtype=torch.bfloat16, device=dev)
+        for i in range(max(args.warmup, 3)):
+            pm.mla_latent_to_v(o, w_uv, v_out)
+        vev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_((i + 29) & 0xFF)
+            vev[i][0].record(stream)
+            pm.mla_latent_to_v(o, w_uv, v_out)
+            vev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        v_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in vev) / args.steps, dist, dev)
+        v_bytes = (o.numel() + w_uv.numel() + v_out.numel()) * 2
+        v_proj = {"op": "mla_latent_to_v", "us_per_call": v_ms * 1e3, "bytes": v_bytes,
+                  "GB/s": v_bytes / (v_ms * 1e-3) / 1e9, "launches": 1,
+                  "bytes_counted": "o in, every head's 512 x 128 bf16 matrix, v out",
+                  "l2": "flushed before every call"}
+
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
     # the shared prefix's rows count once where the call is told of it, and on paged caches,
     # whose shared pages are the same memory in every request
@@ -533,6 +558,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "plain_call": plain,
+            **({"v_proj": v_proj} if v_proj is not None else {}),
             "clocks": dict(clocks.summary(),
                            window=("the timed region" if soak == 0 else
                                    f"the timed region and {soak} identical untimed steps "

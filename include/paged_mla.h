@@ -207,6 +207,22 @@ int mla_merge_partials(const mla_tensor_t* o_parts, const mla_tensor_t* lse_part
                        mla_stream_t stream);
 
 /*
+ * The step after the decode: each head's 512-wide latent output mapped to v_head_dim = 128
+ * by that head's matrix ("[Kimi-K3 MLA TP8] MLA performance" §2 geometry: kv_lora_rank
+ * 512, v_head_dim 128, 12 heads a GPU; §3: a separate batched matmul after the decode):
+ *   v[t, h, n] = sum_{k<512} o[t, h, k] * w_uv[h, k, n]
+ * in fp32, rounded to bf16 (nearest even).
+ *   o     (n_tok, H, 512) BF16 (mla_decode's o), last dim contiguous, token and head
+ *         strides non-negative multiples of 8 elements, 16-byte aligned.
+ *   w_uv  (H, 512, 128) BF16, contiguous, 16-byte aligned.
+ *   v     (n_tok, H, 128) BF16, last dim contiguous, non-negative strides (written).
+ * n_tok = 0 does nothing.  Shapes, dtypes, strides or alignments outside these return
+ * MLA_ERR_INVALID_ARG before anything is enqueued.  Asynchronous on `stream`.
+ */
+int mla_latent_to_v(const mla_tensor_t* o, const mla_tensor_t* w_uv, const mla_tensor_t* v,
+                    mla_stream_t stream);
+
+/*
  * Debug check of a decode call's index inputs on the device, then a host status:
  * MLA_OK, MLA_ERR_BAD_INPUT (indptr not monotone or not starting at 0 for qo, kv_len <
  * q_len, kv_last_page_lens outside [1, PS] (!= 1 when PS = 1), qo_indptr[B] != sum_T) or

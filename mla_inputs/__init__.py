@@ -95,6 +95,15 @@ def fp8_normal_bytes(n: int, gen: torch.Generator, device, chunk: int = 1 << 26)
     return out
 
 
+def make_vproj(n_tok: int, H: int = 12, seed: int = 0, device="cpu", o_scale: float = 1.0):
+    """Inputs of the latent -> v_head_dim step: o (n_tok, H, 512) bf16 from N(0, o_scale^2)
+    and w_uv (H, 512, 128) bf16 from N(0, 1/512), the scale of a random-init projection."""
+    gen = _gen(seed, device)
+    o = (torch.randn((n_tok, H, DV), generator=gen, device=device) * o_scale).to(torch.bfloat16)
+    w = (torch.randn((H, DV, 128), generator=gen, device=device) * DV ** -0.5).to(torch.bfloat16)
+    return o, w
+
+
 def _finish(name, q, kv, kv_lens, q_lens, indices, index_buffer, pool_rows, device,
             q_scale, kv_scale, poison, gen, meta):
     B = len(kv_lens)

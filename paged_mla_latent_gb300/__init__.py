@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "MlaError", "mla_decode", "mla_decode_shared_prefix", "mla_decode_noalloc", "mla_merge_partials",
     "mla_validate", "mla_check_error", "mla_get_workspace_size", "mla_get_shared_prefix_workspace_size",
-    "mla_status_string", "make_workspace", "library_path", "PreparedDecode",
+    "mla_status_string", "make_workspace", "library_path", "PreparedDecode", "mla_latent_to_v",
 ]
 
 MLA_DTYPE_FP8_E4M3FN = 1
@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_validate.argtypes = [P, P, P, P, P, P, vp, c_sz, vp]
     lib.mla_check_error.restype = ctypes.c_int
     lib.mla_check_error.argtypes = [vp, c_sz, vp]
+    lib.mla_latent_to_v.restype = ctypes.c_int
+    lib.mla_latent_to_v.argtypes = [P, P, P, vp]
     return lib
 
 
@@ -283,6 +285,14 @@ def mla_merge_partials(o_parts, lse_parts, reduce_indptr, reduce_idx, o, lse_out
     ew = ctypes.c_void_p(error_word.data_ptr()) if error_word is not None else None
     rc = _lib.mla_merge_partials(*[_ref(d) for d in descs], ew, _stream(stream, o.device))
     _check(rc, "mla_merge_partials")
+
+
+def mla_latent_to_v(o, w_uv, v, stream=None):
+    """v[t, h, :] = o[t, h, :] @ w_uv[h]: the latent o mapped to v_head_dim (see
+    include/paged_mla.h)."""
+    descs = [_desc(t) for t in (o, w_uv, v)]
+    rc = _lib.mla_latent_to_v(*[_ref(d) for d in descs], _stream(stream, v.device))
+    _check(rc, "mla_latent_to_v")
 
 
 def mla_validate(q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,

@@ -189,3 +189,24 @@ def test_merge_rejects_bad_arguments_on_host(lib):
     assert lib._lib.mla_merge_partials(r(op), r(bad_lp), r(ip), r(ix), r(o), None, None, None) == 1
     odd = _t(base + 4, F32, [8, 96, 512])
     assert lib._lib.mla_merge_partials(r(odd), r(lp), r(ip), r(ix), r(o), None, None, None) == 1
+
+
+def test_latent_to_v_rejects_bad_arguments_on_host(lib):
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    BF, F32 = 2, 3
+    base = 1 << 40
+    o = _t(base, BF, [16, 12, 512])
+    w = _t(base + (8 << 20), BF, [12, 512, 128])
+    v = _t(base + (16 << 20), BF, [16, 12, 128])
+    call = lambda o_, w_, v_: lib._lib.mla_latent_to_v(r(o_), r(w_), r(v_), None)
+    assert call(None, w, v) == 1
+    assert call(_t(base, F32, [16, 12, 512]), w, v) == 1                     # o not bf16
+    assert call(_t(base, BF, [16, 12, 256]), w, v) == 1                      # latent width
+    assert call(o, _t(base + (8 << 20), BF, [12, 512, 64]), v) == 1          # v_head_dim
+    assert call(o, _t(base + (8 << 20), BF, [11, 512, 128]), v) == 1         # head count
+    assert call(o, w, _t(base + (16 << 20), BF, [15, 12, 128])) == 1         # v tokens
+    assert call(_t(base + 2, BF, [16, 12, 512]), w, v) == 1                  # o not 16-B aligned
+    assert call(_t(base, BF, [16, 12, 512], [6148, 516, 1]), w, v) == 1      # stride not 8k
+    assert call(o, _t(base + (8 << 20), BF, [12, 512, 128], [65536, 1, 512]), v) == 1  # w transposed
+    # no tokens: nothing to do, nothing enqueued
+    assert call(_t(base, BF, [0, 12, 512]), w, _t(base + (16 << 20), BF, [0, 12, 128])) == 0
