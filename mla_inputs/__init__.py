@@ -11,10 +11,14 @@ issue 4541):
     kv_len ~68.4K per request, q_len 1.
   * §1 "Environment": the workload is a 63,911-token shared prefix + 4,089 unique input
     tokens + up to 350 generated tokens per request.
-  * §5.2: page_size = 1, kv_indptr holds token counts, kv_last_page_lens is all ones.
+  * §5.2: page_size = 1 as captured (kv_indptr holds token counts, kv_last_page_lens is
+    all ones), and the block-granular layout it proposes: make_paged builds caches of
+    page_size-token pages (128 = the allocator's block), kv_indptr counting pages.
 
 and the long-context / shard figures of "Scaling Kimi K3 on AMD Instinct MI355X",
 §1 "Cache" (142,000-token conversation, DCP8 -> 8 shards, 96 heads per shard call).
+make_vproj draws the inputs of the step after the decode (latent o and one 512 x 128
+matrix per head, §2 of the issue: kv_lora_rank 512, v_head_dim 128).
 
 Values are N(0, 1) draws, clamped to +-448 (the e4m3fn range) and rounded to
 float8_e4m3fn by torch's cast; only the resulting bytes matter.  Lengths and jitter come
