@@ -58,7 +58,23 @@ SOAK_S = 1.0   # shortest span of steps the clock record covers
 
 # Sources of other operations, which the decode call never runs: left out of the hash
 # that keys the decode kernels' recorded counters.
-NOT_DECODE_SOURCES = {"mla_vproj.cu"}
+NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu"}
+
+# What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
+# HBM copy peak, but not every call is HBM-bound.
+LIMITER = {
+    "c16+shared_prefix": "pipeline latency of the 48-row tile (MMA issue, softmax, the QK -> "
+                         "softmax -> PV chain) and the cascade merge; DRAM and tensor pipe "
+                         "each near 20 % busy (profiles/mla_decode_c16.md)",
+    "c24+shared_prefix": "as c16+shared_prefix",
+    "c16": "HBM and L2: every request gathers the shared prefix, which L2 serves after the "
+           "first reads",
+    "c24": "as c16",
+    "long": "fixed per-call latencies (launch, set-up, first tile, epilogue, merge) around "
+            "~7 tiles per CTA (profiles/mla_decode_long.md)",
+    "mtp": "one ring stage's round trip (row copies, QK, softmax, PV) at three stages in "
+           "flight (profiles/mla_decode_mtp.md)",
+}
 
 
 def kernel_source_hash() -> str:
@@ -261,6 +277,73 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def time_graph(call, steps, warmup, flush, no_flush, stream, dev, eager, salt=0):
+    """Mean device time (ms) of `call` per step: W warm-up steps, then the call captured in a
+    CUDA graph and replayed K times, each step bracketed by CUDA events on the launching
+    stream, with an L2 flush (512 MB write) before every step outside the events."""
+    for i in range(warmup):
+        if not no_flush:
+            flush.fill_((i + salt) & 0xFF)
+        call()
+    torch.cuda.synchronize(dev)
+    graph = None
+    if not eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        torch.cuda.synchronize(dev)
+        for i in range(2):
+            if not no_flush:
+                flush.fill_((i + salt) & 0xFF)
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if not no_flush:
+            flush.fill_((i + 7 + salt) & 0xFF)
+        ev[i][0].record(stream)
+        graph.replay() if graph is not None else call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / steps, graph
+
+
+def roofline_for(case, entry, ms, peak, peak_kind, config, shared):
+    """Roofline of one decode call: algorithmic bytes / device time against the HBM copy
+    peak.  A shared-prefix call (and any call on pages, whose shared pages are the same
+    memory) counts the shared rows once; the plain call on a shared-prefix batch is given
+    both readings."""
+    paged = int(case.meta.get("page_size", 1)) > 1
+    distinct = mla_inputs.algorithmic_bytes(case, shared if (entry == "shared_prefix" or paged) else 0)
+    r = {"bound": "hbm", "achieved": distinct / (ms * 1e-3) / 1e9, "peak": peak,
+         "unit": "GB/s", "peak_kind": f"{peak_kind} copy bandwidth",
+         "traffic": recorded_traffic(config, entry),
+         "algorithmic_bytes": distinct}
+    r["frac"] = r["achieved"] / peak
+    if entry == "shared_prefix":
+        r["kernel"] = ("mla_decode_shared_prefix call (one cascade decode launch: prefix units "
+                       "then per-request units, then the cascade merge)")
+        r["bytes_counted"] = ("each distinct cache row once (the shared prefix's rows once for "
+                              "the whole batch), 580 B per row with its index (on pages: 576 B "
+                              "per distinct row and 4 B per page id of every request), plus q, "
+                              "o and lse")
+    else:
+        r["kernel"] = "mla_decode call (decode + merge kernels)"
+        r["bytes_counted"] = ("580 B per attended position (row + index), plus q, o and lse"
+                              if not paged else
+                              "576 B per distinct cache row, 4 B per page id, plus q, o and lse")
+        if shared > 0 and not paged:
+            # every request names the shared rows: gathered once per request, but the
+            # distinct rows are what DRAM must deliver at least once
+            d2 = mla_inputs.algorithmic_bytes(case, shared)
+            r["distinct_bytes"] = d2
+            r["frac_distinct"] = d2 / (ms * 1e-3) / 1e9 / peak
+            r["bytes_counted"] += ("; frac counts the shared prefix once per request (all of "
+                                   "it gathered), frac_distinct once per batch")
+    return r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -288,6 +371,11 @@ def main():
                     help="also time mla_latent_to_v (the latent o mapped to v_head_dim 128) on "
                          "this workload's o, L2 flushed before each call; reported under "
                          "'v_proj', outside the decode's timed region")
+    ap.add_argument("--extra-configs", default="default",
+                    help="comma-separated workloads also timed in this run (same process, same "
+                         "clock record) and reported under 'configs'; 'default': c24 (shared-"
+                         "prefix and plain), long, mtp and long96 when the main workload is "
+                         "c16; 'none': no others")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -300,41 +388,52 @@ def main():
 
     import paged_mla_latent_gb300 as pm
     dev = torch.device("cuda", local)
-    case = mla_inputs.make_case(args.config, seed=args.seed + rank, device=dev,
-                                q_scale=args.q_scale, kv_scale=args.kv_scale)
-    n_tok, H = case.q.shape[0], case.q.shape[1]
-    o = torch.empty((n_tok, H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
-    shared = int(case.meta.get("shared_prefix", 0))
-    entry = args.entry
-    paged = int(case.meta.get("page_size", 1)) > 1
-    if entry == "auto":
-        entry = "shared_prefix" if shared > 0 and args.num_kv_splits <= 0 else "plain"
-    ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev,
-                           shared_prefix=(entry == "shared_prefix"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peaks()
 
-    def call(q=case.q, qo=case.qo_indptr, kvp=case.kv_indptr, idx=case.kv_indices,
-             last=case.kv_last_page_lens, out=o, l=lse, which=None):
-        # on the current stream (capturable)
-        if (which or entry) == "shared_prefix":
-            pm.mla_decode_shared_prefix(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q,
-                                        case.sm_scale, case.q_scale, case.kv_scale, shared,
-                                        lse_out=l, workspace=ws)
-        else:
-            pm.mla_decode(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q, case.sm_scale,
-                          case.q_scale, case.kv_scale, num_kv_splits=args.num_kv_splits,
-                          lse_out=l, workspace=ws)
+    def setup(config, entry_arg):
+        case = mla_inputs.make_case(config, seed=args.seed + rank, device=dev,
+                                    q_scale=args.q_scale, kv_scale=args.kv_scale)
+        n_tok, H = case.q.shape[0], case.q.shape[1]
+        o = torch.empty((n_tok, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
+        shared = int(case.meta.get("shared_prefix", 0))
+        entry = entry_arg
+        if entry == "auto":
+            entry = "shared_prefix" if shared > 0 and args.num_kv_splits <= 0 else "plain"
+        # (a shared-prefix workspace also serves the plain call on the same batch)
+        ws = pm.make_workspace(case.B, H, case.max_seqlen_q, args.num_kv_splits, dev,
+                               shared_prefix=(shared > 0 and args.num_kv_splits <= 0))
+
+        def call(which=None, q=case.q, qo=case.qo_indptr, kvp=case.kv_indptr,
+                 idx=case.kv_indices, last=case.kv_last_page_lens, out=o, l=lse):
+            # on the current stream (capturable)
+            if (which or entry) == "shared_prefix":
+                pm.mla_decode_shared_prefix(q, case.kv, out, qo, kvp, idx, last,
+                                            case.max_seqlen_q, case.sm_scale, case.q_scale,
+                                            case.kv_scale, shared, lse_out=l, workspace=ws)
+            else:
+                pm.mla_decode(q, case.kv, out, qo, kvp, idx, last, case.max_seqlen_q,
+                              case.sm_scale, case.q_scale, case.kv_scale,
+                              num_kv_splits=args.num_kv_splits, lse_out=l, workspace=ws)
+        return case, entry, shared, ws, o, lse, call
+
+    def check(ws, what):
+        st = pm.mla_check_error(ws)
+        if st != 0:
+            raise RuntimeError(f"device error in {what}: {pm.mla_status_string(st)}")
+
+    case, entry, shared, ws, o, lse, call = setup(args.config, args.entry)
+    n_tok, H = case.q.shape[0], case.q.shape[1]
+    paged = int(case.meta.get("page_size", 1)) > 1
 
     for i in range(args.warmup):
         if not args.no_l2_flush:
             flush.fill_(i & 0xFF)
         call()
     torch.cuda.synchronize(dev)
-    st = pm.mla_check_error(ws)
-    if st != 0:
-        raise RuntimeError(f"device error during warm-up: {pm.mla_status_string(st)}")
+    check(ws, "warm-up")
 
     # The timed call is a CUDA-graph replay of one mla_decode call (its two kernel launches),
     # so host-side argument marshalling does not leak into the device time.
@@ -355,11 +454,32 @@ def main():
     t_host = (time.perf_counter() - t_host0) / 20
     torch.cuda.synchronize(dev)
 
+    # The other workloads of the benchmark spec, timed in the same process and clock record;
+    # their inputs are built before the record starts.
+    extra_list = []
+    if args.extra_configs == "default":
+        if args.config == "c16":
+            extra_list = [("c24", "shared_prefix"), ("c24", "plain"), ("long", "plain"),
+                          ("mtp", "plain"), ("long96", "plain")]
+    elif args.extra_configs != "none":
+        extra_list = [(c, "auto") for c in args.extra_configs.split(",") if c]
+    built = {}
+    extra_setups = []
+    for cfg, ent in extra_list:
+        if cfg not in built:
+            built[cfg] = setup(cfg, ent)
+        c2, e2, sh2, ws2, o2, l2, call2 = built[cfg]
+        e2 = ent if ent != "auto" else e2
+        extra_setups.append((cfg, c2, e2, sh2, ws2,
+                             (lambda call2=call2, e2=e2: call2(which=e2))))
+    torch.cuda.synchronize(dev)
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    extras = {}
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
@@ -387,46 +507,44 @@ def main():
                     call()
             soak += 64
             torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
-    st = pm.mla_check_error(ws)
-    if st != 0:
-        raise RuntimeError(f"device error in the timed region: {pm.mla_status_string(st)}")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    mean_ms = sum(step_ms) / len(step_ms)
-    mean_ms = max_over_ranks(mean_ms, dist, dev)
+        if dist is not None:
+            dist.barrier()
+        check(ws, "the timed region")
+        step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+        mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, dev)
 
-    # Workloads with a shared prefix: the plain mla_decode on the same inputs, timed the same
-    # way, reported beside the shared-prefix call.
-    plain = None
-    if entry == "shared_prefix":
-        g2 = None
-        if not args.eager:
-            g2 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g2):
-                call(which="plain")
-        torch.cuda.synchronize(dev)
-        for i in range(max(args.warmup, 3)):
-            if not args.no_l2_flush:
-                flush.fill_(i & 0xFF)
-            g2.replay() if g2 is not None else call(which="plain")
-        torch.cuda.synchronize(dev)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.steps):
-            if not args.no_l2_flush:
-                flush.fill_((i + 11) & 0xFF)
-            ev[i][0].record(stream)
-            g2.replay() if g2 is not None else call(which="plain")
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        p_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, dist, dev)
-        plain = {"entry": "mla_decode", "us_per_call": p_ms * 1e3,
-                 "value": whole_job_rate(world, mla_inputs.gathered_kv_bytes(case.kv_lens), p_ms),
-                 "unit": UNIT}
-        st = pm.mla_check_error(ws)
-        if st != 0:
-            raise RuntimeError(f"device error in the plain timing: {pm.mla_status_string(st)}")
+        # Workloads with a shared prefix: the plain mla_decode on the same inputs, timed the
+        # same way, reported beside the shared-prefix call.
+        plain = None
+        if entry == "shared_prefix":
+            p_ms, _ = time_graph(lambda: call(which="plain"), args.steps, max(args.warmup, 3),
+                                 flush, args.no_l2_flush, stream, dev, args.eager, salt=11)
+            p_ms = max_over_ranks(p_ms, dist, dev)
+            gb = mla_inputs.gathered_kv_bytes(case.kv_lens)
+            plain = {"entry": "mla_decode", "us_per_call": p_ms * 1e3,
+                     "value": whole_job_rate(world, gb, p_ms), "unit": UNIT,
+                     "gathered_rate_over_peak_measured": 100.0 * gb / (p_ms * 1e-3) / 1e9 / peak,
+                     "roofline": roofline_for(case, "plain", p_ms, peak, peak_kind,
+                                              args.config, shared)}
+            check(ws, "the plain timing")
+
+        for cfg, c2, e2, sh2, ws2, call2 in extra_setups:
+            ms2, _ = time_graph(call2, args.steps, max(args.warmup, 3), flush, args.no_l2_flush,
+                                stream, dev, args.eager, salt=23)
+            ms2 = max_over_ranks(ms2, dist, dev)
+            check(ws2, f"the {cfg} timing")
+            gb2 = mla_inputs.gathered_kv_bytes(c2.kv_lens)
+            key = cfg if e2 == "plain" and sh2 == 0 else f"{cfg}+{e2}"
+            extras[key] = {
+                "workload": WORKLOAD_TEXT[cfg],
+                "entry": "mla_decode_shared_prefix" if e2 == "shared_prefix" else "mla_decode",
+                "us_per_call": ms2 * 1e3, "value": whole_job_rate(world, gb2, ms2), "unit": UNIT,
+                "gathered_rate_over_peak_measured": 100.0 * gb2 / (ms2 * 1e-3) / 1e9 / peak,
+                "positions": c2.total_kv, "gathered_kv_bytes": gb2,
+                "roofline": roofline_for(c2, e2, ms2, peak, peak_kind, cfg, sh2),
+            }
+            extras[key]["roofline"]["limiter"] = LIMITER.get(key, LIMITER.get(cfg))
+    del built, extra_setups
 
     v_proj = None
     if args.v_proj:
@@ -450,12 +568,9 @@ def main():
                   "l2": "flushed before every call"}
 
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
-    # the shared prefix's rows count once where the call is told of it, and on paged caches,
-    # whose shared pages are the same memory in every request
-    algo = mla_inputs.algorithmic_bytes(case, shared if (entry == "shared_prefix" or paged) else 0)
     value = whole_job_rate(world, gathered, mean_ms)
-    peak, peak_kind = measured_peaks()
-    achieved = algo / (mean_ms * 1e-3) / 1e9
+    roof = roofline_for(case, entry, mean_ms, peak, peak_kind, args.config, shared)
+    roof["limiter"] = LIMITER.get(f"{args.config}+{entry}", LIMITER.get(args.config))
 
     # ---- end to end through the C ABI with host buffers (pinned), copies in the timed region
     e2e = None
@@ -506,9 +621,7 @@ def main():
             torch.cuda.synchronize(dev)
             if i >= 2:
                 e_ms.append((time.perf_counter() - t0) * 1e3)
-        st = pm.mla_check_error(ws)
-        if st != 0:
-            raise RuntimeError(f"device error in the end-to-end timing: {pm.mla_status_string(st)}")
+        check(ws, "the end-to-end timing")
         # (o was last written by the device-timed calls, or by the plain call timed for
         # comparison: the same attention, so equal within the method's tolerance)
         if not torch.allclose(h_out[:o_bytes].view(o.dtype).view(o.shape).float(),
@@ -530,14 +643,19 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "us_per_call": mean_ms * 1e3,
-            "pct_of_peak_measured": 100.0 * value / world / peak,
-            "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+            # 576 B per attended position over the copy peak: a rate, not a DRAM fraction
+            # (shared rows served once per group, or from L2, push it past 100 %)
+            "gathered_rate_over_peak_measured": 100.0 * value / world / peak,
+            "gathered_rate_over_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+            # the DRAM fraction: algorithmic bytes (distinct rows) over the copy peak
+            "pct_of_hbm_peak_measured": 100.0 * roof["frac"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
                        "seed": args.seed, "requests": case.B, "heads": H,
                        "q_len": case.max_seqlen_q, "positions": case.total_kv,
-                       "gathered_kv_bytes": gathered, "algorithmic_bytes": algo,
+                       "gathered_kv_bytes": gathered,
+                       "algorithmic_bytes": roof["algorithmic_bytes"],
                        "num_kv_splits": args.num_kv_splits,
                        "entry": ("mla_decode_shared_prefix (shared prefix of %d positions, "
                                  "known to the caller)" % shared) if entry == "shared_prefix"
@@ -545,33 +663,19 @@ def main():
                        "l2": "flushed before every step (512 MB write, outside the timed region)"
                              if not args.no_l2_flush else "not flushed",
                        "parallelism": f"{world} independent replicas (one batch per GPU)"},
-            "roofline": {"bound": "hbm",
-                         "kernel": ("mla_decode_shared_prefix call (one cascade decode launch: prefix "
-                                    "units then per-request units, then the cascade merge)"
-                                    if entry == "shared_prefix" else
-                                    "mla_decode call (decode + merge kernels)"),
-                         "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                         "traffic": recorded_traffic(args.config, entry),
-                         "bytes_counted": (("576 B per distinct cache row (the %d shared-prefix "
-                                            "positions' pages once), 4 B per page id of every "
-                                            "request (%d-token pages), plus q, o and lse"
-                                            % (shared, int(case.meta["page_size"]))) if paged else
-                                           "each distinct cache row once (the shared prefix's rows "
-                                           "once for the whole batch), 580 B per row with its "
-                                           "index, plus q, o and lse"
-                                           if entry == "shared_prefix" else
-                                           "580 B per attended position (row + index), plus q, "
-                                           "o and lse")},
+            "roofline": roof,
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "plain_call": plain,
+            "configs": extras,
             **({"v_proj": v_proj} if v_proj is not None else {}),
             "clocks": dict(clocks.summary(),
                            window=("the timed region" if soak == 0 else
                                    f"the timed region and {soak} identical untimed steps "
-                                   f"right after it ({args.clock_soak_s:g} s in all)")),
+                                   f"right after it ({args.clock_soak_s:g} s in all)")
+                           + (", then the plain call and the other workloads"
+                              if (plain or extras) else "")),
             "wall_s_timed_region": t_wall,
             "timing": "CUDA graph replay of one call per step" if graph is not None else "eager calls",
             "host_us_per_eager_call": t_host * 1e6,

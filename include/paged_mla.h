@@ -243,6 +243,21 @@ int mla_validate(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
  */
 int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/*
+ * Self-test of the bounded wait every decode pipeline role uses (no counterpart on the
+ * pages: it exists so that the failure path of a wait can be exercised on the GPU without
+ * a fault or a hang).  One thread initialises an mbarrier in shared memory that nothing
+ * ever arrives at and waits on it with the library's wait, limited to limit_ns
+ * (1 us .. 100 ms; the decode's own waits use 2 s).  The wait gives up when the limit
+ * passes: it ORs the timeout bit into *error_word (the bit mla_check_error reports as
+ * MLA_ERR_TIMEOUT), and the kernel writes result[0] = 1 if the wait returned success
+ * (never expected), result[1] = the abort flag the wait raised (1), result[2] = the
+ * microseconds spent waiting.  error_word (1 int32) and result (3 int32) are device
+ * pointers.  Asynchronous on `stream`.
+ */
+int mla_selftest_bounded_wait(int32_t* error_word, int32_t* result, int64_t limit_ns,
+                              mla_stream_t stream);
+
 /* Size of the fixed device scratch array behind mla_decode_noalloc (16 MiB). */
 #define MLA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -264,7 +279,10 @@ int mla_check_error(void* workspace, size_t workspace_bytes, mla_stream_t stream
  * split fits up to ~350 requests with 12-16 heads and q_len 1, and ~18 requests with 12
  * heads and q_len 4; num_kv_splits = 1 fits any batch).  Nothing is allocated: the first call on each device looks up the array's
  * device address (so make that first call before any stream capture), and every call
- * clears the error words and then runs the ordinary decode on `stream`.
+ * runs all of mla_decode's host-side argument checks (returning their status with nothing
+ * enqueued), then clears the array's error words and runs the ordinary decode on
+ * `stream`.  Because each call clears the error words, the bits of a call are only kept
+ * through its error_out: pass error_out to learn of index errors or timeouts.
  * All calls on a device share the array and it keeps the last call's contents: calls
  * that may overlap on the GPU (different streams without ordering) race on it.
  */

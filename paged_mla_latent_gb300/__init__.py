@@ -27,6 +27,7 @@ __all__ = [
     "MlaError", "mla_decode", "mla_decode_shared_prefix", "mla_decode_noalloc", "mla_merge_partials",
     "mla_validate", "mla_check_error", "mla_get_workspace_size", "mla_get_shared_prefix_workspace_size",
     "mla_status_string", "make_workspace", "library_path", "PreparedDecode", "mla_latent_to_v",
+    "mla_selftest_bounded_wait",
 ]
 
 MLA_DTYPE_FP8_E4M3FN = 1
@@ -78,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_check_error.argtypes = [vp, c_sz, vp]
     lib.mla_latent_to_v.restype = ctypes.c_int
     lib.mla_latent_to_v.argtypes = [P, P, P, vp]
+    lib.mla_selftest_bounded_wait.restype = ctypes.c_int
+    lib.mla_selftest_bounded_wait.argtypes = [vp, vp, ctypes.c_int64, vp]
     return lib
 
 
@@ -270,6 +273,12 @@ def mla_decode_noalloc(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_las
     descs = [_desc(t) for t in (q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
                                 kv_last_page_lens, q_scale, kv_scale, lse_out)]
     dq, dkv, do, dqo, dkvp, didx, dlast, dqs, dks, dlse = descs
+    if error_out is not None:
+        # the library copies 4 bytes device-to-device into it after the decode is queued
+        if not isinstance(error_out, torch.Tensor) or error_out.dtype != torch.int32 or \
+                error_out.numel() < 1 or error_out.device != q.device:
+            raise ValueError("error_out must be an int32 tensor of at least one element on "
+                             f"{q.device}")
     ew = ctypes.c_void_p(error_out.data_ptr()) if error_out is not None else None
     rc = _lib.mla_decode_noalloc(_ref(dq), _ref(dkv), _ref(do), _ref(dqo), _ref(dkvp), _ref(didx),
                                  _ref(dlast), int(max_seqlen_q), float(sm_scale), _ref(dqs),
@@ -293,6 +302,19 @@ def mla_latent_to_v(o, w_uv, v, stream=None):
     descs = [_desc(t) for t in (o, w_uv, v)]
     rc = _lib.mla_latent_to_v(*[_ref(d) for d in descs], _stream(stream, v.device))
     _check(rc, "mla_latent_to_v")
+
+
+def mla_selftest_bounded_wait(error_word, result, limit_ns, stream=None):
+    """Run the library's bounded mbarrier wait on a barrier nothing arrives at (see
+    include/paged_mla.h): error_word (1) and result (3) are int32 device tensors."""
+    for t, n in ((error_word, 1), (result, 3)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or t.numel() < n or \
+                not t.is_cuda:
+            raise ValueError(f"expected an int32 CUDA tensor of at least {n} element(s)")
+    rc = _lib.mla_selftest_bounded_wait(ctypes.c_void_p(error_word.data_ptr()),
+                                        ctypes.c_void_p(result.data_ptr()), int(limit_ns),
+                                        _stream(stream, result.device))
+    _check(rc, "mla_selftest_bounded_wait")
 
 
 def mla_validate(q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/paged_mla.h"
+#include "mla_api_internal.h"
 #include "mla_decode_launch.h"
 #include "mla_merge_kernel.cuh"
 #include "mla_sched.cuh"
@@ -338,7 +339,7 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
                 int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
                 const mla_tensor_t* kv_scale, int32_t num_kv_splits, int32_t shared_len,
                 const mla_tensor_t* lse_out, void* workspace, size_t workspace_bytes,
-                mla_stream_t stream_) {
+                mla_stream_t stream_, bool check_only = false) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   CallShape cs;
   int rc = check_inputs(q, kv_buffer, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens, &cs);
@@ -358,6 +359,7 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   Plan plan;
   if ((rc = make_plan(cs.B, cs.H, max_seqlen_q, num_kv_splits, sms, &plan))) return rc;
   if (workspace_bytes < plan.bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (check_only) return MLA_OK;   // every host-side check passed; nothing enqueued
 
   CUtensorMap q_lat, q_rope;
   const int64_t q_rows = cs.n_tok * cs.H;
@@ -442,6 +444,21 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
 }
 
 }  // namespace
+
+namespace pmla {
+
+int check_decode_call(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
+                      const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
+                      const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,
+                      int32_t max_seqlen_q, float sm_scale, const mla_tensor_t* q_scale,
+                      const mla_tensor_t* kv_scale, int32_t num_kv_splits,
+                      const mla_tensor_t* lse_out, void* workspace, size_t workspace_bytes) {
+  return decode_impl(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
+                     max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits, 0, lse_out,
+                     workspace, workspace_bytes, nullptr, /*check_only=*/true);
+}
+
+}  // namespace pmla
 
 extern "C" {
 

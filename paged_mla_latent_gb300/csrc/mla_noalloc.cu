@@ -7,13 +7,15 @@
 // array instead of a caller-provided workspace.  The array is part of this library's
 // module, so every GPU that loads the library holds it (MLA_NOALLOC_SCRATCH_BYTES) until
 // the process exits.  Nothing here allocates: the call looks up the array's device
-// address (once per device), clears the error words, runs the ordinary decode path on the
-// array, and optionally copies the error word to the caller.
+// address (once per device), runs every host-side check of the decode, and only then
+// clears the error words, runs the ordinary decode path on the array, and optionally
+// copies the error word to the caller.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/paged_mla.h"
+#include "mla_api_internal.h"
 
 namespace {
 
@@ -66,6 +68,12 @@ extern "C" int mla_decode_noalloc(const mla_tensor_t* q, const mla_tensor_t* kv_
   if (need > static_cast<size_t>(MLA_NOALLOC_SCRATCH_BYTES)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   if ((rc = scratch_address(&scratch)) != MLA_OK) return rc;
+  // Argument errors come back before anything is enqueued (the memset below included).
+  rc = pmla::check_decode_call(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices,
+                               kv_last_page_lens, max_seqlen_q, sm_scale, q_scale, kv_scale,
+                               num_kv_splits, lse_out, scratch,
+                               static_cast<size_t>(MLA_NOALLOC_SCRATCH_BYTES));
+  if (rc != MLA_OK) return rc;
   // The error words must start at zero; the partials are always written before read.
   if (cudaMemsetAsync(scratch, 0, kErrorBytes, stream) != cudaSuccess) return MLA_ERR_CUDA;
   rc = mla_decode(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,

@@ -82,15 +82,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Slow path of mbar_wait: poll until the phase completes, the CTA's abort flag goes up, or
-// kWaitLimitNs passes (then raise the flag and the device error bit).  Kept out of line
+// limit_ns passes (then raise the flag and the device error bit).  Kept out of line
 // so that the many call sites stay small.
 static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            int* err_word) {
+                                            int* err_word,
+                                            unsigned long long limit_ns = kWaitLimitNs) {
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err_word, kErrTimeout);
       return false;
@@ -99,11 +100,13 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t par
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (without
-// waiting) once the CTA's abort flag is up, and raises it itself after kWaitLimitNs.
+// waiting) once the CTA's abort flag is up, and raises it itself after limit_ns
+// (kWaitLimitNs in every kernel of the library; shorter only in the wait's self-test).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err_word) {
+                                          int* err_word,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err_word);
+  return mbar_wait_slow(bar, parity, abort_flag, err_word, limit_ns);
 }
 
 // Same, ignoring the abort flag: used only while draining in-flight copies / MMAs

@@ -101,3 +101,38 @@ def oracle_sampled(case, samples):
         o, lse = oracle.attend_one(q_host[r][h], rows, np.arange(n_att, dtype=np.int32), sm, qs, ks)
         out.append((r, h, o, lse))
     return out
+
+
+def oracle_requests(case, reqs):
+    """Oracle for every query token and head of the requests `reqs` of a large case (one-
+    token pages): {b: (o_ref (T_b, H, 512), lse_ref (T_b, H))}.  Each request's rows are
+    gathered once on the device, copied to the host and decoded by the oracle as a batch
+    of one (all its heads and drafts at once, OpenMP across them)."""
+    sm, qs, ks = case.scales()
+    out = {}
+    for b in reqs:
+        rows = gather_rows(case, b)
+        L = rows.shape[0]
+        t0, t1 = int(case.qo_indptr[b]), int(case.qo_indptr[b + 1])
+        q = case.q[t0:t1].cpu().numpy()
+        o_ref, lse_ref = oracle.decode(q, rows, np.array([0, t1 - t0], np.int32),
+                                       np.array([0, L], np.int32), np.arange(L, dtype=np.int32),
+                                       sm, qs, ks)
+        out[b] = (o_ref, lse_ref)
+    return out
+
+
+def compare_requests(case, o, lse, refs, what=""):
+    """Assert the tolerance on every (token, head) of the requests in `refs`."""
+    og = o.float().cpu().numpy().astype(np.float64)
+    lg = lse.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for b, (o_ref, lse_ref) in refs.items():
+        t0, t1 = int(case.qo_indptr[b]), int(case.qo_indptr[b + 1])
+        d = np.abs(og[t0:t1] - o_ref)
+        bound = O_ATOL + O_RTOL * np.abs(o_ref)
+        assert (d <= bound).all(), (what, b, float(d.max()))
+        dl = np.abs(lg[t0:t1] - lse_ref)
+        assert (dl <= LSE_ATOL).all(), (what, b, float(dl.max()))
+        worst = max(worst, float((d / bound).max()))
+    return worst
