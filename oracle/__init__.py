@@ -27,6 +27,12 @@ The step after the decode (same issue, §2 geometry and §3: the 512-wide latent
 to v_head_dim = 128 by a separate batched matmul, one 512 x 128 matrix per head):
     v[t, h, n] = sum_{k<512} o[t, h, k] * w_uv[h, k, n]       (latent_to_v)
 
+The step before it (same issue, §3: q's rope part rotated and concatenated after its 512
+latent columns, the step's new 576-wide entry written into the cache; rope_concat_cache in
+rope_cache.c, fp32 rotation, e4m3 codes of fp32(value / scale), ties to even, saturating):
+    q_out[t, h] = e4m3([q_nope[t, h] / q_scale, rot(q_pe[t, h], pos_t) / q_scale])
+    cache[slot_t] = e4m3([kv_c[t] / kv_scale, rot(k_pe[t], pos_t) / kv_scale])
+
 Every function has a pin in ``tests/test_oracle_pins.py`` (brute force, closed forms,
 invariants); none is "parity unpinned".
 """
@@ -41,6 +47,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mla_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "rope_cache.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libmlaoracle.so")
 _lock = threading.Lock()
@@ -58,11 +65,12 @@ def build(force: bool = False) -> str:
     """Compile mla_oracle.c into oracle/_build/libmlaoracle.so (portable C, no ISA flags)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(p) for p in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-adds, every float operation rounds on its own
     cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
-           "-o", tmp, _SRC, "-lm"]
+           "-ffp-contract=off", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -89,6 +97,15 @@ def _load():
         lib.mlao_merge.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_int64, _f64p, _f64p]
         lib.mlao_max_threads.restype = ctypes.c_int
         lib.mlao_max_threads.argtypes = []
+        lib.mlao_e4m3_encode.restype = ctypes.c_uint
+        lib.mlao_e4m3_encode.argtypes = [ctypes.c_double]
+        _u16p = ctypes.POINTER(ctypes.c_uint16)
+        _f32p = ctypes.POINTER(ctypes.c_float)
+        lib.mlao_rope_concat_cache.restype = ctypes.c_int
+        lib.mlao_rope_concat_cache.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, _f32p,
+                                               ctypes.c_int64, ctypes.c_int, _i32p,
+                                               ctypes.c_float, ctypes.c_float, ctypes.c_int64,
+                                               ctypes.c_int, _u8p, _u8p, ctypes.c_int64]
         _lib = lib
         return lib
 
@@ -269,3 +286,51 @@ def latent_to_v(o, w_uv) -> np.ndarray:
     for h in range(o.shape[1]):
         out[:, h, :] = o[:, h, :] @ w[h]
     return out
+
+
+def e4m3_encode(x) -> int:
+    """e4m3fn code of the finite value nearest to x (ties to the even code, saturating at
+    +-448, NaN -> 0x7F): the format's round-to-nearest-even, by search over its table."""
+    return int(_load().mlao_e4m3_encode(float(x)))
+
+
+def rope_concat_cache(q_nope, q_pe, kv_c, k_pe, positions, cos_sin, neox, slot_mapping,
+                      q_scale, kv_scale, cache):
+    """The fused step before the decode (rope_cache.c).
+
+    q_nope (T, H, 512), q_pe (T, H, 64), kv_c (T, 512), k_pe (T, 64): bf16 bit patterns
+    (uint16 arrays); positions, slot_mapping (T,) int32; cos_sin (max_pos, 64) float32;
+    cache: uint8 array whose slots are its rows of 576 bytes in slot order (a paged cache
+    (N_pages, PS, [1,] 576) reshaped to (N_pages * PS, 576)).  Returns (q_out (T, H, 576)
+    uint8, new cache (same shape as `cache`), error bits: 1 position outside the table,
+    2 slot outside the cache).  q_out bytes that are not written are 0x7F (fp8 NaN).
+    """
+    lib = _load()
+    _u16p = ctypes.POINTER(ctypes.c_uint16)
+    _f32p = ctypes.POINTER(ctypes.c_float)
+
+    def u16(a):
+        a = np.asarray(a)
+        if a.dtype not in (np.uint16, np.int16):
+            raise TypeError("bf16 operands are passed as their uint16 bit patterns")
+        return np.ascontiguousarray(a.view(np.uint16))
+
+    qn, qp, kc, kp = u16(q_nope), u16(q_pe), u16(kv_c), u16(k_pe)
+    T, H = qn.shape[0], qn.shape[1]
+    if qn.shape != (T, H, 512) or qp.shape != (T, H, 64) or kc.shape != (T, 512) or \
+            kp.shape != (T, 64):
+        raise ValueError("shapes: q_nope (T,H,512), q_pe (T,H,64), kv_c (T,512), k_pe (T,64)")
+    pos = _i32(positions).reshape(-1)
+    slots = _i32(slot_mapping).reshape(-1)
+    cs = np.ascontiguousarray(np.asarray(cos_sin, dtype=np.float32))
+    if pos.size != T or slots.size != T or cs.ndim != 2 or cs.shape[1] != 64:
+        raise ValueError("positions/slot_mapping (T,), cos_sin (max_pos, 64)")
+    out_cache = _u8(cache).copy()
+    flat = out_cache.reshape(-1, D)
+    q_out = np.full((T, H, D), 0x7F, dtype=np.uint8)
+    err = lib.mlao_rope_concat_cache(
+        _ptr(qn, _u16p), _ptr(qp, _u16p), _ptr(kc, _u16p), _ptr(kp, _u16p), _ptr(pos, _i32p),
+        _ptr(cs, _f32p), cs.shape[0], int(bool(neox)), _ptr(slots, _i32p),
+        float(np.float32(q_scale)), float(np.float32(kv_scale)), T, H, _ptr(q_out, _u8p),
+        _ptr(flat, _u8p), flat.shape[0])
+    return q_out, out_cache, int(err)
