@@ -344,6 +344,64 @@ def roofline_for(case, entry, ms, peak, peak_kind, config, shared):
     return r
 
 
+def time_adjacent(pm, dev, stream, flush, steps, warmup, seed):
+    """The steps around the decode, each on its own (L2 flushed before every call): the
+    q-rope + concat + fp8 cache write at the c16 and mtp token counts, and the latent ->
+    v_head_dim matmul on the decode's o at the same shapes."""
+    out = {}
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_((i + 41) & 0xFF)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    peak, _ = measured_peaks()
+    for name, T in (("c16", 16), ("mtp", 256)):
+        H = 12
+        inp = mla_inputs.make_rope_inputs(T, H, seed=seed + T, device=dev)
+        kv = torch.zeros((5_283_840, 576), dtype=torch.uint8, device=dev) if name == "c16" else \
+            torch.zeros((1 << 22, 576), dtype=torch.uint8, device=dev)
+        g = torch.Generator(device=dev).manual_seed(seed + T)
+        slots = torch.randperm(kv.shape[0], generator=g, device=dev)[:T].to(torch.int32)
+        q_out = torch.empty((T, H, 576), dtype=torch.uint8, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        qs = torch.tensor(mla_inputs.DEFAULT_Q_SCALE, device=dev)
+        ks = torch.tensor(mla_inputs.DEFAULT_KV_SCALE, device=dev)
+        ms = timed(lambda: pm.mla_qk_rope_concat_and_cache(
+            inp["q_nope"], inp["q_pe"], inp["kv_c"], inp["k_pe"], inp["positions"],
+            inp["cos_sin"], 0, slots, qs, ks, q_out, kv, err))
+        if int(err.item()) != 0:
+            raise RuntimeError("device error in the rope/cache-write timing")
+        nbytes = T * (2 * H * 576 + 2 * 576 + 8 + 256 + H * 576 + 576)
+        out[f"rope_cache_{name}"] = {
+            "op": "mla_qk_rope_concat_and_cache", "tokens": T, "heads": H,
+            "us_per_call": ms * 1e3, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+            "bytes_counted": "bf16 q (latent + rope), new latent + rope key, position, slot, "
+                             "table row in; fp8 q and one 576-B cache entry out, per token",
+            "launches": 1}
+        del kv
+        o, w_uv = mla_inputs.make_vproj(T, H, seed=seed + 17, device=dev, o_scale=0.05)
+        v = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: pm.mla_latent_to_v(o, w_uv, v))
+        nbytes = (o.numel() + w_uv.numel() + v.numel()) * 2
+        out[f"latent_to_v_{name}"] = {
+            "op": "mla_latent_to_v", "tokens": T, "heads": H, "us_per_call": ms * 1e3,
+            "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+            "bytes_counted": "o in, every head's 512 x 128 bf16 matrix, v out", "launches": 1}
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -371,6 +429,9 @@ def main():
                     help="also time mla_latent_to_v (the latent o mapped to v_head_dim 128) on "
                          "this workload's o, L2 flushed before each call; reported under "
                          "'v_proj', outside the decode's timed region")
+    ap.add_argument("--no-adjacent", action="store_true",
+                    help="skip timing the steps around the decode (rope/cache write, latent "
+                         "-> v_head_dim), reported under 'adjacent_steps'")
     ap.add_argument("--extra-configs", default="default",
                     help="comma-separated workloads also timed in this run (same process, same "
                          "clock record) and reported under 'configs'; 'default': c24 (shared-"
@@ -567,6 +628,11 @@ def main():
                   "bytes_counted": "o in, every head's 512 x 128 bf16 matrix, v out",
                   "l2": "flushed before every call"}
 
+    adjacent = None
+    if not args.no_adjacent:
+        adjacent = time_adjacent(pm, dev, stream, flush, args.steps, max(args.warmup, 3),
+                                 args.seed)
+
     gathered = mla_inputs.gathered_kv_bytes(case.kv_lens)
     value = whole_job_rate(world, gathered, mean_ms)
     roof = roofline_for(case, entry, mean_ms, peak, peak_kind, args.config, shared)
@@ -669,6 +735,7 @@ def main():
             "gpu_launches": 2 * args.steps,
             "plain_call": plain,
             "configs": extras,
+            "adjacent_steps": adjacent,
             **({"v_proj": v_proj} if v_proj is not None else {}),
             "clocks": dict(clocks.summary(),
                            window=("the timed region" if soak == 0 else

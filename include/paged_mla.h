@@ -223,6 +223,53 @@ int mla_latent_to_v(const mla_tensor_t* o, const mla_tensor_t* w_uv, const mla_t
                     mla_stream_t stream);
 
 /*
+ * The step that produces the decode's inputs ("[Kimi-K3 MLA TP8] MLA performance" §3
+ * "Entry point": q comes out of a fused step that rotates q's rope part, places it after
+ * the 512 latent columns and writes the step's new cache entry into the cache the decode
+ * reads; §2: an entry is 512 latent + 64 rope columns; §4.1: fp8 e4m3fn q and cache with
+ * float32 per-tensor scales).  For token t < T and head h < H, with p = positions[t] and
+ * the table row cos_sin[p] = (cos th_0 .. cos th_31, sin th_0 .. sin th_31):
+ *   rot(v)  rotates the pairs of the 64 rope values v by th_i: pair i is (v[2i], v[2i+1])
+ *           (is_neox = 0) or (v[i], v[i+32]) (is_neox = 1), and (x, y) becomes
+ *           (x cos th_i - y sin th_i, y cos th_i + x sin th_i), every product and sum
+ *           rounded to fp32 (no fused multiply-add);
+ *   e(v, s) the e4m3fn code nearest to fp32(v / s) (ties to even, saturating at +-448);
+ *   q_out[t, h, 0:512]   = e(q_nope[t, h, :], q_scale)
+ *   q_out[t, h, 512:576] = e(rot(q_pe[t, h, :]), q_scale)
+ *   cache slot slot_mapping[t] (= page * PS + slot) = [e(kv_c[t], kv_scale),
+ *                                                     e(rot(k_pe[t]), kv_scale)]
+ * so that the decode's dequantisation (code * scale) returns the rotated values.
+ *   q_nope        (T, H, 512) BF16: the latent part of q (already absorbed)
+ *   q_pe          (T, H, 64)  BF16: the rope part of q, before rotation
+ *   kv_c          (T, 512)    BF16: the step's new latent entries
+ *   k_pe          (T, 64)     BF16: their rope keys, before rotation
+ *                 (each: last dim contiguous, 16-byte aligned, other strides non-negative
+ *                 multiples of 8 elements: views into wider projections are fine)
+ *   positions     (T,) INT32: position of each token (its row of cos_sin)
+ *   cos_sin       (max_pos, 64) FP32, last dim contiguous, row stride a multiple of 4
+ *   is_neox       0 or 1 (pair convention above)
+ *   slot_mapping  (T,) INT32: cache slot of token t's entry; < 0: no entry (padding)
+ *   q_scale, kv_scale  0-dim (or 1-element) FP32 device tensors
+ *   q_out         (T, H, 576) FP8_E4M3FN, contiguous, 16-byte aligned (written): the
+ *                 decode's q
+ *   kv_buffer     the decode's cache, (N, 576) or (N_pages, PS, 1, 576) FP8_E4M3FN as
+ *                 mla_decode takes it (written at the mapped slots only)
+ *   error_word    device int32 (required): a slot >= N_pages * PS is skipped and sets bit
+ *                 64; a position outside [0, max_pos) sets bit 1 and leaves that token's
+ *                 rope columns (of q_out and of its entry) unwritten
+ * Two tokens mapped to one slot race (which entry lands is unspecified); the outputs may
+ * not overlap the inputs.  Shapes, dtypes, strides or alignments outside these return
+ * MLA_ERR_INVALID_ARG before anything is enqueued.  Asynchronous on `stream`.
+ */
+int mla_qk_rope_concat_and_cache(const mla_tensor_t* q_nope, const mla_tensor_t* q_pe,
+                                 const mla_tensor_t* kv_c, const mla_tensor_t* k_pe,
+                                 const mla_tensor_t* positions, const mla_tensor_t* cos_sin,
+                                 int32_t is_neox, const mla_tensor_t* slot_mapping,
+                                 const mla_tensor_t* q_scale, const mla_tensor_t* kv_scale,
+                                 const mla_tensor_t* q_out, const mla_tensor_t* kv_buffer,
+                                 int32_t* error_word, mla_stream_t stream);
+
+/*
  * Debug check of a decode call's index inputs on the device, then a host status:
  * MLA_OK, MLA_ERR_BAD_INPUT (indptr not monotone or not starting at 0 for qo, kv_len <
  * q_len, kv_last_page_lens outside [1, PS] (!= 1 when PS = 1), qo_indptr[B] != sum_T) or

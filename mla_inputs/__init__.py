@@ -108,6 +108,30 @@ def make_vproj(n_tok: int, H: int = 12, seed: int = 0, device="cpu", o_scale: fl
     return o, w
 
 
+def make_rope_inputs(n_tok: int, H: int = 12, max_pos: int = 73728, seed: int = 0,
+                     device="cpu", value_scale: float = 1.0, rope_base: float = 10000.0):
+    """Inputs of the step before the decode (q rope + concat + cache write): bf16 q_nope
+    (n_tok, H, 512), q_pe (n_tok, H, 64), kv_c (n_tok, 512), k_pe (n_tok, 64) from
+    N(0, value_scale^2); positions uniform in [0, max_pos); a float32 rotary table
+    (max_pos, 64) of cos then sin of p * rope_base^(-i/32), i < 32 (the caller's table: the
+    pages give neither base nor scaling, any table is valid input).  max_pos 73,728 is the
+    captured deployment's max model length (issue §1)."""
+    gen = _gen(seed, device)
+
+    def normal(*shape):
+        return (torch.randn(shape, generator=gen, device=device) * value_scale).to(torch.bfloat16)
+
+    q_nope, q_pe = normal(n_tok, H, DV), normal(n_tok, H, 64)
+    kv_c, k_pe = normal(n_tok, DV), normal(n_tok, 64)
+    positions = torch.randint(0, max_pos, (n_tok,), generator=gen, device=device,
+                              dtype=torch.int64).to(torch.int32)
+    inv = rope_base ** (-np.arange(32, dtype=np.float64) / 32.0)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    table = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+    return dict(q_nope=q_nope, q_pe=q_pe, kv_c=kv_c, k_pe=k_pe, positions=positions,
+                cos_sin=table.to(device))
+
+
 def _finish(name, q, kv, kv_lens, q_lens, indices, index_buffer, pool_rows, device,
             q_scale, kv_scale, poison, gen, meta):
     B = len(kv_lens)

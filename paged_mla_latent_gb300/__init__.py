@@ -27,7 +27,7 @@ __all__ = [
     "MlaError", "mla_decode", "mla_decode_shared_prefix", "mla_decode_noalloc", "mla_merge_partials",
     "mla_validate", "mla_check_error", "mla_get_workspace_size", "mla_get_shared_prefix_workspace_size",
     "mla_status_string", "make_workspace", "library_path", "PreparedDecode", "mla_latent_to_v",
-    "mla_selftest_bounded_wait",
+    "mla_selftest_bounded_wait", "mla_qk_rope_concat_and_cache",
 ]
 
 MLA_DTYPE_FP8_E4M3FN = 1
@@ -79,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_check_error.argtypes = [vp, c_sz, vp]
     lib.mla_latent_to_v.restype = ctypes.c_int
     lib.mla_latent_to_v.argtypes = [P, P, P, vp]
+    lib.mla_qk_rope_concat_and_cache.restype = ctypes.c_int
+    lib.mla_qk_rope_concat_and_cache.argtypes = [P, P, P, P, P, P, c_i32, P, P, P, P, P, vp, vp]
     lib.mla_selftest_bounded_wait.restype = ctypes.c_int
     lib.mla_selftest_bounded_wait.argtypes = [vp, vp, ctypes.c_int64, vp]
     return lib
@@ -302,6 +304,24 @@ def mla_latent_to_v(o, w_uv, v, stream=None):
     descs = [_desc(t) for t in (o, w_uv, v)]
     rc = _lib.mla_latent_to_v(*[_ref(d) for d in descs], _stream(stream, v.device))
     _check(rc, "mla_latent_to_v")
+
+
+def mla_qk_rope_concat_and_cache(q_nope, q_pe, kv_c, k_pe, positions, cos_sin, is_neox,
+                                 slot_mapping, q_scale, kv_scale, q_out, kv_buffer,
+                                 error_word, stream=None):
+    """Rotate q's and the new keys' rope columns, quantise q to the decode's fp8 q_out and
+    write each token's new 576-wide entry into kv_buffer at its slot (see
+    include/paged_mla.h).  error_word: an int32 device tensor (>= 1 element)."""
+    if not isinstance(error_word, torch.Tensor) or error_word.dtype != torch.int32 or \
+            error_word.numel() < 1 or error_word.device != q_out.device:
+        raise ValueError(f"error_word must be an int32 tensor on {q_out.device}")
+    descs = [_desc(t) for t in (q_nope, q_pe, kv_c, k_pe, positions, cos_sin)]
+    tail = [_desc(t) for t in (slot_mapping, q_scale, kv_scale, q_out, kv_buffer)]
+    rc = _lib.mla_qk_rope_concat_and_cache(*[_ref(d) for d in descs], int(is_neox),
+                                           *[_ref(d) for d in tail],
+                                           ctypes.c_void_p(error_word.data_ptr()),
+                                           _stream(stream, q_out.device))
+    _check(rc, "mla_qk_rope_concat_and_cache")
 
 
 def mla_selftest_bounded_wait(error_word, result, limit_ns, stream=None):

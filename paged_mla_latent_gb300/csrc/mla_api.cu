@@ -447,6 +447,8 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
 
 namespace pmla {
 
+void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
+
 int check_decode_call(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_tensor_t* o,
                       const mla_tensor_t* qo_indptr, const mla_tensor_t* kv_indptr,
                       const mla_tensor_t* kv_indices, const mla_tensor_t* kv_last_page_lens,

@@ -9,6 +9,10 @@
 
 namespace pmla {
 
+// cuTensorMapEncodeTiled, found once through the runtime's driver entry point (no libcuda
+// link), or null if the driver does not provide it.
+void* tensor_map_encoder();
+
 // Every host-side check mla_decode makes on these arguments (shapes, dtypes, strides,
 // scalars, workspace size and alignment), without enqueuing anything.  Returns MLA_OK or
 // the status mla_decode would return before its first launch.

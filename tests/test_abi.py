@@ -210,3 +210,47 @@ def test_latent_to_v_rejects_bad_arguments_on_host(lib):
     assert call(o, _t(base + (8 << 20), BF, [12, 512, 128], [65536, 1, 512]), v) == 1  # w transposed
     # no tokens: nothing to do, nothing enqueued
     assert call(_t(base, BF, [0, 12, 512]), w, _t(base + (16 << 20), BF, [0, 12, 128])) == 0
+
+
+def test_rope_cache_rejects_bad_arguments_on_host(lib):
+    """mla_qk_rope_concat_and_cache: every shape, dtype, stride and alignment check returns
+    MLA_ERR_INVALID_ARG (or UNSUPPORTED) before anything touches the device; no tokens is
+    a no-op."""
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    F8, BF, F32, I32 = 1, 2, 3, 4
+    b = 1 << 40
+    T, H = 4, 12
+    good = dict(qn=_t(b, BF, [T, H, 512]), qp=_t(b + (1 << 20), BF, [T, H, 64]),
+                kc=_t(b + (2 << 20), BF, [T, 512]), kp=_t(b + (3 << 20), BF, [T, 64]),
+                pos=_t(b + (4 << 20), I32, [T]), cs=_t(b + (5 << 20), F32, [128, 64]), neox=0,
+                slots=_t(b + (6 << 20), I32, [T]), qs=_t(b + (7 << 20), F32, []),
+                ks=_t(b + (8 << 20), F32, []), qo=_t(b + (9 << 20), F8, [T, H, 576]),
+                kv=_t(b + (16 << 20), F8, [1024, 576]), err=b + (10 << 20))
+
+    def call(**over):
+        a = dict(good, **over)
+        return lib._lib.mla_qk_rope_concat_and_cache(
+            r(a["qn"]), r(a["qp"]), r(a["kc"]), r(a["kp"]), r(a["pos"]), r(a["cs"]), a["neox"],
+            r(a["slots"]), r(a["qs"]), r(a["ks"]), r(a["qo"]), r(a["kv"]),
+            ctypes.c_void_p(a["err"]) if a["err"] else None, None)
+
+    assert call(qn=None) == 1
+    assert call(qn=_t(b, F32, [T, H, 512])) == 1                          # not bf16
+    assert call(qp=_t(b + (1 << 20), BF, [T, H, 32])) == 1                # rope width
+    assert call(qp=_t(b + (1 << 20) + 2, BF, [T, H, 64])) == 1            # not 16-B aligned
+    assert call(qp=_t(b + (1 << 20), BF, [T, H, 64], [H * 196, 196, 1])) == 1   # stride not 8k
+    assert call(kc=_t(b + (2 << 20), BF, [T + 1, 512])) == 1              # token count
+    assert call(pos=_t(b + (4 << 20), F32, [T])) == 1                     # positions not int32
+    assert call(cs=_t(b + (5 << 20), F32, [128, 32])) == 1                # table width
+    assert call(neox=3) == 1
+    assert call(slots=_t(b + (6 << 20), I32, [T - 1])) == 1
+    assert call(qs=_t(b + (7 << 20), F32, [2])) == 1                      # scale not scalar
+    assert call(qo=_t(b + (9 << 20), F8, [T, H, 576], [H * 640, 640, 1])) == 1  # q_out strided
+    assert call(kv=_t(b + (16 << 20), F8, [64, 3, 1, 576])) == 2          # page_size not 2^k
+    assert call(kv=_t(b + (16 << 20), F8, [1024, 576], [584, 1])) == 1    # pitch not 16-B multiple
+    assert call(err=0) == 1                                               # no error word
+    # no tokens: nothing to do, nothing enqueued
+    assert call(qn=_t(b, BF, [0, H, 512]), qp=_t(b + (1 << 20), BF, [0, H, 64]),
+                kc=_t(b + (2 << 20), BF, [0, 512]), kp=_t(b + (3 << 20), BF, [0, 64]),
+                pos=_t(b + (4 << 20), I32, [0]), slots=_t(b + (6 << 20), I32, [0]),
+                qo=_t(b + (9 << 20), F8, [0, H, 576])) == 0
