@@ -12,7 +12,8 @@
 //   warp 0   : TMA producer.  The K = 512 reduction runs in eight slices of 64: the matrix
 //              slice (64 k rows x 128 n, MN-major, two 128-byte swizzled column chunks) and
 //              the o slice (NT token rows x 64 k, K-major, 128-byte swizzle; rows past the
-//              last token read zeros) land in a 4-stage ring.
+//              last token read zeros) land in eight stages (all in flight at once) for
+//              tiles of up to 64 tokens, else in a ring of 6 (128 tokens) or 4 stages.
 //   warp 1   : MMA issuer (tcgen05 kind::f16, bf16 x bf16, FP32 accumulator in TMEM: lane =
 //              v column n, column = token), four K = 16 MMAs a slice.
 //   warps 2-5: epilogue, TMEM lane quadrant (warp % 4): 16 tokens a load, bf16 stores.
@@ -34,7 +35,6 @@ constexpr int kVK = 512;                      // kv_lora_rank (the reduction)
 constexpr int kVN = 128;                      // v_head_dim (the MMA's M)
 constexpr int kKSlice = 64;                   // k per stage: one 128-byte row of bf16
 constexpr int kSlices = kVK / kKSlice;        // 8
-constexpr int kVStages = 4;
 constexpr int kAChunkBytes = kKSlice * 128;   // 64 k rows x 64 n (128 B): 8 KB
 constexpr int kASliceBytes = 2 * kAChunkBytes;
 constexpr int kVThreads = 192;
@@ -43,8 +43,11 @@ template <int NT>
 struct VLayout {
   static constexpr int kBSliceBytes = NT * 128;                  // NT token rows x 128 B
   static constexpr int kStageBytes = kASliceBytes + kBSliceBytes;  // multiple of 2 KB
+  // up to 64 tokens every slice has its own stage (all eight loads in flight from the
+  // start: one DRAM round trip); wider tiles cycle through a ring of 6 or 4
+  static constexpr int kVStages = NT <= 64 ? kSlices : (NT == 128 ? 6 : 4);
   static constexpr int kBarOff = kVStages * kStageBytes;
-  static constexpr int kSmem = kBarOff + 128 + 1024;             // + 1 KB alignment slack
+  static constexpr int kSmem = kBarOff + 256 + 1024;             // + 1 KB alignment slack
   static constexpr int kTmemCols = NT < 32 ? 32 : NT;
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
   static_assert(kSmem <= 232448, "shared memory");
@@ -91,19 +94,21 @@ __global__ void __launch_bounds__(kVThreads, 1)
     mla_latent_to_v_kernel(const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_o, const VProjParams p) {
   using LY = VLayout<NT>;
+  constexpr int kVStages = LY::kVStages;
   extern __shared__ uint8_t smem_raw[];
   // the swizzled layouts need a 1024-byte aligned window
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
-  // barriers: full[4] (+0), empty[4] (+32), done (+64), drain (+72); then the TMEM base,
-  // the abort flag and a sink for the wait's error bit (this call has no error word)
+  // barriers: full[S] (+0), empty[S] (+8 S), done (+16 S), drain (+16 S + 8); then the
+  // TMEM base, the abort flag and a sink for the wait's error bit (no error word here)
   const uint32_t bars = sbase + LY::kBarOff;
   const uint32_t full0 = bars, empty0 = bars + 8 * kVStages, done = bars + 16 * kVStages;
   const uint32_t drain = done + 8;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + LY::kBarOff + 80);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kBarOff + 84);
-  int* err_sink = reinterpret_cast<int*>(smem + LY::kBarOff + 88);
+  uint8_t* words = smem + LY::kBarOff + 16 * kVStages + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(words);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(words + 4);
+  int* err_sink = reinterpret_cast<int*>(words + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
