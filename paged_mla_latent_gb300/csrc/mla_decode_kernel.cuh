@@ -702,24 +702,38 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
         constexpr uint32_t idesc_pv = idesc_f8(128, NPV, true, true);
         int n_piece = 0;
         Piece pc;
+        // Descriptors are built once, for stage 0, P buffer 0 and the q tile; every MMA's
+        // operand is one of them moved by a compile-time byte offset (desc_at: one 32-bit
+        // add), plus a stage or buffer offset once per tile.  The issuing warp shares its
+        // sub-partition with producer and softmax warps, so the instructions between MMAs
+        // count: building both descriptors from addresses for every MMA cost 2-4 % of the
+        // call time on every workload.
+        const uint64_t k_lat0 = smem_desc(sbase, 16, 1024, kSw128);              // K, latent
+        const uint64_t k_rope0 = smem_desc(sbase + LY::kRopeOff, 16, 512, kSw64);  // K, rope
+        const uint64_t v_lat0 = smem_desc(sbase, LY::kLatBlock, 1024, kSw128);    // V^T
+        const uint64_t q_lat = smem_desc(sQ, 16, 1024, kSw128);
+        const uint64_t q_rope = smem_desc(sQ + 4 * NG * 128, 16, 512, kSw64);
+        // P, MN-major without swizzle: 32 positions (K) in 8-position core matrices of 128
+        // bytes, 128 bytes apart (leading byte offset); NPV columns (MN) in groups of 16,
+        // LY::kPGroup apart (stride byte offset)
+        const uint64_t p0 = smem_desc(LY::kPInRope ? sbase + LY::kRopeOff : sbase + LY::kPOff, 128,
+                                      LY::kPGroup, kSwNone);
         auto issue_pv = [&](uint32_t i, bool first_of_piece) {
           const int sb = i & 1;
           const int stage = static_cast<int>(i % STAGES);
           tc_fence_after();
-          const uint32_t st = sbase + stage * LY::kStageBytes;
-          const uint32_t pbuf = LY::kPInRope ? st + LY::kRopeOff : sbase + LY::kPOff + sb * NPV * LY::kTile;
+          const uint64_t va = desc_at(v_lat0, stage * LY::kStageBytes);
+          const uint64_t pb = desc_at(p0, LY::kPInRope ? stage * LY::kStageBytes : sb * NPV * LY::kTile);
   #pragma unroll
           for (int bk = 0; bk < 4; ++bk) {
             const uint32_t d = tmem + LY::kOBase + bk * NPV;
   #pragma unroll
             for (int kk = 0; kk < LY::kTile / 32; ++kk) {
-              // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K)
-              const uint64_t a = smem_desc(st + bk * LY::kLatBlock + kk * 32 * 128, LY::kLatBlock, 1024, kSw128);
-              // B = P, MN-major without swizzle: 32 positions (K) in 8-position core
-              // matrices of 128 bytes, 128 bytes apart (leading byte offset); NPV columns
-              // (MN) in groups of 16, LY::kPGroup apart (stride byte offset)
-              const uint64_t b = smem_desc(pbuf + kk * 4 * 128, 128, LY::kPGroup, kSwNone);
-              mma_f8_warp(d, a, b, idesc_pv, (first_of_piece && kk == 0) ? 0u : 1u);
+              // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K);
+              // B = P: 32 positions (K) x NPV columns
+              mma_f8_warp(d, desc_at(va, bk * LY::kLatBlock + kk * 32 * 128),
+                          desc_at(pb, kk * 4 * 128), idesc_pv,
+                          (first_of_piece && kk == 0) ? 0u : 1u);
             }
           }
           mma_commit_warp(mbase + kMiscEmpty + 8 * stage);
@@ -731,20 +745,17 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           // through the async proxy
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t st = sbase + stage * LY::kStageBytes;
+          const uint64_t ka = desc_at(k_lat0, stage * LY::kStageBytes);
+          const uint64_t kr = desc_at(k_rope0, stage * LY::kStageBytes);
           const uint32_t d = tmem + (i & 1) * LY::kSStride;
   #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {   // latent columns 0..511, 32 per MMA
-            const uint64_t a = smem_desc(st + (kk >> 2) * LY::kLatBlock + (kk & 3) * 32, 16, 1024, kSw128);
-            const uint64_t b = smem_desc(sQ + (kk >> 2) * NG * 128 + (kk & 3) * 32, 16, 1024, kSw128);
-            mma_f8_warp(d, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 16; ++kk)   // latent columns 0..511, 32 per MMA
+            mma_f8_warp(d, desc_at(ka, (kk >> 2) * LY::kLatBlock + (kk & 3) * 32),
+                        desc_at(q_lat, (kk >> 2) * NG * 128 + (kk & 3) * 32), idesc_qk,
+                        kk > 0 ? 1u : 0u);
   #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {    // rope columns 512..575
-            const uint64_t a = smem_desc(st + LY::kRopeOff + kk * 32, 16, 512, kSw64);
-            const uint64_t b = smem_desc(sQ + 4 * NG * 128 + kk * 32, 16, 512, kSw64);
-            mma_f8_warp(d, a, b, idesc_qk, 1u);
-          }
+          for (int kk = 0; kk < 2; ++kk)    // rope columns 512..575
+            mma_f8_warp(d, desc_at(kr, kk * 32), desc_at(q_rope, kk * 32), idesc_qk, 1u);
           mma_commit_warp(mbase + kMiscSFull + 8 * (i & 1));
         };
         if constexpr (STAGES >= 3) {

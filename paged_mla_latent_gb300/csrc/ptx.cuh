@@ -301,6 +301,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The descriptor d moved by `bytes` (a multiple of 16; the address stays below 256 KB):
+// only the 14-bit start-address field changes, and it sits in the low word, so one 32-bit
+// add does it.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B and an FP32 accumulator.
 //   [4,6) D format (1 = f32), [7,10) A format (0 = e4m3), [10,13) B format,
 //   [15] A MN-major, [16] B MN-major, [17,23) N >> 3, [24,29) M >> 4.
