@@ -63,15 +63,17 @@ NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "m
 # What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
 # HBM copy peak, but not every call is HBM-bound.
 LIMITER = {
-    "c16+shared_prefix": "pipeline latency of the 48-row tile (MMA issue, softmax, the QK -> "
-                         "softmax -> PV chain) and the cascade merge; DRAM and tensor pipe "
-                         "each near 20 % busy (profiles/mla_decode_c16.md)",
+    "c16+shared_prefix": "MMA instructions: about 30 per 96-position tile of 48 query rows "
+                         "at ~100 cycles each (a fixed cost per tcgen05 instruction, the "
+                         "arithmetic is ~24 of them), plus the cascade merge; DRAM ~23 % "
+                         "busy (profiles/mla_decode_c16.md)",
     "c24+shared_prefix": "as c16+shared_prefix",
-    "c16": "HBM and L2: every request gathers the shared prefix, which L2 serves after the "
-           "first reads",
+    "c16": "MMA instructions (34 per 128-position tile of 16 query rows) while every "
+           "request gathers the shared prefix, which L2 serves after the first reads",
     "c24": "as c16",
-    "long": "fixed per-call latencies (launch, set-up, first tile, epilogue, merge) around "
-            "~7 tiles per CTA (profiles/mla_decode_long.md)",
+    "long": "fixed per-call latencies (launch, first rows ~4 us after launch, epilogue, "
+            "the slowest CTA, merge) around 8 tiles per CTA streamed at ~4.7 TB/s "
+            "(profiles/mla_decode_long.md)",
     "mtp": "one ring stage's round trip (row copies, QK, softmax, PV) at three stages in "
            "flight (profiles/mla_decode_mtp.md)",
 }
