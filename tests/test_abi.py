@@ -254,3 +254,13 @@ def test_rope_cache_rejects_bad_arguments_on_host(lib):
                 kc=_t(b + (2 << 20), BF, [0, 512]), kp=_t(b + (3 << 20), BF, [0, 64]),
                 pos=_t(b + (4 << 20), I32, [0]), slots=_t(b + (6 << 20), I32, [0]),
                 qo=_t(b + (9 << 20), F8, [0, H, 576])) == 0
+
+
+def test_bounded_wait_selftest_rejects_bad_arguments_on_host(lib):
+    """The wait's self-test checks its limit and pointers before launching anything."""
+    f = lib._lib.mla_selftest_bounded_wait
+    word, res = ctypes.c_void_p(1 << 40), ctypes.c_void_p((1 << 40) + 64)
+    assert f(None, res, 1_000_000, None) == 1
+    assert f(word, None, 1_000_000, None) == 1
+    for bad in (0, 999, 100_000_001):
+        assert f(word, res, bad, None) == 1
