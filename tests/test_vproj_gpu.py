@@ -39,7 +39,10 @@ def _check(o, w, v):
     return float((err / bound).max())
 
 
-@pytest.mark.parametrize("n_tok,H", [(16, 12), (1, 96), (37, 12), (256, 12), (1061, 12), (3, 16)])
+# token tiles: 16 (c16, 96-head shard, ragged), 32 (mtp), 128 (1,061 tokens: nine tiles, six
+# stages cycling), 256 (4,096 tokens: a ring of four stages), one head
+@pytest.mark.parametrize("n_tok,H", [(16, 12), (1, 96), (37, 12), (256, 12), (1061, 12), (3, 16),
+                                     (4096, 12), (200, 1)])
 def test_latent_to_v_matches_oracle(pm, n_tok, H):
     o, w = mla_inputs.make_vproj(n_tok, H, seed=n_tok + H, device="cuda")
     v = torch.full((n_tok, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
