@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/paged_mla.h"
 #include "mla_api_internal.h"
@@ -222,14 +223,18 @@ template <int NT>
 cudaError_t launch_vproj(const CUtensorMap& tw, const CUtensorMap& to, const VProjParams& p,
                          int H, cudaStream_t stream) {
   using LY = VLayout<NT>;
+  static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(mla_latent_to_v_kernel<NT>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(mla_latent_to_v_kernel<NT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
   }
   const dim3 grid(static_cast<unsigned>((p.n_tok + NT - 1) / NT), static_cast<unsigned>(H));
   mla_latent_to_v_kernel<NT><<<grid, kVThreads, LY::kSmem, stream>>>(tw, to, p);
