@@ -79,7 +79,7 @@ enum : int {
   kMiscTmem = 128,    // u32 tensor memory base
   kMiscAbort = 132,   // int abort flag
   kMiscRowOff = 192,  // int64 row output offsets [NG] (NG <= 48 -> 384 bytes, to 576)
-  kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG], then int lim[NG]
+  kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG]
 };
 
 // Cache positions per pipeline tile.  The MMA's M is always 128 (TMEM lanes = positions);
@@ -110,10 +110,10 @@ struct DecodeLayout {
   static_assert(kStageBytes % 1024 == 0 && kLatBlock % 1024 == 0, "swizzle atoms");
   static constexpr int kMiscOff = kPOff + kPBytes;
   static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 3072;
-  static constexpr int kMiscLim = kMiscRed + 5 * NG * 4;        // int causal limit [NG]
+  static constexpr int kMiscRedEnd = kMiscRed + 5 * NG * 4;     // red[4][NG], scale [NG]
   // tile-max exchange of each softmax warpgroup (64 floats; one group uses red)
-  static constexpr int kMiscXch = (kMiscLim + 4 * NG + 15) / 16 * 16;
-  static_assert((NG <= 16 ? kMiscLim + 4 * NG : kMiscXch + 256 * (NG / 16)) <= kMiscBytes,
+  static constexpr int kMiscXch = (kMiscRedEnd + 15) / 16 * 16;
+  static_assert((NG <= 16 ? kMiscRedEnd : kMiscXch + 256 * (NG / 16)) <= kMiscBytes,
                 "misc region overflow");
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
   // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
@@ -342,7 +342,6 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
     float* s_alpha = red + 4 * NG + c0;      // this chunk's rescale factors [16]
     float* xch = LY::kGroups == 1 ? red
                                   : reinterpret_cast<float*>(misc + LY::kMiscXch) + 64 * grp;
-    int* s_lim = reinterpret_cast<int*>(misc + LY::kMiscLim);
     constexpr int kCh = NG / 16;
 
     uint32_t it_g = 0;
@@ -360,9 +359,11 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
         l_acc[k] = 0.f;
       }
       const int causal_from = pc.cfrom;   // positions beyond this need the causal test
-      // draft t of this group's row n sees positions <= L - T + t
-      if (prow < 16) s_lim[c0 + prow] = causal_from + (pc.g * NG + c0 + prow) / H;
-      bar_sync(bar_g, 128);
+      // Row r = pc.g * NG + n of the group is draft r / H, which sees positions
+      // <= causal_from + r / H.  At position pos > causal_from the columns beyond their
+      // draft's limit are therefore a prefix of the chunk: k < (pos - causal_from) * H - row0.
+      const int row0 = pc.g * NG + c0;
+      const int rows_left = pc.rows - c0;   // columns k >= rows_left are padding rows
       for (int t = 0; t < nt; ++t, ++it_g) {
         const int sb = it_g & 1;
         mbar_wait(mbase + kMiscSFull + 8 * sb, (it_g >> 1) & 1, abort_flag, prm.err);
@@ -371,13 +372,22 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const int pos = pc.j0 + t * LY::kTile + prow;
           // (lanes past a 96-position tile hold don't-care logits and write no P)
           const bool in_piece = prow < LY::kTile && pos < pc.j1;
-          const bool causal = in_piece && pos > causal_from;
-          // scaled logit (log2 units) of column n, with masks: past the piece or beyond the
+          // columns k < kcut of this position are masked: all of them past the piece, the
+          // prefix beyond the drafts' limits under the causal rule.  One cut per tile keeps
+          // the per-column work to two compares and selects (a per-column limit read from
+          // shared memory cost ~0.3 us a tile in the shared-prefix call).
+          int kcut = 0;
+          if (!in_piece) {
+            kcut = 16;
+          } else if (pos > causal_from) {
+            const int64_t cut = static_cast<int64_t>(pos - causal_from) * H - row0;
+            kcut = cut >= 16 ? 16 : (cut <= 0 ? 0 : static_cast<int>(cut));
+          }
+          // scaled logit (log2 units) of column k, with masks: past the piece or beyond the
           // draft's causal limit -> -inf; padding rows -> 0 (finite, discarded)
-          auto xform = [&](float sraw, int n) -> float {
-            float v = in_piece ? sraw * scale_log2 : -INFINITY;
-            if (causal && pos > s_lim[n]) v = -INFINITY;
-            return (n >= pc.rows) ? 0.f : v;
+          auto xform = [&](float sraw, int k) -> float {
+            const float v = k < kcut ? -INFINITY : sraw * scale_log2;
+            return k < rows_left ? v : 0.f;
           };
           const int stage = static_cast<int>(it_g % STAGES);
           // P tile: this position's 16-byte vectors (see LY::kPGroup)
@@ -386,11 +396,24 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           float xs[16];
           tmem_ld16(tl + sb * LY::kSStride + c0, xs);
           tmem_wait_ld();
+          // The softmax warps share their schedulers with the producer and MMA warps, and
+          // their time per tile follows their instruction count: positions inside the piece
+          // with 16 real rows and no causal cut (almost all of them) skip the masks.
+          // Lanes past a 96-position tile (a whole warp) hold no position: all -inf.
           float dmax = -INFINITY;
+          if (prow >= LY::kTile) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            xs[k] = xform(xs[k], c0 + k);
-            dmax = fmaxf(dmax, xs[k] - m_ref[k]);
+            for (int k = 0; k < 16; ++k) xs[k] = -INFINITY;
+          } else {
+            if (kcut == 0 && rows_left >= 16) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) xs[k] *= scale_log2;
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], k);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) dmax = fmaxf(dmax, xs[k] - m_ref[k]);
           }
           if (bar_red_or(bar_g, 128, dmax > kMoveAt)) {
             // rare: move these columns' reference to their tile maxima
@@ -434,26 +457,28 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           }
           // scaled probabilities (<= 2^kMoveAt), split into two FP8 planes:
           // hi = e4m3(p), lo = e4m3(kLoScale (p - hi)), the residual taken in f16x2
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int k = 0; k < 16; k += 2) {
-            const float p0 = ex2_approx(xs[k] - m_ref[k]);
-            const float p1 = ex2_approx(xs[k + 1] - m_ref[k + 1]);
-            l_acc[k] += p0;
-            l_acc[k + 1] += p1;
-            const uint32_t p16 = f32x2_to_f16x2(p1, p0);          // low half: p0
-            const uint32_t hi = f16x2_to_e4m3x2(p16);             // byte 0: p0, byte 1: p1
-            const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), kLoScaleF16x2);
-            const uint32_t lo = f16x2_to_e4m3x2(r16);              // kLoScale (p - hi)
-            if ((k & 2) == 0) {
-              hw[k >> 2] = hi;
-              lw[k >> 2] = lo;
-            } else {
-              hw[k >> 2] |= hi << 16;
-              lw[k >> 2] |= lo << 16;
-            }
-          }
+          // (positions past a 96-position tile hold no P: their weights are 0 and their
+          // lanes skip the conversion)
           if (prow < LY::kTile) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+              const float p0 = ex2_approx(xs[k] - m_ref[k]);
+              const float p1 = ex2_approx(xs[k + 1] - m_ref[k + 1]);
+              l_acc[k] += p0;
+              l_acc[k + 1] += p1;
+              const uint32_t p16 = f32x2_to_f16x2(p1, p0);          // low half: p0
+              const uint32_t hi = f16x2_to_e4m3x2(p16);             // byte 0: p0, byte 1: p1
+              const uint32_t r16 = f16x2_mul(f16x2_sub(p16, e4m3x2_to_f16x2(hi)), kLoScaleF16x2);
+              const uint32_t lo = f16x2_to_e4m3x2(r16);              // kLoScale (p - hi)
+              if ((k & 2) == 0) {
+                hw[k >> 2] = hi;
+                lw[k >> 2] = lo;
+              } else {
+                hw[k >> 2] |= hi << 16;
+                lw[k >> 2] |= lo << 16;
+              }
+            }
             *reinterpret_cast<uint4*>(pb + grp * LY::kPGroup) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(pb + (kCh + grp) * LY::kPGroup) =
                 make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -662,7 +687,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             cp_async_16(dst, kv + off + 16 * lane, ((vmask >> j) & 1u) << 4);
           }
           // rope columns: 8 rows x 4 chunks per instruction
-  #pragma unroll
+#pragma unroll
           for (int m = 0; m < (LY::kRowsPerProducer + 7) / 8; ++m) {
             const int j = 8 * m + (lane >> 2);
             const int c = lane & 3;
@@ -724,10 +749,10 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           tc_fence_after();
           const uint64_t va = desc_at(v_lat0, stage * LY::kStageBytes);
           const uint64_t pb = desc_at(p0, LY::kPInRope ? stage * LY::kStageBytes : sb * NPV * LY::kTile);
-  #pragma unroll
+#pragma unroll
           for (int bk = 0; bk < 4; ++bk) {
             const uint32_t d = tmem + LY::kOBase + bk * NPV;
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < LY::kTile / 32; ++kk) {
               // A = V^T block bk: 128 value columns (MN, contiguous) x 32 positions (K);
               // B = P: 32 positions (K) x NPV columns
@@ -748,12 +773,12 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const uint64_t ka = desc_at(k_lat0, stage * LY::kStageBytes);
           const uint64_t kr = desc_at(k_rope0, stage * LY::kStageBytes);
           const uint32_t d = tmem + (i & 1) * LY::kSStride;
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 16; ++kk)   // latent columns 0..511, 32 per MMA
             mma_f8_warp(d, desc_at(ka, (kk >> 2) * LY::kLatBlock + (kk & 3) * 32),
                         desc_at(q_lat, (kk >> 2) * NG * 128 + (kk & 3) * 32), idesc_qk,
                         kk > 0 ? 1u : 0u);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 2; ++kk)    // rope columns 512..575
             mma_f8_warp(d, desc_at(kr, kk * 32), desc_at(q_rope, kk * 32), idesc_qk, 1u);
           mma_commit_warp(mbase + kMiscSFull + 8 * (i & 1));
