@@ -79,7 +79,7 @@ enum : int {
   kMiscTmem = 128,    // u32 tensor memory base
   kMiscAbort = 132,   // int abort flag
   kMiscRowOff = 192,  // int64 row output offsets [NG] (NG <= 48 -> 384 bytes, to 576)
-  kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG]
+  kMiscRed = 640,     // float red[4][NG], then float scale / alpha [NG], then int lim[NG]
 };
 
 // Cache positions per pipeline tile.  The MMA's M is always 128 (TMEM lanes = positions);
@@ -110,10 +110,10 @@ struct DecodeLayout {
   static_assert(kStageBytes % 1024 == 0 && kLatBlock % 1024 == 0, "swizzle atoms");
   static constexpr int kMiscOff = kPOff + kPBytes;
   static constexpr int kMiscBytes = (NG <= 16) ? 1024 : 3072;
-  static constexpr int kMiscRedEnd = kMiscRed + 5 * NG * 4;     // red[4][NG], scale [NG]
+  static constexpr int kMiscLim = kMiscRed + 5 * NG * 4;        // int causal limit [NG]
   // tile-max exchange of each softmax warpgroup (64 floats; one group uses red)
-  static constexpr int kMiscXch = (kMiscRedEnd + 15) / 16 * 16;
-  static_assert((NG <= 16 ? kMiscRedEnd : kMiscXch + 256 * (NG / 16)) <= kMiscBytes,
+  static constexpr int kMiscXch = (kMiscLim + 4 * NG + 15) / 16 * 16;
+  static_assert((NG <= 16 ? kMiscLim + 4 * NG : kMiscXch + 256 * (NG / 16)) <= kMiscBytes,
                 "misc region overflow");
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes;
   // Tensor memory columns: two S buffers, then four O blocks of kNPV columns.
@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
     float* s_alpha = red + 4 * NG + c0;      // this chunk's rescale factors [16]
     float* xch = LY::kGroups == 1 ? red
                                   : reinterpret_cast<float*>(misc + LY::kMiscXch) + 64 * grp;
+    int* s_lim = reinterpret_cast<int*>(misc + LY::kMiscLim);   // 16-row kernel only
     constexpr int kCh = NG / 16;
 
     uint32_t it_g = 0;
@@ -359,11 +360,12 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
         l_acc[k] = 0.f;
       }
       const int causal_from = pc.cfrom;   // positions beyond this need the causal test
-      // Row r = pc.g * NG + n of the group is draft r / H, which sees positions
-      // <= causal_from + r / H.  At position pos > causal_from the columns beyond their
-      // draft's limit are therefore a prefix of the chunk: k < (pos - causal_from) * H - row0.
-      const int row0 = pc.g * NG + c0;
-      const int rows_left = pc.rows - c0;   // columns k >= rows_left are padding rows
+      if constexpr (NG == 16) {
+        // draft t of this group's row n sees positions <= causal_from + t (16-row kernel:
+        // one limit per column in shared memory, see the masks below)
+        if (prow < 16) s_lim[c0 + prow] = causal_from + (pc.g * NG + c0 + prow) / H;
+        bar_sync(bar_g, 128);
+      }
       for (int t = 0; t < nt; ++t, ++it_g) {
         const int sb = it_g & 1;
         mbar_wait(mbase + kMiscSFull + 8 * sb, (it_g >> 1) & 1, abort_flag, prm.err);
@@ -372,23 +374,8 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const int pos = pc.j0 + t * LY::kTile + prow;
           // (lanes past a 96-position tile hold don't-care logits and write no P)
           const bool in_piece = prow < LY::kTile && pos < pc.j1;
-          // columns k < kcut of this position are masked: all of them past the piece, the
-          // prefix beyond the drafts' limits under the causal rule.  One cut per tile keeps
-          // the per-column work to two compares and selects (a per-column limit read from
-          // shared memory cost ~0.3 us a tile in the shared-prefix call).
-          int kcut = 0;
-          if (!in_piece) {
-            kcut = 16;
-          } else if (pos > causal_from) {
-            const int64_t cut = static_cast<int64_t>(pos - causal_from) * H - row0;
-            kcut = cut >= 16 ? 16 : (cut <= 0 ? 0 : static_cast<int>(cut));
-          }
-          // scaled logit (log2 units) of column k, with masks: past the piece or beyond the
-          // draft's causal limit -> -inf; padding rows -> 0 (finite, discarded)
-          auto xform = [&](float sraw, int k) -> float {
-            const float v = k < kcut ? -INFINITY : sraw * scale_log2;
-            return k < rows_left ? v : 0.f;
-          };
+          // Scaled logits (log2 units) with masks: past the piece or beyond the draft's
+          // causal limit -> -inf; padding rows -> 0 (finite, discarded).
           const int stage = static_cast<int>(it_g % STAGES);
           // P tile: this position's 16-byte vectors (see LY::kPGroup)
           uint8_t* pb = (LY::kPInRope ? smem + stage * LY::kStageBytes + LY::kRopeOff
@@ -396,21 +383,47 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           float xs[16];
           tmem_ld16(tl + sb * LY::kSStride + c0, xs);
           tmem_wait_ld();
-          // The softmax warps share their schedulers with the producer and MMA warps, and
-          // their time per tile follows their instruction count: positions inside the piece
-          // with 16 real rows and no causal cut (almost all of them) skip the masks.
-          // Lanes past a 96-position tile (a whole warp) hold no position: all -inf.
           float dmax = -INFINITY;
-          if (prow >= LY::kTile) {
+          if constexpr (NG == 16) {
+            // One limit per column, read from shared memory.  (The per-tile cut below, and
+            // even the row bound held as (rows - c0) across the tile loop, measured 4 %
+            // slower on the 16-row kernel's calls, with fewer instructions executed and more
+            // instruction-fetch stalls; the cause was not found.)
+            const bool causal = in_piece && pos > causal_from;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float v = in_piece ? xs[k] * scale_log2 : -INFINITY;
+              if (causal && pos > s_lim[c0 + k]) v = -INFINITY;
+              xs[k] = (c0 + k >= pc.rows) ? 0.f : v;
+              dmax = fmaxf(dmax, xs[k] - m_ref[k]);
+            }
+          } else if (prow >= LY::kTile) {
+            // lanes past a 96-position tile (a whole warp) hold no position
 #pragma unroll
             for (int k = 0; k < 16; ++k) xs[k] = -INFINITY;
           } else {
-            if (kcut == 0 && rows_left >= 16) {
+            // Row r = pc.g * NG + c0 + k of the group is draft r / H, which sees positions
+            // <= causal_from + r / H: at position pos the columns beyond their drafts' limits
+            // are the prefix k < (pos - causal_from) * H - (pc.g * NG + c0) of the chunk (none
+            // at or before causal_from).  One cut per tile, and no masks at all for interior
+            // positions with 16 real rows: the softmax warps share their schedulers with the
+            // producer and MMA warps, and their time per tile follows their instruction count
+            // (a per-column limit read from shared memory cost ~0.3 us a tile in the
+            // shared-prefix call).
+            const int rows_left = pc.rows - c0;   // columns k >= rows_left are padding rows
+            const int64_t cut = static_cast<int64_t>(pos - causal_from) * H - (pc.g * NG + c0);
+            const int kcut = static_cast<int>(cut < 0 ? 0 : (cut > 16 ? 16 : cut));
+            if (in_piece && kcut == 0 && rows_left >= 16) {
 #pragma unroll
               for (int k = 0; k < 16; ++k) xs[k] *= scale_log2;
-            } else {
+            } else if (in_piece && kcut == 0) {
 #pragma unroll
-              for (int k = 0; k < 16; ++k) xs[k] = xform(xs[k], k);
+              for (int k = 0; k < 16; ++k) xs[k] = k < rows_left ? xs[k] * scale_log2 : 0.f;
+            } else {
+              const int kc = in_piece ? kcut : 16;
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                xs[k] = k < rows_left ? (k < kc ? -INFINITY : xs[k] * scale_log2) : 0.f;
             }
 #pragma unroll
             for (int k = 0; k < 16; ++k) dmax = fmaxf(dmax, xs[k] - m_ref[k]);
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           // hi = e4m3(p), lo = e4m3(kLoScale (p - hi)), the residual taken in f16x2
           // (positions past a 96-position tile hold no P: their weights are 0 and their
           // lanes skip the conversion)
-          if (prow < LY::kTile) {
+          if (LY::kTile == 128 || prow < LY::kTile) {
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
