@@ -63,19 +63,22 @@ NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "m
 # What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
 # HBM copy peak, but not every call is HBM-bound.
 LIMITER = {
-    "c16+shared_prefix": "MMA instructions: about 30 per 96-position tile of 48 query rows "
-                         "at ~100 cycles each (a fixed cost per tcgen05 instruction, the "
-                         "arithmetic is ~24 of them), plus the cascade merge; DRAM ~23 % "
-                         "busy (profiles/mla_decode_c16.md)",
+    "c16+shared_prefix": "the 48-row tile pipeline: a ring stage is refilled only after its "
+                         "PV, and the row copies (~0.7 us to issue 96 rows) plus their "
+                         "arrival take longer than the two tiles in between, so the MMA warp "
+                         "waits ~0.4 us a tile for rows after issuing its 30 MMAs at the "
+                         "lone-warp rate; plus the cascade merge; DRAM ~23 % busy "
+                         "(profiles/mla_decode_c16.md)",
     "c24+shared_prefix": "as c16+shared_prefix",
-    "c16": "MMA instructions (34 per 128-position tile of 16 query rows) while every "
-           "request gathers the shared prefix, which L2 serves after the first reads",
+    "c16": "the 16-row tile pipeline while every request gathers the shared prefix (L2 "
+           "serves it after the first reads): ~1.44 us per 128-position tile, the row "
+           "copies' issue (~0.86 us a tile) and the ring's round trip",
     "c24": "as c16",
     "long": "fixed per-call latencies (launch, first rows ~4 us after launch, epilogue, "
             "the slowest CTA, merge) around 8 tiles per CTA streamed at ~4.7 TB/s "
             "(profiles/mla_decode_long.md)",
     "mtp": "one ring stage's round trip (row copies, QK, softmax, PV) at three stages in "
-           "flight (profiles/mla_decode_mtp.md)",
+           "flight; DRAM 65 % busy (profiles/mla_decode_mtp.md)",
 }
 
 
