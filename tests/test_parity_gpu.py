@@ -145,6 +145,16 @@ def test_causal_drafts(pm, scales):
     _check(case)
 
 
+@pytest.mark.parametrize("H,T", [(24, 2), (16, 3), (8, 4), (20, 2), (40, 3)])
+def test_causal_drafts_other_head_counts(pm, H, T):
+    """Draft boundaries that fall inside a 16-row softmax chunk at other alignments than
+    12 heads give (rows t * H of a group), short last chunks, and groups of 32 and 48
+    rows; a request shorter than its drafts' window (L == T) included."""
+    case = mla_inputs.make_custom([T, 97, 700], q_lens=[T] * 3, H=H, seed=17 + H + T,
+                                  q_scale=1.0, kv_scale=1.0, name=f"mtp-H{H}-T{T}")
+    _check(case)
+
+
 def test_mixed_query_lengths(pm):
     case = mla_inputs.make_custom([300, 800, 50, 1200], q_lens=[1, 3, 2, 4], H=12, seed=7,
                                   q_scale=1.0, kv_scale=1.0, name="mixed-q")
