@@ -563,6 +563,14 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
           const bool vec = !direct || prm.o_vec16;
           float* fdst = direct ? reinterpret_cast<float*>(prm.o) : prm.part_o;
           __nv_bfloat16* hdst = reinterpret_cast<__nv_bfloat16*>(prm.o);
+          // the rows' scales and this lane's output rows, read once for the four blocks
+          float scl[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) scl[k] = s_scale[c0 + k];
+          int64_t offq[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            offq[g] = s_off[c0 + (to_bf16 ? 8 * (g & 1) + (lane & 7) : 4 * g + (lane & 3))];
           #pragma unroll 1
           for (int bk = 0; bk < 4; ++bk) {
             float hi[16], lo[16];
@@ -570,7 +578,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
             tmem_ld16(tl + LY::kOBase + bk * NPV + NG + c0, lo);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) hi[k] = (hi[k] + lo[k] * (1.0f / kLoScale)) * s_scale[c0 + k];
+            for (int k = 0; k < 16; ++k) hi[k] = (hi[k] + lo[k] * (1.0f / kLoScale)) * scl[k];
             const int cw = bk * 128 + 32 * q4;   // first column of this warp
             if (!vec) {
 #pragma unroll
@@ -588,7 +596,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
               const int cs = cw + 8 * (lane >> 3);
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const int64_t off = s_off[c0 + 8 * h + (lane & 7)];
+                const int64_t off = offq[h];
                 if (off >= 0) {
                   const float* a = hi + 8 * h;
                   *reinterpret_cast<uint4*>(hdst + off + cs) =
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(DecodeLayout<NG, STAGES>::kThreads, 1)
               const int cs = cw + 4 * (lane >> 2);
 #pragma unroll
               for (int g = 0; g < 4; ++g) {
-                const int64_t off = s_off[c0 + 4 * g + (lane & 3)];
+                const int64_t off = offq[g];
                 if (off >= 0)
                   *reinterpret_cast<float4*>(fdst + off + cs) =
                       make_float4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
