@@ -525,7 +525,7 @@ def main():
     t_host = (time.perf_counter() - t_host0) / 20
     torch.cuda.synchronize(dev)
 
-    # The other workloads of the benchmark spec, timed in the same process and clock record;
+    # The other measured workloads (c24, long, mtp, long96), timed in the same process and clock record;
     # their inputs are built before the record starts.
     extra_list = []
     if args.extra_configs == "default":
