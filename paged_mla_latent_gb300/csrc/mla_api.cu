@@ -186,15 +186,19 @@ struct Plan {
   int NG, groups, grid, splits;
   int64_t slots;
   size_t lse_off, o_off, bytes;
-  // Shared-prefix cascade (decode batches of <= 24 rows per request, at least one group):
-  // 48-row tiles over gsize-request prefix units and per-request units, pslots partial
+  // Shared-prefix cascade (decode batches of <= 48 rows per request, at least one group):
+  // cng-row tiles over gsize-request prefix units and per-request units, pslots partial
   // slots at plse_off / po_off (same header); cbytes = the larger of both layouts.
   bool cascade_ok;
+  int cng;
   int gsize;
   int64_t pslots;
   size_t plse_off, po_off, cbytes;
 };
-constexpr int kPrefixNG = 48;
+// Rows of the cascade's tiles: 96 (the rows-on-lanes kernel) when a group of at least two
+// requests fits and the batch fills one; else 48 for batches of 2..3 small requests.
+constexpr int kPrefixNG = 96;
+constexpr int kPrefixNGSmall = 48;
 
 int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Plan* p) {
   if (B < 0 || H < 1 || H > kMaxHeads || max_seqlen_q < 1 || max_seqlen_q > kMaxSeqlenQ)
@@ -210,20 +214,27 @@ int make_plan(int B, int64_t H, int max_seqlen_q, int num_kv_splits, int sms, Pl
   p->o_off = align_up(p->lse_off + static_cast<size_t>(p->slots) * p->NG * sizeof(float), 256);
   p->bytes = p->o_off + static_cast<size_t>(p->slots) * p->NG * kDV * sizeof(float);
   p->cascade_ok = false;
+  p->cng = kPrefixNG;
   p->gsize = 1;
   p->pslots = 0;
   p->plse_off = p->po_off = p->bytes;
   p->cbytes = p->bytes;
-  if (p->splits == 0 && rows <= kPrefixNG / 2 && B >= kPrefixNG / rows) {
-    // (at least one full group: for fewer requests the extra launches cost more than
-    // sharing the prefix saves)
+  // (at least one full group: for fewer requests the extra launches cost more than
+  // sharing the prefix saves)
+  int cng = 0;
+  if (rows <= kPrefixNG / 2 && B >= kPrefixNG / rows)
+    cng = kPrefixNG;
+  else if (rows <= kPrefixNGSmall / 2 && B >= kPrefixNGSmall / rows)
+    cng = kPrefixNGSmall;
+  if (p->splits == 0 && cng > 0) {
     p->cascade_ok = true;
-    p->gsize = kPrefixNG / rows;
+    p->cng = cng;
+    p->gsize = cng / rows;
     const int VP = (B + p->gsize - 1) / p->gsize;
     p->pslots = partial_slots(VP + B, 1, 0, p->grid);
     p->plse_off = kHeaderBytes;
-    p->po_off = align_up(p->plse_off + static_cast<size_t>(p->pslots) * kPrefixNG * sizeof(float), 256);
-    const size_t end = p->po_off + static_cast<size_t>(p->pslots) * kPrefixNG * kDV * sizeof(float);
+    p->po_off = align_up(p->plse_off + static_cast<size_t>(p->pslots) * cng * sizeof(float), 256);
+    const size_t end = p->po_off + static_cast<size_t>(p->pslots) * cng * kDV * sizeof(float);
     p->cbytes = end > p->bytes ? end : p->bytes;
   }
   return MLA_OK;
@@ -281,19 +292,19 @@ cudaError_t launch_merge(const MergeShape& ms, int64_t n_rows, const Params& mp,
   return cudaLaunchKernelExC(&cfg, merge_fn<K>(ms), args);
 }
 
-// Shared-prefix cascade: one launch of the 48-row kernel over the prefix units (groups of
-// plan.gsize requests attending the first `shared` positions) and the requests' own
+// Shared-prefix cascade: one launch of the plan.cng-row kernel over the prefix units (groups
+// of plan.gsize requests attending the first `shared` positions) and the requests' own
 // units, then the cascade merge of each row's two parts.
 int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr, int64_t q_rows,
                    int32_t shared, int max_rows, cudaStream_t stream) {
   uint8_t* ws = reinterpret_cast<uint8_t*>(prm.err);
   int rc;
   CUtensorMap p_lat, p_rope;
-  if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-  if ((rc = make_map(&p_rope, q_ptr, q_rows, kD, 64, kPrefixNG, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
+  if ((rc = make_map(&p_lat, q_ptr, q_rows, kD, 128, plan.cng, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  if ((rc = make_map(&p_rope, q_ptr, q_rows, kD, 64, plan.cng, CU_TENSOR_MAP_SWIZZLE_64B))) return rc;
   DecodeParams pp = prm;
   pp.sp.mode = pp.sp.log2_page > 0 ? kSchedCascadePaged : kSchedCascade;
-  pp.sp.NG = kPrefixNG;
+  pp.sp.NG = plan.cng;
   pp.sp.groups = 1;
   pp.sp.gsize = plan.gsize;
   pp.sp.shared = shared;
@@ -301,7 +312,9 @@ int launch_cascade(const Plan& plan, const DecodeParams& prm, const void* q_ptr,
   pp.part_lse = reinterpret_cast<float*>(ws + plan.plse_off);
   pp.part_o = reinterpret_cast<float*>(ws + plan.po_off);
   pp.n_slots = plan.pslots;
-  if ((rc = launch_decode_ng48(p_lat, p_rope, pp, plan.grid, stream))) return rc;
+  rc = plan.cng == kPrefixNG ? launch_decode_ng96(p_lat, p_rope, pp, plan.grid, stream)
+                             : launch_decode_ng48(p_lat, p_rope, pp, plan.grid, stream);
+  if (rc) return rc;
 
   CascadeMergeParams mp;
   mp.sp = pp.sp;
@@ -418,7 +431,8 @@ int decode_impl(const mla_tensor_t* q, const mla_tensor_t* kv_buffer, const mla_
   switch (plan.NG) {
     case 16: rc = launch_decode_ng16(q_lat, q_rope, prm, plan.grid, stream); break;
     case 32: rc = launch_decode_ng32(q_lat, q_rope, prm, plan.grid, stream); break;
-    default: rc = launch_decode_ng48(q_lat, q_rope, prm, plan.grid, stream); break;
+    case 48: rc = launch_decode_ng48(q_lat, q_rope, prm, plan.grid, stream); break;
+    default: rc = launch_decode_ng96(q_lat, q_rope, prm, plan.grid, stream); break;
   }
   if (rc) return rc;
 

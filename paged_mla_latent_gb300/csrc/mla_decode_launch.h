@@ -16,5 +16,8 @@ int launch_decode_ng32(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream);
 int launch_decode_ng48(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
                        const DecodeParams& prm, int grid, cudaStream_t stream);
+// mla_decode_rows96_kernel (mla_decode_rows96.cuh): 96 rows, any schedule mode.
+int launch_decode_ng96(const CUtensorMap& q_lat, const CUtensorMap& q_rope,
+                       const DecodeParams& prm, int grid, cudaStream_t stream);
 
 }  // namespace pmla

@@ -41,12 +41,15 @@ constexpr int kD = 576;             // latent entry width
 constexpr int kDV = 512;            // value width
 constexpr int kMinChunk = 256;      // auto policy: at least this many rows per CTA
 
-// Rows per group (MMA N of the QK product) for a call with max_seqlen_q * H rows per
-// request.  Fewer groups means fewer passes over the same cache rows.
+// Rows per group for a call with max_seqlen_q * H rows per request: 16, 32 or 48 (the
+// kernel with positions on the tensor-memory lanes, rows on the MMA's N), or 96 (the kernel
+// with the rows on the lanes) for more than 48.  Fewer groups means fewer passes over the
+// same cache rows.
 PMLA_HD inline int pick_group_rows(int rows_per_request) {
   if (rows_per_request <= 16) return 16;
   if (rows_per_request <= 32) return 32;
-  return 48;
+  if (rows_per_request <= 48) return 48;
+  return 96;
 }
 PMLA_HD inline int groups_for(int rows_per_request, int ng) {
   return (rows_per_request + ng - 1) / ng;

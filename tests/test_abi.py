@@ -63,9 +63,14 @@ def test_workspace_size_plan(lib):
     ng, slots = 16, 16 + 152
     plain = 256 + slots * ng * 513 * 4
     assert plain <= sz < plain + 2 * 256
-    # 96 heads -> two groups of 48 rows
+    # 96 heads -> one group of 96 rows
     sz96 = lib.mla_get_workspace_size(1, 96, 1, 0, 152)
-    assert sz96 >= (2 + 152) * 48 * 513 * 4
+    plain96 = 256 + (1 + 152) * 96 * 513 * 4
+    assert plain96 <= sz96 < plain96 + 2 * 256
+    # 128 heads -> two groups of 96 rows (the second one 32 rows deep)
+    sz128 = lib.mla_get_workspace_size(1, 128, 1, 0, 152)
+    plain128 = 256 + (2 + 152) * 96 * 513 * 4
+    assert plain128 <= sz128 < plain128 + 2 * 256
     # one split per request needs no partials
     assert lib.mla_get_workspace_size(16, 12, 1, 1, 152) == 256
     with pytest.raises(lib.MlaError):
@@ -75,13 +80,21 @@ def test_workspace_size_plan(lib):
 
 
 def test_shared_prefix_workspace_size(lib):
-    # the cascade's 48-row slots: ceil(B / 4) prefix units + B own units + SMs
+    # the cascade's 96-row slots: ceil(B / 8) prefix units + B own units + SMs
     sz = lib.mla_get_shared_prefix_workspace_size(16, 12, 1, 152)
-    cascade = 256 + (4 + 16 + 152) * 48 * 513 * 4
+    cascade = 256 + (2 + 16 + 152) * 96 * 513 * 4
     assert cascade <= sz < cascade + 2 * 256
     assert sz > lib.mla_get_workspace_size(16, 12, 1, 0, 152)
+    # 48 rows a request: groups of two
+    sz48 = lib.mla_get_shared_prefix_workspace_size(64, 12, 4, 152)
+    cascade48 = 256 + (32 + 64 + 152) * 96 * 513 * 4
+    assert cascade48 <= sz48 < cascade48 + 2 * 256
+    # four or more but fewer than eight 12-row requests: the 48-row cascade, groups of four
+    sz4 = lib.mla_get_shared_prefix_workspace_size(5, 12, 1, 152)
+    cascade4 = 256 + (2 + 5 + 152) * 48 * 513 * 4
+    assert cascade4 <= sz4 < cascade4 + 2 * 256
     # batches that never take the shared-prefix path need only the plain workspace
-    for B, H, T in [(3, 12, 1), (1, 12, 1), (64, 12, 4), (16, 96, 1)]:
+    for B, H, T in [(3, 12, 1), (1, 12, 1), (64, 16, 4), (16, 96, 1)]:
         assert (lib.mla_get_shared_prefix_workspace_size(B, H, T, 152) ==
                 lib.mla_get_workspace_size(B, H, T, 0, 152))
 

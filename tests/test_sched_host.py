@@ -68,7 +68,13 @@ def sim():
 
 
 def pick_ng(rows):
-    return 16 if rows <= 16 else (32 if rows <= 32 else 48)
+    return 16 if rows <= 16 else (32 if rows <= 32 else (48 if rows <= 48 else 96))
+
+
+def cascade_ng(rows, B):
+    """The shared-prefix cascade's group rows as the library picks them: 96 when a group of
+    at least two requests fits and the batch fills one, else 48."""
+    return 96 if rows <= 48 and B >= 96 // rows else 48
 
 
 def host_costs(sim, mode, NG, rows):
@@ -279,11 +285,12 @@ def check_cascade(sim, kv_lens, q_lens, H, grid, shared, costs="none"):
     kvp = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
     qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     rows = max(q_lens) * H
-    gsize = 48 // rows
+    NG = cascade_ng(rows, B)
+    gsize = NG // rows
     P = shared
     VP = (B + gsize - 1) // gsize
-    cw = resolve_costs(sim, costs, 1, 48, rows)
-    pieces = cascade_pieces(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared, cw)
+    cw = resolve_costs(sim, costs, 1, NG, rows)
+    pieces = cascade_pieces(sim, kvp, qop, B, H, NG, 1, grid, 1, gsize, shared, cw)
     n_slots = sim.sched_partial_slots(VP + B, 1, 0, grid)
     cover = {}
     for cta, v, g, j0, j1, prow, slot, direct, kv0, cfrom in pieces:
@@ -308,7 +315,7 @@ def check_cascade(sim, kv_lens, q_lens, H, grid, shared, costs="none"):
             assert j0 == pos, f"gap/overlap in unit {v}"
             pos = j1
         assert pos == max(L, 0)
-        need, first, count = cascade_partials(sim, kvp, qop, B, H, 48, 1, grid, 1, gsize, shared,
+        need, first, count = cascade_partials(sim, kvp, qop, B, H, NG, 1, grid, 1, gsize, shared,
                                               v, 0, cw)
         if L <= 0:
             assert need == 0
@@ -325,6 +332,8 @@ CASCADE_CASES = [
     ([3000, 2500, 4000, 2200, 2600], [1] * 5, 12, 2200),  # one request ends with the prefix
     ([9000] * 4, [2] * 4, 12, 8999),                      # two queries per request
     ([12000] * 7, [1] * 7, 8, 5000),                      # 8 heads: groups of 6 requests
+    ([6000, 6100, 5900, 7000, 6500], [4] * 5, 12, 5000),  # 48 rows: 96-row groups of 2
+    ([3000 + 11 * i for i in range(9)], [1] * 9, 12, 2048),   # 96-row groups: 8 + 1
 ]
 
 
@@ -455,7 +464,8 @@ def check_cascade_paged(sim, kv_lens, q_lens, H, grid, shared, page_size, costs=
     kvp, last = _paged_csr(kv_lens, page_size)
     qop = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     rows = max(q_lens) * H
-    gsize = 48 // rows
+    NG = cascade_ng(rows, B)
+    gsize = NG // rows
     P = shared
     VP = (B + gsize - 1) // gsize
     lg = page_size.bit_length() - 1
@@ -464,7 +474,7 @@ def check_cascade_paged(sim, kv_lens, q_lens, H, grid, shared, page_size, costs=
     out = np.zeros(cap * 10, dtype=np.int64)
     # mode 2: the paged cascade the library launches on pages of several tokens
     mode = 2 if page_size > 1 else 1
-    args = (kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, 48, 1, 0, grid, mode, gsize,
+    args = (kvp.ctypes.data_as(i32p), qop.ctypes.data_as(i32p), B, H, NG, 1, 0, grid, mode, gsize,
             shared, *costs, lg, last.ctypes.data_as(i32p))
     n = sim.sched_pieces_full(*args, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cap)
     assert n >= 0
