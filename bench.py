@@ -63,11 +63,11 @@ NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "m
 # What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
 # HBM copy peak, but not every call is HBM-bound.
 LIMITER = {
-    "c16+shared_prefix": "the 48-row tile pipeline: a ring stage is refilled only after its "
-                         "PV, and the row copies (~0.7 us to issue 96 rows) plus their "
-                         "arrival take longer than the two tiles in between, so the MMA warp "
-                         "waits ~0.4 us a tile for rows after issuing its 30 MMAs at the "
-                         "lone-warp rate; plus the cascade merge; DRAM ~23 % busy "
+    "c16+shared_prefix": "the 96-row tile pipeline: 34 MMAs per 64-position tile (~0.86 us, "
+                         "each bound by the shared-memory bytes it reads) plus ~0.4 us of "
+                         "barrier polls and bookkeeping in the issuing warp, the 12-row own "
+                         "units paying a full tile's MMAs; the epilogue of 96-row fp32 "
+                         "partials (~6.4 us) and the cascade merge; DRAM ~22 % busy "
                          "(profiles/mla_decode_c16.md)",
     "c24+shared_prefix": "as c16+shared_prefix",
     "c16": "the 16-row tile pipeline while every request gathers the shared prefix (L2 "
@@ -79,6 +79,10 @@ LIMITER = {
             "(profiles/mla_decode_long.md)",
     "mtp": "one ring stage's round trip (row copies, QK, softmax, PV) at three stages in "
            "flight; DRAM 65 % busy (profiles/mla_decode_mtp.md)",
+    "long96": "the 96-row tile pipeline (one pass over the cache for all 96 heads): 34 MMAs "
+              "per 64-position tile plus the issuing warp's bookkeeping, ~15 tiles per CTA; "
+              "the epilogue of 96-row fp32 partials (~6.4 us) and the merge "
+              "(profiles/mla_decode_long96.md)",
 }
 
 

@@ -1,7 +1,7 @@
 """Parity of the CUDA decode path (through the C ABI) with the FP64 oracle.
 
 Small cases are compared element by element; they span several 128-position tiles, a
-ragged tail, every row-group size (16 / 32 / 48 rows), causal drafts, split policies and
+ragged tail, every row-group size (16 / 32 / 48 / 96 rows), causal drafts, split policies and
 poisoned memory.  Full-size workloads are checked on sampled outputs and invariants.
 """
 import math
@@ -132,7 +132,8 @@ def test_shared_prefix_cascade_many_requests(pm):
 
 @pytest.mark.parametrize("H", [16, 24, 40, 96])
 def test_head_counts(pm, H):
-    """16 -> one 16-row group, 24 -> 32-row group, 40 -> 48-row group, 96 -> two 48-row groups."""
+    """16 -> one 16-row group, 24 -> 32-row group, 40 -> 48-row group, 96 -> one 96-row group
+    (the kernel with the query rows on the tensor-memory lanes)."""
     case = mla_inputs.make_custom([1500, 333], H=H, seed=5, q_scale=1.0, kv_scale=1.0, name=f"H{H}")
     _check(case)
 
