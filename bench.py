@@ -37,6 +37,7 @@ METRIC = "MLA decode effective KV-cache GB/s (% of GB300 HBM peak) and µs per d
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD_TEXT = {
     "tiny": "tiny decode: batch 2, 12 heads, q_len 1, kv_lens {256, 300}, 1,024-row fp8 pool",
     "c16": "concurrency-16 decode: batch 16, 12 heads, q_len 1, 63,911 shared-prefix + 4,089 "
@@ -318,11 +319,40 @@ def time_graph(call, steps, warmup, flush, no_flush, stream, dev, eager, salt=0)
     return sum(a.elapsed_time(b) for a, b in ev) / steps, graph
 
 
+# What binds each call's decode kernel, from its timeline and ncu captures (profiles/): the
+# HBM roofline below is the contract's, but not every call is HBM-bound.
+BINDS = {
+    "c16+shared_prefix": "tensor-core MMA stream (96-row kernel: 34 MMAs a 64-position tile, "
+                         "each bound by the shared-memory operand bytes it reads)",
+    "c24+shared_prefix": "tensor-core MMA stream (96-row kernel)",
+    "c16p128+shared_prefix": "tensor-core MMA stream (96-row kernel)",
+    "long96": "tensor-core MMA stream (96-row kernel)",
+    "c16": "row-copy issue and the ring's refill (16-row kernel; the shared rows from L2)",
+    "c24": "row-copy issue and the ring's refill (16-row kernel; the shared rows from L2)",
+    "c16p128": "row-copy issue and the ring's refill (16-row kernel)",
+    "long": "fixed per-call latencies around ~8 streamed tiles per CTA",
+    "longp128": "fixed per-call latencies around ~8 streamed tiles per CTA",
+    "mtp": "the 48-row ring's round trip, DRAM 66 % busy",
+}
+# FP8 dense tensor peak: the measured bf16 cuBLAS burst times the nominal fp8 : bf16 ratio
+# (4.5 : 2.25 PFLOP/s).
+FP8_OVER_BF16 = 2.0
+
+
+def measured_fp8_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]) * FP8_OVER_BF16, "measured bf16 burst x 2"
+    return FALLBACK_BF16_TFLOPS * FP8_OVER_BF16, "fallback bf16 burst x 2"
+
+
 def roofline_for(case, entry, ms, peak, peak_kind, config, shared):
     """Roofline of one decode call: algorithmic bytes / device time against the HBM copy
     peak.  A shared-prefix call (and any call on pages, whose shared pages are the same
     memory) counts the shared rows once; the plain call on a shared-prefix batch is given
-    both readings."""
+    both readings.  Beside it, the same call's algorithmic FP8 work (2 x (576 + 512) flops
+    per attended row and position) against the FP8 tensor peak, and what binds the call."""
     paged = int(case.meta.get("page_size", 1)) > 1
     distinct = mla_inputs.algorithmic_bytes(case, shared if (entry == "shared_prefix" or paged) else 0)
     r = {"bound": "hbm", "achieved": distinct / (ms * 1e-3) / 1e9, "peak": peak,
@@ -330,6 +360,13 @@ def roofline_for(case, entry, ms, peak, peak_kind, config, shared):
          "traffic": recorded_traffic(config, entry),
          "algorithmic_bytes": distinct}
     r["frac"] = r["achieved"] / peak
+    key = f"{config}+{entry}" if entry == "shared_prefix" else config
+    r["binds"] = BINDS.get(key)
+    flops = mla_inputs.useful_flops(case.kv_lens, case.q_lens, case.H)
+    tpeak, tkind = measured_fp8_tflops()
+    ach = flops / (ms * 1e-3) / 1e12
+    r["tensor_roofline"] = {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s",
+                            "peak_kind": tkind, "frac": ach / tpeak, "algorithmic_flops": flops}
     if entry == "shared_prefix":
         r["kernel"] = ("mla_decode_shared_prefix call (one cascade decode launch: prefix units "
                        "then per-request units, then the cascade merge)")
