@@ -22,7 +22,8 @@
 //   * A ring of four 64-position stages (shared memory: 4 x 36 KB of rows, 54 KB of q, two
 //     P buffers of 12 KB).
 //
-// Warps: 0-3 and 5-7 gather rows as in mla_decode_kernel; warp 4 issues the MMAs; warps
+// Warps: 0-2 and 5-7 gather rows as in mla_decode_kernel; warp 4 issues the QKs and warp 3
+// the PVs (two issuers, so that one's waits overlap the other's MMAs); warps
 // 8-15 are two softmax warpgroups: warp 8 + 4 h + q handles query rows 32 q .. 32 q + 31
 // (TMEM lane quadrant q; q = 3 holds no rows) over positions 32 h .. 32 h + 31 of each tile,
 // one row per thread, so a row's maximum and sum need no shuffles: the two halves exchange
@@ -63,9 +64,10 @@ struct Rows96Layout {
   static constexpr int kPv = 96;        // pv_done[2]
   static constexpr int kQFull = 112;
   static constexpr int kQEmpty = 120;
-  static constexpr int kDrain = 128;
+  static constexpr int kDrain = 128;     // QK issuer's MMAs done
   static constexpr int kTmemSlot = 136;
   static constexpr int kAbort = 140;
+  static constexpr int kDrainPv = 144;   // PV issuer's MMAs done
   static constexpr int kRowOff = 192;                  // int64 output offset [NG]
   static constexpr int kXch = kRowOff + 8 * NG;        // float [tile parity][half][NG]
   static constexpr int kAlpha = kXch + 16 * NG;        // float rescale factor [NG]
@@ -87,7 +89,11 @@ struct Rows96Layout {
   static constexpr int kTmemCols = 512;
   static_assert(kSfLo + 8 <= kTmemCols, "tensor memory overflow");
   static constexpr int kThreads = 512;                 // 16 warps
-  static constexpr int kRowsPerProducer = (kTile + 6) / 7;   // 10
+  // Warps 0-2 and 5-7 gather rows, warp 4 issues QK, warp 3 issues PV.
+  static constexpr int kProducers = 6;
+  static constexpr int kQkWarp = 4;
+  static constexpr int kPvWarp = 3;
+  static constexpr int kRowsPerProducer = (kTile + kProducers - 1) / kProducers;   // 11
   // setmaxnreg: warpgroups 0-1 (producers, issuer) give registers to warpgroups 2-3
   static constexpr int kRegsLow = 96;
   static constexpr int kRegsHigh = 160;
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(mbase + LY::kFull + 8 * s, kProducerThreads);
+      mbar_init(mbase + LY::kFull + 8 * s, 32 * LY::kProducers);
       mbar_init(mbase + LY::kEmpty + 8 * s, 1);
     }
     mbar_init(mbase + LY::kSFull, 1);
@@ -170,11 +176,12 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
     mbar_init(mbase + LY::kQFull, 1);
     mbar_init(mbase + LY::kQEmpty, 1);
     mbar_init(mbase + LY::kDrain, 1);
+    mbar_init(mbase + LY::kDrainPv, 1);
     *abort_flag = 0;
     fence_mbar_init();
     issue_q_load<NG>(sQ, &tm_q_lat, &tm_q_rope, first_qrow, mbase + LY::kQFull);
   }
-  if (warp == kMmaWarp) {
+  if (warp == LY::kQkWarp) {
     tmem_alloc(smem_u32(misc + LY::kTmemSlot), LY::kTmemCols);
     tmem_relinquish();
   }
@@ -313,6 +320,11 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
               lw[k >> 2] |= lo << 16;
             }
           }
+          // the buffer's previous tile (it_g - 2) must have been read by its PV: the PV
+          // issuer is not ordered with the QK that signalled this tile's logits
+          if (it_g >= 2)
+            mbar_wait_test_first(mbase + LY::kPv + 8 * (it_g & 1), ((it_g - 2) >> 1) & 1,
+                                 abort_flag, prm.err);
           uint8_t* pb = prow + (it_g & 1) * 2 * LY::kPPlane;
           *reinterpret_cast<uint4*>(pb) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(pb + LY::kPChunk) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
@@ -424,12 +436,12 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LY::kRegsLow));
-    if (warp != kMmaWarp) {
-      // ===================================================== producers (7 warps)
-      // As in mla_decode_kernel: producer pw copies tile rows r = pw + 7 j (j < rows_w), lane
+    if (warp != LY::kQkWarp && warp != LY::kPvWarp) {
+      // ===================================================== producers (6 warps)
+      // As in mla_decode_kernel: producer pw copies tile rows r = pw + 6 j (j < rows_w), lane
       // j loads row j's id; 16-byte cp.async into the 128-byte (latent) / 64-byte (rope)
       // swizzled layouts.
-      const int pw = warp < kMmaWarp ? warp : warp - 1;
+      const int pw = warp < LY::kPvWarp ? warp : warp - 2;
       uint32_t it_g = 0;
       int n_piece = 0;
       int q_loads = 0;
@@ -440,7 +452,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
       const int smask = (1 << lg) - 1;
       const int64_t ppitch = prm.page_pitch;
       const int64_t spitch = prm.kv_pitch;
-      const int rows_w = (LY::kTile - pw + kProducerWarps - 1) / kProducerWarps;   // 10 / 9
+      const int rows_w = (LY::kTile - pw + LY::kProducers - 1) / LY::kProducers;   // 11 / 10
       while (!aborted && iter.next(pc, &bad)) {
         const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
         if (warp == 0 && lane == 0) {
@@ -459,7 +471,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
         const int64_t kvbase = pc.kv0;
         auto load_row = [&](int t, int j) -> int64_t {
           if (j >= rows_w) return -1;
-          const int pos = pc.j0 + t * LY::kTile + pw + kProducerWarps * j;
+          const int pos = pc.j0 + t * LY::kTile + pw + LY::kProducers * j;
           if (pos >= pc.j1) return -1;
           const int64_t gi = kvbase + (pos >> lg);
           if (gi < 0 || gi >= prm.kv_indices_len) {
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
           const int64_t rid = nxt >= 0 ? nxt : 0;
           if (t + 1 < nt) nxt = load_row(t + 1, lane);
           if (t + 2 < nt && lane < rows_w) {
-            const int pos2 = pc.j0 + (t + 2) * LY::kTile + pw + kProducerWarps * lane;
+            const int pos2 = pc.j0 + (t + 2) * LY::kTile + pw + LY::kProducers * lane;
             const int64_t gi = kvbase + (pos2 >> lg);
             if (gi >= 0 && gi < prm.kv_indices_len && pos2 < pc.j1) prefetch_l1(prm.kv_indices + gi);
           }
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < LY::kRowsPerProducer; ++j) {
               if (j < rows_w) {
-                const int r = pw + kProducerWarps * j;
+                const int r = pw + LY::kProducers * j;
                 const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
                 cp_async_16(dst, kv + offs[j] + 16 * lane, ((vmask >> j) & 1u) << 4);
               }
@@ -512,7 +524,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
           } else {
 #pragma unroll 5
             for (int j = 0; j < rows_w; ++j) {
-              const int r = pw + kProducerWarps * j;
+              const int r = pw + LY::kProducers * j;
               const int64_t off = __shfl_sync(0xffffffffu, rid, j);
               const uint32_t dst = st + blk + r * 128 + ((chunk ^ (r & 7)) << 4);
               cp_async_16(dst, kv + off + 16 * lane, ((vmask >> j) & 1u) << 4);
@@ -524,7 +536,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
             const int c = lane & 3;
             const int64_t off = __shfl_sync(0xffffffffu, rid, j);
             if (j < rows_w) {
-              const int r = pw + kProducerWarps * j;
+              const int r = pw + LY::kProducers * j;
               const uint32_t dst = st + LY::kRopeOff + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
               cp_async_16(dst, kv + off + 512 + 16 * c, ((vmask >> j) & 1u) << 4);
             }
@@ -538,88 +550,33 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
         mbar_wait_drain(mbase + LY::kQFull, (q_loads - 1) & 1);
       __syncwarp();
     } else {
-      // ===================================================== MMA issuer (one warp)
-      // Order: QK(0), QK(1), PV(0), QK(2), PV(1), ... (CTA-wide tile numbers).  QK(i) needs
-      // its stage's rows, the piece's q rows and S read by every softmax warp of tile i - 1
-      // (one S buffer); PV(i) needs P(i).  Every wait is bounded.
-      {
-        // (a phase seen complete by any lane is complete for all: only this warp's progress
-        // can complete the next one)
-        auto wait1 = [&](uint32_t bar_, uint32_t parity) -> bool {
-          if (__any_sync(0xffffffffu, mbar_test(bar_, parity))) return true;
-          return warp_bcast(mbar_wait(bar_, parity, abort_flag, prm.err));
-        };
+      // ===================================================== MMA issuers (two warps)
+      // Warp 4 issues QK(0), QK(1), ... and warp 3 PV(0), PV(1), ... (CTA-wide tile
+      // numbers), each waiting (bounded) only for its own inputs: QK(i) for its stage's rows,
+      // the piece's q rows and S read by every softmax warp of tile i - 1 (one S buffer);
+      // PV(i) for P(i), which implies QK(i) done.  The tensor pipe takes MMAs from both: one
+      // warp's barrier polls and bookkeeping overlap the other's MMAs (one warp issuing both
+      // left the pipe idle ~30 % of each tile).  A probe measured the same MMA throughput from
+      // two issuing warps as from one.
+      // (a phase seen complete by any lane is complete for all: only this warp's progress
+      // can complete the next one)
+      auto wait1 = [&](uint32_t bar_, uint32_t parity) -> bool {
+        if (__any_sync(0xffffffffu, mbar_test(bar_, parity))) return true;
+        return warp_bcast(mbar_wait(bar_, parity, abort_flag, prm.err));
+      };
+      Piece pc;
+      uint32_t i = 0;
+      bool ok = true;
+      if (warp == LY::kQkWarp) {
         constexpr uint32_t idesc_qk = idesc_f8(128, LY::kTile, false, false);
-        constexpr uint32_t idesc_pv = idesc_f8_blockscaled(128, NG, true, false);
         const uint64_t q_lat = smem_desc(sQ, 16, 1024, kSw128);
         const uint64_t q_rope = smem_desc(sQ + LY::kQRopeOff, 16, 512, kSw64);
         const uint64_t k_lat0 = smem_desc(sbase, 16, 1024, kSw128);
         const uint64_t k_rope0 = smem_desc(sbase + LY::kRopeOff, 16, 512, kSw64);
-        const uint64_t v_lat0 = smem_desc(sbase, LY::kLatBlock, 1024, kSw128);
-        // P, K-major without swizzle: 16-position chunks kPChunk apart (leading byte offset),
-        // 8-row core matrices 128 bytes apart (stride byte offset)
-        const uint64_t p_hi0 = smem_desc(sbase + LY::kPOff, LY::kPChunk, 128, kSwNone);
-        const uint32_t sfa = tmem + LY::kSfA;
-        const uint32_t sfh = tmem + LY::kSfHi;
-        const uint32_t sfl = tmem + LY::kSfLo;
-        auto issue_qk = [&](uint32_t i) {
-          const int stage = static_cast<int>(i % STAGES);
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint64_t ka = desc_at(k_lat0, stage * LY::kStageBytes);
-          const uint64_t kr = desc_at(k_rope0, stage * LY::kStageBytes);
-          const uint32_t d = tmem + LY::kSCol;
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk)   // latent columns, 32 per MMA: A = q, B = rows
-            mma_f8_warp(d, desc_at(q_lat, (kk >> 2) * LY::kQLatBlock + (kk & 3) * 32),
-                        desc_at(ka, (kk >> 2) * LY::kLatBlock + (kk & 3) * 32), idesc_qk,
-                        kk > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_f8_warp(d, desc_at(q_rope, kk * 32), desc_at(kr, kk * 32), idesc_qk, 1u);
-          mma_commit_warp(mbase + LY::kSFull);
-        };
-        auto issue_pv = [&](uint32_t i, bool first_of_piece) {
-          const int stage = static_cast<int>(i % STAGES);
-          tc_fence_after();
-          const uint64_t va = desc_at(v_lat0, stage * LY::kStageBytes);
-          const uint64_t ph = desc_at(p_hi0, (i & 1) * 2 * LY::kPPlane);
-#pragma unroll
-          for (int bk = 0; bk < 4; ++bk) {
-            const uint32_t d = tmem + LY::kOBase + bk * NG;
-#pragma unroll
-            for (int kk = 0; kk < LY::kTile / 32; ++kk) {
-              // A = V^T block bk (128 value columns x 32 positions); B = P (32 positions x
-              // NG rows), hi plane at scale 1, lo plane at scale 2^-4
-              const uint64_t a = desc_at(va, bk * LY::kLatBlock + kk * 32 * 128);
-              mma_f8_scaled_warp(d, a, desc_at(ph, kk * 2 * LY::kPChunk), idesc_pv, sfa, sfh,
-                                 (first_of_piece && kk == 0) ? 0u : 1u);
-              mma_f8_scaled_warp(d, a, desc_at(ph, LY::kPPlane + kk * 2 * LY::kPChunk), idesc_pv,
-                                 sfa, sfl, 1u);
-            }
-          }
-          mma_commit_warp(mbase + LY::kEmpty + 8 * stage);
-          mma_commit_warp(mbase + LY::kPv + 8 * (i & 1));
-        };
         int n_piece = 0;
-        Piece pc;
-        uint32_t i = 0;
-        bool pend = false;
-        uint32_t pend_j = 0;
-        bool pend_first = false;
-        bool ok = true;
-        auto pv_step = [&]() {
-          const uint32_t j = pend_j;
-          if (!wait1(mbase + LY::kPFull + 8 * (j & 1), (j >> 1) & 1)) {
-            ok = false;
-            return;
-          }
-          issue_pv(j, pend_first);
-          pend = false;
-        };
         while (ok && iter.next(pc, &bad)) {
           const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
-          for (int t = 0; t < nt && ok; ++t) {
+          for (int t = 0; t < nt && ok; ++t, ++i) {
             if (t == 0 && !wait1(mbase + LY::kQFull, n_piece & 1)) {
               ok = false;
               break;
@@ -633,19 +590,70 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
               ok = false;
               break;
             }
-            issue_qk(i);
-            if (t == nt - 1) mma_commit_warp(mbase + LY::kQEmpty);
-            if (pend) pv_step();
-            pend = true;
-            pend_j = i;
-            pend_first = (t == 0);
-            ++i;
+            // the stage was written by cp.async (generic proxy); the tensor core reads it
+            // through the async proxy
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint64_t ka = desc_at(k_lat0, stage * LY::kStageBytes);
+            const uint64_t kr = desc_at(k_rope0, stage * LY::kStageBytes);
+            const uint32_t d = tmem + LY::kSCol;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)   // latent columns, 32 per MMA: A = q, B = rows
+              mma_f8_warp(d, desc_at(q_lat, (kk >> 2) * LY::kQLatBlock + (kk & 3) * 32),
+                          desc_at(ka, (kk >> 2) * LY::kLatBlock + (kk & 3) * 32), idesc_qk,
+                          kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+              mma_f8_warp(d, desc_at(q_rope, kk * 32), desc_at(kr, kk * 32), idesc_qk, 1u);
+            mma_commit_warp(mbase + LY::kSFull);
+            if (t == nt - 1) mma_commit_warp(mbase + LY::kQEmpty);   // q may be overwritten
           }
           ++n_piece;
         }
-        if (ok && pend) pv_step();
+        // Drain: all MMAs must complete before tensor memory is released.
         mma_commit_warp(mbase + LY::kDrain);
         if (lane == 0) mbar_wait_drain(mbase + LY::kDrain, 0);
+      } else {
+        constexpr uint32_t idesc_pv = idesc_f8_blockscaled(128, NG, true, false);
+        const uint64_t v_lat0 = smem_desc(sbase, LY::kLatBlock, 1024, kSw128);
+        // P, K-major without swizzle: 16-position chunks kPChunk apart (leading byte offset),
+        // 8-row core matrices 128 bytes apart (stride byte offset)
+        const uint64_t p_hi0 = smem_desc(sbase + LY::kPOff, LY::kPChunk, 128, kSwNone);
+        const uint32_t sfa = tmem + LY::kSfA;
+        const uint32_t sfh = tmem + LY::kSfHi;
+        const uint32_t sfl = tmem + LY::kSfLo;
+        while (ok && iter.next(pc, &bad)) {
+          const int nt = (pc.j1 - pc.j0 + LY::kTile - 1) / LY::kTile;
+          for (int t = 0; t < nt && ok; ++t, ++i) {
+            if (!wait1(mbase + LY::kPFull + 8 * (i & 1), (i >> 1) & 1)) {
+              ok = false;
+              break;
+            }
+            const int stage = static_cast<int>(i % STAGES);
+            tc_fence_after();
+            const uint64_t va = desc_at(v_lat0, stage * LY::kStageBytes);
+            const uint64_t ph = desc_at(p_hi0, (i & 1) * 2 * LY::kPPlane);
+#pragma unroll
+            for (int bk = 0; bk < 4; ++bk) {
+              const uint32_t d = tmem + LY::kOBase + bk * NG;
+#pragma unroll
+              for (int kk = 0; kk < LY::kTile / 32; ++kk) {
+                // A = V^T block bk (128 value columns x 32 positions); B = P (32 positions x
+                // NG rows), hi plane at scale 1, lo plane at scale 2^-4
+                const uint64_t a = desc_at(va, bk * LY::kLatBlock + kk * 32 * 128);
+                mma_f8_scaled_warp(d, a, desc_at(ph, kk * 2 * LY::kPChunk), idesc_pv, sfa, sfh,
+                                   (t == 0 && kk == 0) ? 0u : 1u);
+                mma_f8_scaled_warp(d, a, desc_at(ph, LY::kPPlane + kk * 2 * LY::kPChunk),
+                                   idesc_pv, sfa, sfl, 1u);
+              }
+            }
+            // the stage (its QK finished before P(i) existed) and O's tile are released
+            mma_commit_warp(mbase + LY::kEmpty + 8 * stage);
+            mma_commit_warp(mbase + LY::kPv + 8 * (i & 1));
+          }
+        }
+        mma_commit_warp(mbase + LY::kDrainPv);
+        if (lane == 0) mbar_wait_drain(mbase + LY::kDrainPv, 0);
       }
       __syncwarp();
     }
@@ -653,7 +661,7 @@ __global__ void __launch_bounds__(Rows96Layout::kThreads, 1)
   if (bad && (threadIdx.x & 31) == 0) atomicOr(prm.err, kErrBadIndptr);
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == LY::kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, LY::kTmemCols);
   }
