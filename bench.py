@@ -64,12 +64,12 @@ NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "m
 # What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
 # HBM copy peak, but not every call is HBM-bound.
 LIMITER = {
-    "c16+shared_prefix": "the 96-row tile pipeline: 34 MMAs per 64-position tile (~0.86 us, "
-                         "each bound by the shared-memory bytes it reads) plus ~0.4 us of "
-                         "barrier polls and bookkeeping in the issuing warp, the 12-row own "
-                         "units paying a full tile's MMAs; the epilogue of 96-row fp32 "
-                         "partials (~6.4 us) and the cascade merge; DRAM ~22 % busy "
-                         "(profiles/mla_decode_c16.md)",
+    "c16+shared_prefix": "the 96-row tile pipeline: 34 MMAs per 64-position tile (~0.9-1 us "
+                         "of tensor pipe, each bound by the shared-memory bytes it reads) "
+                         "issued from a QK and a PV warp, the period (~1.2 us) set by the single "
+                         "S buffer's hand-off; the 12-row own units pay a full tile's MMAs; the "
+                         "epilogue of 96-row fp32 partials (~6.4 us) and the cascade merge; "
+                         "DRAM ~24 % busy (profiles/mla_decode_c16.md)",
     "c24+shared_prefix": "as c16+shared_prefix",
     "c16": "the 16-row tile pipeline while every request gathers the shared prefix (L2 "
            "serves it after the first reads): ~1.44 us per 128-position tile, the row "
@@ -81,9 +81,8 @@ LIMITER = {
     "mtp": "one ring stage's round trip (row copies, QK, softmax, PV) at three stages in "
            "flight; DRAM 65 % busy (profiles/mla_decode_mtp.md)",
     "long96": "the 96-row tile pipeline (one pass over the cache for all 96 heads): 34 MMAs "
-              "per 64-position tile plus the issuing warp's bookkeeping, ~15 tiles per CTA; "
-              "the epilogue of 96-row fp32 partials (~6.4 us) and the merge "
-              "(profiles/mla_decode_long96.md)",
+              "per 64-position tile from a QK and a PV warp, ~15 tiles per CTA; the epilogue "
+              "of 96-row fp32 partials (~6.4 us) and the merge (profiles/mla_decode_long96.md)",
 }
 
 
