@@ -59,7 +59,8 @@ SOAK_S = 1.0   # shortest span of steps the clock record covers
 
 # Sources of other operations, which the decode call never runs: left out of the hash
 # that keys the decode kernels' recorded counters.
-NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "mla_noalloc.cu"}
+NOT_DECODE_SOURCES = {"mla_vproj.cu", "mla_selftest.cu", "mla_rope_cache.cu", "mla_noalloc.cu",
+                      "mla_prefix_expand.cu"}
 
 # What binds each call, from its ncu capture (profiles/): the roofline's denominator is the
 # HBM copy peak, but not every call is HBM-bound.
@@ -697,6 +698,25 @@ def main():
         used = int(case.kv_indptr[-1])
         parts = [("q", case.q), ("qo", case.qo_indptr), ("kvp", case.kv_indptr),
                  ("idx", case.kv_indices[:used]), ("last", case.kv_last_page_lens)]
+        # The shared-prefix call's page table goes over as a prefix cache keeps it: the
+        # shared pages once, then each request's own pages; mla_expand_shared_prefix_indices
+        # builds the full table on the device inside the timed step.
+        compact = None
+        if entry == "shared_prefix":
+            ps = int(case.meta.get("page_size", 1))
+            n_sh = shared // ps
+            kvp_h = [int(x) for x in case.kv_indptr.cpu()]
+            idx_h = case.kv_indices.cpu()
+            sh_ids = idx_h[kvp_h[0]:kvp_h[0] + n_sh].clone()
+            if all(torch.equal(idx_h[kvp_h[b]:kvp_h[b] + n_sh], sh_ids) for b in range(case.B)):
+                owns = [idx_h[kvp_h[b] + n_sh:kvp_h[b + 1]] for b in range(case.B)]
+                own_ptr = [0]
+                for x in owns:
+                    own_ptr.append(own_ptr[-1] + x.numel())
+                compact = (n_sh, own_ptr[-1])
+                parts = [("q", case.q), ("qo", case.qo_indptr), ("shared", sh_ids),
+                         ("optr", torch.tensor(own_ptr, dtype=torch.int32)),
+                         ("own", torch.cat(owns)), ("last", case.kv_last_page_lens)]
         offs, tot = {}, 0
         for k, t in parts:
             offs[k] = tot
@@ -717,13 +737,20 @@ def main():
         h_out = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
         h2d = sum(t.numel() * t.element_size() for _, t in parts)
         d2h = o_bytes + lse.numel() * lse.element_size()
+        if compact is not None:
+            kvp_dev = torch.empty(case.B + 1, dtype=torch.int32, device=dev)
+            idx_dev = torch.empty(case.B * compact[0] + compact[1], dtype=torch.int32, device=dev)
+        else:
+            kvp_dev, idx_dev = d_in["kvp"], d_in["idx"]
         # the public call prepared once for these buffers (PreparedDecode), run each step
-        prep = pm.PreparedDecode(d_in["q"], case.kv, o_e, d_in["qo"], d_in["kvp"], d_in["idx"],
+        prep = pm.PreparedDecode(d_in["q"], case.kv, o_e, d_in["qo"], kvp_dev, idx_dev,
                                  d_in["last"], case.max_seqlen_q, case.sm_scale, case.q_scale,
                                  case.kv_scale, num_kv_splits=args.num_kv_splits, lse_out=lse_e,
                                  workspace=ws,
                                  shared_prefix_len=shared if entry == "shared_prefix" else None,
-                                 stream=stream)
+                                 stream=stream,
+                                 compact_page_table=(None if compact is None else
+                                                     (d_in["shared"], d_in["optr"], d_in["own"])))
         e_ms = []
         n_e2e = max(5, min(args.steps, 20))
         for i in range(n_e2e + 2):
@@ -745,7 +772,11 @@ def main():
             raise RuntimeError("end-to-end output differs from the device-timed call's")
         e_mean = max_over_ranks(sum(e_ms) / len(e_ms), dist, dev)
         e2e = {"value": whole_job_rate(world, gathered, e_mean), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_mean}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_mean,
+               "page_table": ("shared pages once + each request's own pages, expanded on the "
+                              "device (mla_expand_shared_prefix_indices, run by "
+                              "PreparedDecode) inside the step"
+                              if compact is not None else "full CSR uploaded every step")}
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -167,12 +167,12 @@ int mla_get_shared_prefix_workspace_size(int32_t batch_size, int32_t num_heads,
  *                      shared-prefix path; with less (but at least
  *                      mla_get_workspace_size(B, H, max_seqlen_q, 0, ...)) it runs the
  *                      plain decode.
- * The shared positions are attended in groups of requests (48 query rows per tile, i.e.
- * 4 requests at 12 heads and q_len 1), so each shared row is read once per group instead
- * of once per request; each request's own positions run separately and the two halves
- * are merged by their log-sum-exp.  Batches with fewer requests than one group, more
- * than 24 query rows per request, or fewer than 1024 shared positions (whole pages) run
- * the plain decode.
+ * The shared positions are attended in groups of requests (96 query rows per tile, i.e.
+ * 8 requests at 12 heads and q_len 1; 48 rows for batches of 4..7 requests of at most 24
+ * rows), so each shared row is read once per group instead of once per request; each
+ * request's own positions run separately and the two halves are merged by their
+ * log-sum-exp.  Batches with fewer requests than one group, more than 48 query rows per
+ * request, or fewer than 1024 shared positions (whole pages) run the plain decode.
  */
 int mla_decode_shared_prefix(const mla_tensor_t* q, const mla_tensor_t* kv_buffer,
                              const mla_tensor_t* o, const mla_tensor_t* qo_indptr,
@@ -182,6 +182,33 @@ int mla_decode_shared_prefix(const mla_tensor_t* q, const mla_tensor_t* kv_buffe
                              const mla_tensor_t* kv_scale, int32_t shared_prefix_len,
                              const mla_tensor_t* lse_out, void* workspace,
                              size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * The CSR page table (kv_indptr, kv_indices) of a batch whose requests share their first
+ * pages, built on the device from the compact form a prefix cache keeps: the shared pages
+ * once and each request's own pages ("[Kimi-K3 MLA TP8] MLA performance" §1 "Environment":
+ * decode batches over a shared prefix; §4.1: the page table mla_decode reads; §5.4:
+ * cross-request reuse).  A caller that uploads its page table every step moves the shared
+ * ids over the host link once instead of once per request, then calls
+ * mla_decode_shared_prefix (or mla_decode) on the result.  For request b < B:
+ *   kv_indptr[b]   = b * S + (own_indptr[b] - own_indptr[0]),   kv_indptr[B] likewise
+ *   kv_indices[kv_indptr[b] + j] = shared_indices[j]                          (j < S)
+ *                                = own_indices[own_indptr[b] + j - S]          (j >= S)
+ *   shared_indices (S,) INT32 page ids (S >= 0; with S = 0 a null pointer is allowed)
+ *   own_indptr     (B+1,) INT32, non-decreasing offsets into own_indices, own_indptr[0] >= 0
+ *   own_indices    (>= own_indptr[B],) INT32 (empty: a null pointer is allowed)
+ *   kv_indptr      (B+1,) INT32 (written)
+ *   kv_indices     INT32 (written), room for B * S + own_indptr[B] - own_indptr[0] entries
+ * All on the device; nothing is read by the host.  A request whose own_indptr entries are
+ * out of order or past own_indices is skipped (its kv_indptr entry is not written) and
+ * flags bit 2 in `error_word` (an int on the device, may be NULL); entries past the end of
+ * kv_indices are not written and flag bit 8.  B <= 65535.  Enqueued on `stream`.
+ */
+int mla_expand_shared_prefix_indices(const mla_tensor_t* shared_indices,
+                                     const mla_tensor_t* own_indptr,
+                                     const mla_tensor_t* own_indices,
+                                     const mla_tensor_t* kv_indptr, const mla_tensor_t* kv_indices,
+                                     int32_t* error_word, mla_stream_t stream);
 
 /*
  * Softmax-weighted merge of partial results ("Scaling Kimi K3 on AMD Instinct MI355X",

@@ -73,6 +73,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, P, c_i32, ctypes.c_float, P, P, c_i32, P, vp, vp]
     lib.mla_merge_partials.restype = ctypes.c_int
     lib.mla_merge_partials.argtypes = [P, P, P, P, P, P, vp, vp]
+    lib.mla_expand_shared_prefix_indices.restype = ctypes.c_int
+    lib.mla_expand_shared_prefix_indices.argtypes = [P, P, P, P, P, vp, vp]
     lib.mla_validate.restype = ctypes.c_int
     lib.mla_validate.argtypes = [P, P, P, P, P, P, vp, c_sz, vp]
     lib.mla_check_error.restype = ctypes.c_int
@@ -227,7 +229,11 @@ class PreparedDecode:
 
     def __init__(self, q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_last_page_lens,
                  max_seqlen_q, sm_scale, q_scale, kv_scale, num_kv_splits=0, lse_out=None,
-                 workspace=None, shared_prefix_len=None, stream=None):
+                 workspace=None, shared_prefix_len=None, stream=None, compact_page_table=None):
+        """compact_page_table: optional (shared_indices, own_indptr, own_indices) device
+        tensors; run() then first rebuilds kv_indptr / kv_indices from them with
+        mla_expand_shared_prefix_indices (a caller that uploads its page table every step
+        sends the shared pages once)."""
         shared = shared_prefix_len is not None
         if workspace is None:
             workspace = make_workspace(len(kv_indptr) - 1, q.shape[1], max_seqlen_q,
@@ -250,12 +256,22 @@ class PreparedDecode:
                           float(sm_scale), r[7], r[8], int(num_kv_splits), r[9]) + tail
         self._device = q.device
         self._stream = None if stream is None else _stream(stream, q.device)
+        self._expand = None
+        if compact_page_table is not None:
+            sh, optr, own = compact_page_table
+            self._expand_keep = (sh, optr, own)
+            self._expand_descs = [_desc(t) for t in (sh, optr, own)] + self._descs[4:6]
+            self._expand = tuple(_ref(d) for d in self._expand_descs) + (None,)
 
     def run(self, stream=None):
         """Enqueue the call on `stream` (default: the stream given when prepared, else
         torch's current stream)."""
         st = _stream(stream, self._device) if stream is not None else (
             self._stream if self._stream is not None else _stream(None, self._device))
+        if self._expand is not None:
+            rc = _lib.mla_expand_shared_prefix_indices(*self._expand, st)
+            if rc != 0:
+                raise MlaError(rc, "mla_expand_shared_prefix_indices")
         rc = self._fn(*self._args, st)
         if rc != 0:
             raise MlaError(rc, self._where)
@@ -287,6 +303,21 @@ def mla_decode_noalloc(q, kv_buffer, o, qo_indptr, kv_indptr, kv_indices, kv_las
                                  _ref(dks), int(num_kv_splits), _ref(dlse), ew,
                                  _stream(stream, q.device))
     _check(rc, "mla_decode_noalloc")
+
+
+def mla_expand_shared_prefix_indices(shared_indices, own_indptr, own_indices, kv_indptr,
+                                     kv_indices, error_word=None, stream=None):
+    """Build the full page table of a shared-prefix batch on the device from the shared page
+    ids (once) and each request's own ids (see include/paged_mla.h)."""
+    descs = [_desc(t) for t in (shared_indices, own_indptr, own_indices, kv_indptr, kv_indices)]
+    if error_word is not None and (not isinstance(error_word, torch.Tensor) or
+                                   error_word.dtype != torch.int32 or error_word.numel() < 1 or
+                                   error_word.device != kv_indices.device):
+        raise ValueError("error_word must be an int32 tensor on the page table's device")
+    ew = ctypes.c_void_p(error_word.data_ptr()) if error_word is not None else None
+    rc = _lib.mla_expand_shared_prefix_indices(*[_ref(d) for d in descs], ew,
+                                               _stream(stream, kv_indices.device))
+    _check(rc, "mla_expand_shared_prefix_indices")
 
 
 def mla_merge_partials(o_parts, lse_parts, reduce_indptr, reduce_idx, o, lse_out=None,

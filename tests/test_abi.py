@@ -277,3 +277,22 @@ def test_bounded_wait_selftest_rejects_bad_arguments_on_host(lib):
     assert f(word, None, 1_000_000, None) == 1
     for bad in (0, 999, 100_000_001):
         assert f(word, res, bad, None) == 1
+
+
+def test_prefix_expand_rejects_bad_arguments_before_launch(lib):
+    """Host-side checks of mla_expand_shared_prefix_indices (fake device addresses: every
+    case fails before anything is enqueued)."""
+    I32 = 4
+    base = 1 << 40
+    good = dict(shared=_t(base, I32, [10]), optr=_t(base + 4096, I32, [4]),
+                own=_t(base + 8192, I32, [30]), kvp=_t(base + 12288, I32, [4]),
+                idx=_t(base + 16384, I32, [60]))
+    def call(**kw):
+        a = dict(good, **kw)
+        return lib._lib.mla_expand_shared_prefix_indices(
+            ctypes.byref(a["shared"]), ctypes.byref(a["optr"]), ctypes.byref(a["own"]),
+            ctypes.byref(a["kvp"]), ctypes.byref(a["idx"]), None, None)
+    assert call(kvp=_t(base + 12288, I32, [5])) == 1          # kv_indptr length != own_indptr
+    assert call(optr=_t(base + 4096, 3, [4])) == 1            # own_indptr not int32
+    assert call(idx=_t(base + 16384, I32, [29])) == 1         # not even room for B x S shared ids
+    assert call(shared=_t(base + 2, I32, [10])) == 1          # misaligned
