@@ -89,3 +89,25 @@ def test_algorithmic_bytes_count_distinct_rows_under_a_shared_prefix():
     rest = rows * (576 + 1024 + 4)
     assert mla_inputs.algorithmic_bytes(case) == 580 * case.total_kv + rest
     assert mla_inputs.algorithmic_bytes(case, 256) == 580 * distinct + rest
+
+
+def test_roofline_names_the_binding_and_carries_the_tensor_view():
+    """bench.roofline_for: the HBM roofline of the scope table (580 B per attended position),
+    what binds the call, and the algorithmic FP8 work against the FP8 peak (2 x (576 + 512)
+    flops per attended row and position, drafts counted causally)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import mla_inputs
+    case = mla_inputs.make_custom([300, 410], q_lens=[1, 3], H=12, seed=4)
+    ms, peak = 0.05, 6785.2
+    r = bench.roofline_for(case, "plain", ms, peak, "measured", "c16", 0)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["frac"] == pytest.approx(mla_inputs.algorithmic_bytes(case) / (ms * 1e-3) / 1e9 / peak)
+    assert r["binds"] and "16-row kernel" in r["binds"]
+    t = r["tensor_roofline"]
+    attended = 300 + (408 + 409 + 410)            # q_len 3 over kv_len 410: causal counts
+    assert t["algorithmic_flops"] == 2 * (576 + 512) * 12 * attended
+    assert t["bound"] == "tensor" and t["unit"] == "TFLOP/s"
+    assert t["peak"] > 0 and t["frac"] == pytest.approx(t["achieved"] / t["peak"])
+    r2 = bench.roofline_for(case, "shared_prefix", ms, peak, "measured", "c16", 0)
+    assert "96-row kernel" in r2["binds"]
