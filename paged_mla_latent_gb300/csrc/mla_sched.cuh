@@ -105,8 +105,23 @@ struct SchedParams {
 // optimum at 512 to 768.  Prefix and own units take the same weight per position: with one
 // softmax warpgroup per 16 query rows a 48-row prefix tile costs what a 12-row own tile
 // does (cheaper prefix weights measured slower).
+// The cascade in 96-row groups (mla_decode_rows96.cuh) charges 256 positions a piece and a
+// prefix position 1.15 own positions: its 12-row own pieces end with a short epilogue, its
+// 96-row prefix pieces with a long one (~6.4 us), and its prefix tiles carry the full
+// softmax.  A sweep of 128 .. 512 positions and 1.0 .. 1.35 put the optimum there (c16
+// shared prefix 59.9 -> 56.4 us, c24 74.6 -> 71.7 us, the 128-token-page cascade within
+// 0.5 %).
 constexpr int kPieceCostPositions = 512;
+constexpr int kCascade96PieceCost = 256;
+constexpr int kCascade96OwnWeight = 20;      // prefix : own = 23 : 20 = 1.15
+constexpr int kCascade96PrefixWeight = 23;
 inline void sched_set_costs(SchedParams* sp, int /*rows_per_request*/) {
+  if (sp->mode != kSchedWhole && sp->NG == 96) {
+    sp->w_own = kCascade96OwnWeight;
+    sp->w_prefix = kCascade96PrefixWeight;
+    sp->piece_cost = kCascade96PieceCost * kCascade96OwnWeight;
+    return;
+  }
   sp->w_own = 1;
   sp->w_prefix = 0;   // reads as w_own
   sp->piece_cost = kPieceCostPositions;

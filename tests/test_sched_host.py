@@ -185,12 +185,16 @@ def test_schedule_covers_every_position_once(sim, kv_lens, q_lens, H, splits, gr
 
 
 def test_library_costs(sim):
-    """The weights the library sets: one per position and 512 per piece, on the plain and
-    the cascade line alike."""
+    """The weights the library sets: one per position and 512 per piece on the plain line
+    and the 48-row cascade; the cascade in 96-row groups charges 256 positions a piece and a
+    prefix position 1.15 own ones (23 : 20)."""
     assert host_costs(sim, 0, 16, 12) == (1, 0, 512)
     assert host_costs(sim, 0, 48, 48) == (1, 0, 512)
+    assert host_costs(sim, 0, 96, 96) == (1, 0, 512)
     assert host_costs(sim, 1, 48, 12) == (1, 0, 512)
     assert host_costs(sim, 1, 48, 24) == (1, 0, 512)
+    assert host_costs(sim, 1, 96, 12) == (20, 23, 256 * 20)
+    assert host_costs(sim, 2, 96, 24) == (20, 23, 256 * 20)
 
 
 @pytest.mark.parametrize("costs", ["host", (7, 11, 999)])
