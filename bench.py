@@ -70,7 +70,7 @@ LIMITER = {
                          "issued from a QK and a PV warp, the period (~1.2 us) set by the single "
                          "S buffer's hand-off; the 12-row own units pay a full tile's MMAs; the "
                          "epilogue of 96-row fp32 partials (~6.4 us) and the cascade merge; "
-                         "DRAM ~24 % busy (profiles/mla_decode_c16.md)",
+                         "DRAM ~25 % busy (profiles/mla_decode_c16.md)",
     "c24+shared_prefix": "as c16+shared_prefix",
     "c16": "the 16-row tile pipeline while every request gathers the shared prefix (L2 "
            "serves it after the first reads): ~1.44 us per 128-position tile, the row "
