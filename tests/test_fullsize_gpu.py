@@ -1,8 +1,8 @@
 """Full-size workloads, in the launch configuration bench.py times (automatic split-KV,
 bf16 o, fp32 lse, CUDA stream of the caller), checked against the oracle on every query
 token and head of every request the test names: every request of the concurrency-16/24
-batches (so every slot of every 48-row shared-prefix group), all 12 heads of the 142K-
-position request unsplit and split, all drafts and heads of the shortest, the longest and
+batches (so every slot of every shared-prefix group: 96 rows, 8 requests x 12 heads), all
+12 heads of the 142K-position request unsplit and split, all drafts and heads of the shortest, the longest and
 four more multi-token requests, and all 96 heads of the 8-shard merge.
 """
 import functools
