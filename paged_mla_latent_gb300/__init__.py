@@ -233,7 +233,9 @@ class PreparedDecode:
         """compact_page_table: optional (shared_indices, own_indptr, own_indices) device
         tensors; run() then first rebuilds kv_indptr / kv_indices from them with
         mla_expand_shared_prefix_indices (a caller that uploads its page table every step
-        sends the shared pages once)."""
+        sends the shared pages once).  The expansion's device-side errors (an own_indptr
+        that is not monotone, a table longer than kv_indices) go to the workspace's error
+        word, where mla_check_error reports them with the decode's own."""
         shared = shared_prefix_len is not None
         if workspace is None:
             workspace = make_workspace(len(kv_indptr) - 1, q.shape[1], max_seqlen_q,
@@ -261,7 +263,8 @@ class PreparedDecode:
             sh, optr, own = compact_page_table
             self._expand_keep = (sh, optr, own)
             self._expand_descs = [_desc(t) for t in (sh, optr, own)] + self._descs[4:6]
-            self._expand = tuple(_ref(d) for d in self._expand_descs) + (None,)
+            self._expand = tuple(_ref(d) for d in self._expand_descs) + (
+                ctypes.c_void_p(workspace.data_ptr()),)
 
     def run(self, stream=None):
         """Enqueue the call on `stream` (default: the stream given when prepared, else

@@ -296,3 +296,74 @@ def test_prefix_expand_rejects_bad_arguments_before_launch(lib):
     assert call(optr=_t(base + 4096, 3, [4])) == 1            # own_indptr not int32
     assert call(idx=_t(base + 16384, I32, [29])) == 1         # not even room for B x S shared ids
     assert call(shared=_t(base + 2, I32, [10])) == 1          # misaligned
+
+
+class _RecordingLib:
+    """Stands in for the C library: records each entry point's arguments."""
+
+    def __init__(self, expand_rc=0):
+        self.calls = []
+        self.expand_rc = expand_rc
+
+    def mla_expand_shared_prefix_indices(self, *args):
+        self.calls.append(("expand", args))
+        return self.expand_rc
+
+    def mla_decode_shared_prefix(self, *args):
+        self.calls.append(("decode", args))
+        return 0
+
+
+def _prepared_with_compact_table(pm):
+    import torch
+    B, H, n_sh = 2, 12, 5
+    own_lens = [3, 4]
+    t = {
+        "q": torch.zeros(B, H, 576, dtype=torch.uint8),
+        "kv": torch.zeros(64, 576, dtype=torch.uint8),
+        "o": torch.zeros(B, H, 512, dtype=torch.bfloat16),
+        "qo": torch.arange(B + 1, dtype=torch.int32),
+        "kvp": torch.zeros(B + 1, dtype=torch.int32),
+        "idx": torch.zeros(B * n_sh + sum(own_lens), dtype=torch.int32),
+        "last": torch.ones(B, dtype=torch.int32),
+        "qs": torch.ones(1, dtype=torch.float32),
+        "ks": torch.ones(1, dtype=torch.float32),
+        "lse": torch.zeros(B, H, dtype=torch.float32),
+        "ws": torch.zeros(4096, dtype=torch.uint8),
+        "shared": torch.arange(n_sh, dtype=torch.int32),
+        "optr": torch.tensor([0, 3, 7], dtype=torch.int32),
+        "own": torch.arange(10, 17, dtype=torch.int32),
+    }
+    prep = pm.PreparedDecode(t["q"], t["kv"], t["o"], t["qo"], t["kvp"], t["idx"], t["last"], 1,
+                             192 ** -0.5, t["qs"], t["ks"], lse_out=t["lse"], workspace=t["ws"],
+                             shared_prefix_len=n_sh, stream=0,
+                             compact_page_table=(t["shared"], t["optr"], t["own"]))
+    return prep, t
+
+
+def test_prepared_decode_expands_into_the_workspace_error_word(lib, monkeypatch):
+    """PreparedDecode with a compact page table: run() enqueues the expansion first, with
+    the page-table tensors it was given and the workspace's error word (so mla_check_error
+    reports a failed expansion), then the decode, both on the same stream."""
+    fake = _RecordingLib()
+    monkeypatch.setattr(lib, "_lib", fake)
+    prep, t = _prepared_with_compact_table(lib)
+    prep.run()
+    assert [c[0] for c in fake.calls] == ["expand", "decode"]
+    ex, dec = fake.calls[0][1], fake.calls[1][1]
+    ptrs = [a._obj.ptr for a in ex[:5]]
+    assert ptrs == [t[k].data_ptr() for k in ("shared", "optr", "own", "kvp", "idx")]
+    assert ex[5].value == t["ws"].data_ptr()
+    assert dec[-3].value == t["ws"].data_ptr()
+    assert dec[-2].value == t["ws"].numel()
+    assert ex[6].value == dec[-1].value
+
+
+def test_prepared_decode_stops_when_the_expansion_is_rejected(lib, monkeypatch):
+    """A host-side rejection of the expansion raises and enqueues no decode."""
+    fake = _RecordingLib(expand_rc=1)
+    monkeypatch.setattr(lib, "_lib", fake)
+    prep, _ = _prepared_with_compact_table(lib)
+    with pytest.raises(lib.MlaError):
+        prep.run()
+    assert [c[0] for c in fake.calls] == ["expand"]
